@@ -1,0 +1,268 @@
+"""Plain fp64 CPU oracle for the fused-chain hot path -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg import this package.  The product library never loads it, and it imports
+nothing from the product: it has its own spec parser (below), its own dtype
+conversions and its own arithmetic (``oracle.c``).
+
+What each function follows is cited in ``oracle.c``.  The spec language read
+here is the one the library's ``fuse_compile`` accepts::
+
+    [shuffle:G;]op;op;...     op = add | mul | scale:<c> | relu | sigmoid
+                                   | exp | cast:f16 | cast:f32 | cast:bf16
+
+Reading of the multi-input chain of "DeepJIT" section 4.1 ((a + b) -> relu ->
+scale -> + c): ``add`` and ``mul`` each consume the next input tensor, which
+has the chain's current dtype; ``scale`` multiplies by an fp32 constant.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import struct
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+F32, F16, BF16 = 0, 1, 2
+DTYPE_CODES = {"f32": F32, "f16": F16, "bf16": BF16}
+DTYPE_NAMES = {v: k for k, v in DTYPE_CODES.items()}
+STORAGE = {F32: np.float32, F16: np.uint16, BF16: np.uint16}
+
+OP_ADD, OP_MUL, OP_SCALE, OP_RELU, OP_SIGMOID, OP_EXP, OP_CAST = 1, 2, 3, 4, 5, 6, 7
+_UNARY = {"relu": OP_RELU, "sigmoid": OP_SIGMOID, "exp": OP_EXP}
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (plain -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-std=c11",
+                               "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        P, I64, I, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        L.oracle_round_f16.restype = D
+        L.oracle_round_f16.argtypes = [D]
+        L.oracle_round_bf16.restype = D
+        L.oracle_round_bf16.argtypes = [D]
+        L.oracle_round_f32.restype = D
+        L.oracle_round_f32.argtypes = [D]
+        L.oracle_store.argtypes = [P, I64, I, P]
+        L.oracle_load.argtypes = [P, I, I64, P]
+        L.oracle_chain_eval.argtypes = [I, P, P, P, P, P, I64, P, I, P, P]
+        L.oracle_chain_check.restype = I64
+        L.oracle_chain_check.argtypes = [I, P, P, P, P, P, I64, P, I, P, P, I, P, P]
+        L.oracle_channel_shuffle.argtypes = [P, P, I64, I64, I64, I64, I, I]
+        L.oracle_rmsnorm_residual.argtypes = [P, P, P, I, I64, I64, ctypes.c_float, P, P]
+        L.oracle_rope_qkv_split.argtypes = [P, I, I64, I, I, P, D, P, P, P, P, P]
+        L.oracle_detect_decode.argtypes = [P, I, P, P, P, I, I, I, P, P]
+        _lib = L
+    return _lib
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---------------------------------------------------------------- dtypes
+
+def to_double(raw: np.ndarray, dt: int) -> np.ndarray:
+    """Exact binary64 value of stored elements (fp32 array, or uint16 bits)."""
+    raw = np.ascontiguousarray(raw)
+    out = np.empty(raw.size, np.float64)
+    lib().oracle_load(_p(raw), dt, raw.size, _p(out))
+    return out.reshape(raw.shape)
+
+
+def store(values: np.ndarray, dt: int) -> np.ndarray:
+    """Round binary64 values to dtype dt (nearest-even) and return the storage."""
+    v = _c(values, np.float64)
+    out = np.empty(v.size, STORAGE[dt])
+    lib().oracle_store(_p(v), v.size, dt, _p(out))
+    return out.reshape(v.shape)
+
+
+def round_f16(x: float) -> float:
+    return lib().oracle_round_f16(float(x))
+
+
+def round_bf16(x: float) -> float:
+    return lib().oracle_round_bf16(float(x))
+
+
+def round_f32(x: float) -> float:
+    return lib().oracle_round_f32(float(x))
+
+
+# ---------------------------------------------------------------- chains
+
+@dataclass
+class Chain:
+    ops: list            # op codes
+    args: list           # scale constant (fp32 value) or cast target dtype
+    in_idx: list         # input consumed by add/mul (else 0)
+    in_dtypes: list      # dtype of every input tensor, input 0 first
+    out_dtype: int
+    groups: int          # ChannelShuffle groups on input 0 (0 = none)
+
+
+def _f32(x: float) -> float:
+    return struct.unpack("<f", struct.pack("<f", x))[0]
+
+
+def parse_spec(spec: str, in_dtype: int) -> Chain:
+    """Read a spec into op codes, following the dtype through the casts."""
+    ops, args, in_idx, in_dtypes = [], [], [], [in_dtype]
+    groups, cur = 0, in_dtype
+    items = [s.strip() for s in spec.split(";") if s.strip()]
+    for pos, item in enumerate(items):
+        name, _, arg = item.partition(":")
+        if name == "shuffle":
+            if pos != 0:
+                raise ValueError("shuffle must come first")
+            groups = int(arg)
+            if groups <= 0:
+                raise ValueError("shuffle groups must be positive")
+            continue
+        if name in ("add", "mul"):
+            ops.append(OP_ADD if name == "add" else OP_MUL)
+            args.append(0.0)
+            in_idx.append(len(in_dtypes))
+            in_dtypes.append(cur)
+        elif name == "scale":
+            ops.append(OP_SCALE)
+            args.append(_f32(float(arg)))
+            in_idx.append(0)
+        elif name in _UNARY:
+            ops.append(_UNARY[name])
+            args.append(0.0)
+            in_idx.append(0)
+        elif name == "cast":
+            cur = DTYPE_CODES[arg]
+            ops.append(OP_CAST)
+            args.append(float(cur))
+            in_idx.append(0)
+        else:
+            raise ValueError(f"unknown op {item!r}")
+    return Chain(ops, args, in_idx, in_dtypes, cur, groups)
+
+
+def _chain_arrays(ch: Chain, inputs, shape):
+    ins = [np.ascontiguousarray(a) for a in inputs]
+    if len(ins) != len(ch.in_dtypes):
+        raise ValueError(f"chain takes {len(ch.in_dtypes)} inputs, got {len(ins)}")
+    ptrs = (ctypes.c_void_p * len(ins))(*[a.ctypes.data for a in ins])
+    ops = np.array(ch.ops or [0], np.int32)
+    args = np.array(ch.args or [0.0], np.float64)
+    idx = np.array(ch.in_idx or [0], np.int32)
+    dts = np.array(ch.in_dtypes, np.int32)
+    nchw = np.array(list(shape) if ch.groups else [1, 1, 1, 1], np.int64)
+    return ins, ptrs, ops, args, idx, dts, nchw
+
+
+def chain_eval(spec: str, in_dtype: int, inputs, shape, idx=None):
+    """Exact value (binary64) of each output element, before the final store.
+
+    inputs: storage arrays (input 0 first); shape: the tensor shape (NCHW when
+    the spec starts with shuffle); idx: optional output indices to evaluate.
+    Returns (values, out_dtype)."""
+    ch = parse_spec(spec, in_dtype)
+    ins, ptrs, ops, args, iidx, dts, nchw = _chain_arrays(ch, inputs, shape)
+    n = int(np.prod(shape)) if idx is None else len(idx)
+    sel = None if idx is None else _c(idx, np.int64)
+    out = np.empty(n, np.float64)
+    lib().oracle_chain_eval(len(ch.ops), _p(ops), _p(args), _p(iidx), ptrs, _p(dts), n,
+                            _p(sel), ch.groups, _p(nchw), _p(out))
+    return out, ch.out_dtype
+
+
+def chain_check(spec: str, in_dtype: int, inputs, shape, device_out, idx=None):
+    """Classify device results: returns (fails, counts[4], classes).
+
+    classes: 0 flat tolerance, 1 running error bound, 2 fail, 3 unpinned."""
+    ch = parse_spec(spec, in_dtype)
+    ins, ptrs, ops, args, iidx, dts, nchw = _chain_arrays(ch, inputs, shape)
+    dev = np.ascontiguousarray(device_out).reshape(-1)
+    if dev.dtype != STORAGE[ch.out_dtype]:
+        raise ValueError("device output storage does not match the chain's output dtype")
+    n = dev.size
+    sel = None if idx is None else _c(idx, np.int64)
+    cls = np.empty(n, np.int8)
+    counts = np.zeros(4, np.int64)
+    fails = lib().oracle_chain_check(len(ch.ops), _p(ops), _p(args), _p(iidx), ptrs, _p(dts), n,
+                                     _p(sel), ch.groups, _p(nchw), _p(dev), ch.out_dtype,
+                                     _p(cls), _p(counts))
+    return int(fails), counts, cls
+
+
+# ---------------------------------------------------------------- fixed ops
+
+def channel_shuffle(x: np.ndarray, groups: int) -> np.ndarray:
+    """ChannelShuffle of an NCHW array, element bytes copied unchanged."""
+    x = np.ascontiguousarray(x)
+    n, c, h, w = x.shape
+    if c % groups:
+        raise ValueError("channels must divide by groups")
+    out = np.empty_like(x)
+    lib().oracle_channel_shuffle(_p(x), _p(out), n, c, h, w, groups, x.itemsize)
+    return out
+
+
+def rmsnorm_residual(x, res, w, dt: int, eps: float):
+    """Returns (y, residual_out) in binary64, shaped like x."""
+    x, res, w = (np.ascontiguousarray(a) for a in (x, res, w))
+    rows, hidden = x.shape
+    y = np.empty((rows, hidden), np.float64)
+    r = np.empty((rows, hidden), np.float64)
+    lib().oracle_rmsnorm_residual(_p(x), _p(res), _p(w), dt, rows, hidden, ctypes.c_float(eps),
+                                  _p(y), _p(r))
+    return y, r
+
+
+def rope_qkv_split(qkv, dt: int, heads: int, head_dim: int, positions, base: float = 10000.0):
+    """qkv: [tokens, 3*heads*head_dim] storage.  Returns q, k, v, q_mag, k_mag
+    as binary64 arrays shaped [heads, tokens, head_dim]."""
+    qkv = np.ascontiguousarray(qkv)
+    tokens = qkv.shape[0]
+    pos = _c(positions, np.int64)
+    shp = (heads, tokens, head_dim)
+    q, k, v, qm, km = (np.empty(shp, np.float64) for _ in range(5))
+    lib().oracle_rope_qkv_split(_p(qkv), dt, tokens, heads, head_dim, _p(pos), float(base),
+                                _p(q), _p(k), _p(v), _p(qm), _p(km))
+    return q, k, v, qm, km
+
+
+def detect_decode(feats, dt: int, strides, anchors, na: int, no: int):
+    """feats: list of [1, na*no, H, W] storage arrays.  anchors: [nscales, na, 2].
+    Returns (out [rows, no], term_mag [rows, no]) in binary64."""
+    feats = [np.ascontiguousarray(f) for f in feats]
+    hw = np.array([d for f in feats for d in f.shape[2:]], np.int32)
+    rows = sum(na * f.shape[2] * f.shape[3] for f in feats)
+    ptrs = (ctypes.c_void_p * len(feats))(*[f.ctypes.data for f in feats])
+    st = _c(strides, np.float64)
+    an = _c(anchors, np.float64).reshape(-1)
+    out = np.empty((rows, no), np.float64)
+    mag = np.empty((rows, no), np.float64)
+    lib().oracle_detect_decode(ptrs, dt, _p(hw), _p(st), _p(an), len(feats), na, no, _p(out),
+                               _p(mag))
+    return out, mag

@@ -1,0 +1,241 @@
+"""Pins for the oracle's elementwise chains and their acceptance check (CPU).
+
+What pins what:
+  * hand-derived worked examples (tests/golden) for add -> relu -> scale and
+    for multi-input chains (input order, op order);
+  * every fp16 bit pattern through each unary op, against numpy / scipy
+    library routines (exp, expit) and the relu definition's special cases;
+  * the fp32 working range (overflow to inf) against numpy's float32 cast;
+  * the ChannelShuffle prologue against numpy reshape/transpose;
+  * the acceptance check: a simulated fp32 device (numpy float32, one rounding
+    per step) must always pass, perturbed results must fail, and a value that
+    lands on an fp16 rounding midpoint must be accepted either way.
+"""
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _num(tok):
+    tok = tok.strip()
+    if "0x" in tok:
+        return float.fromhex(tok)
+    return float(tok)
+
+
+def test_golden_add_relu_scale():
+    rows = [l.split("#", 1)[0].split() for l in open(os.path.join(GOLDEN, "add_relu_scale.txt"))]
+    rows = [r for r in rows if r]
+    a = np.array([_num(r[0]) for r in rows], np.float32)
+    b = np.array([_num(r[1]) for r in rows], np.float32)
+    want = np.array([_num(r[2]) for r in rows])
+    got, odt = oracle.chain_eval("add;relu;scale:0.5", oracle.F32, [a, b], a.shape)
+    assert odt == oracle.F32
+    assert np.array_equal(got, want), (got, want)
+    assert not np.any(np.signbit(got))  # relu of -0 and of NaN is +0
+
+
+def test_golden_multi_input_chains():
+    n = 0
+    for line in open(os.path.join(GOLDEN, "chain_multi_input.txt")):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        spec, ins, want = (s.strip() for s in line.split("|"))
+        arrays = [np.array([float(v)], np.float32) for v in ins.split()]
+        got, _ = oracle.chain_eval(spec, oracle.F32, arrays, (1,))
+        assert got[0] == float(want), (spec, got[0], want)
+        n += 1
+    assert n >= 6
+
+
+ALL_F16 = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+F16_VALUES = ALL_F16.view(np.float16).astype(np.float64)
+FP32_INF = lambda v: np.isinf(np.asarray(v, np.float64).astype(np.float32))  # noqa: E731
+
+
+def _unary(spec):
+    got, _ = oracle.chain_eval(spec, oracle.F16, [ALL_F16], ALL_F16.shape)
+    return got
+
+
+def test_relu_every_fp16():
+    got = _unary("relu")
+    x = F16_VALUES
+    pos = x > 0
+    assert np.array_equal(got[pos], x[pos])
+    assert np.all(got[~pos] == 0.0) and not np.any(np.signbit(got[~pos]))  # NaN, -0, negatives
+
+
+def test_exp_every_fp16():
+    got = _unary("exp")
+    x = F16_VALUES
+    with np.errstate(over="ignore", invalid="ignore"):
+        want = np.exp(x)
+        ovf = FP32_INF(want) & ~np.isnan(want)
+    want = np.where(ovf, np.inf, want)
+    fin = np.isfinite(want)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    assert np.array_equal(got[np.isinf(want)], want[np.isinf(want)])
+    np.testing.assert_allclose(got[fin], want[fin], rtol=4.5e-16, atol=0)  # 2 ulp of binary64
+    assert got[ALL_F16 == 0][0] == 1.0  # exp(0) = 1
+
+
+def test_sigmoid_every_fp16():
+    got = _unary("sigmoid")
+    want = scipy.special.expit(F16_VALUES)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    np.testing.assert_allclose(got[~nan], want[~nan], rtol=4e-16, atol=1e-300)
+    assert got[ALL_F16 == 0][0] == 0.5  # sigma(0) = 1/2
+
+
+def test_cast_round_trip_every_fp16():
+    got = _unary("cast:f32;cast:f16")
+    keep = ~np.isnan(F16_VALUES)
+    assert np.array_equal(got[keep], F16_VALUES[keep])
+    assert np.array_equal(oracle.store(got[keep], oracle.F16), ALL_F16[keep])
+
+
+def test_cast_rounds_like_numpy():
+    x = workloads.uniform(100_000, -70000.0, 70000.0, 11, oracle.F32)
+    got, odt = oracle.chain_eval("cast:f16", oracle.F32, [x], x.shape)
+    assert odt == oracle.F16
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).astype(np.float64)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("op,fn", [("add", np.add), ("mul", np.multiply)])
+def test_binary_ops_random_pairs(op, fn):
+    a = workloads.uniform(50_000, -2, 2, 12, oracle.F32)
+    b = workloads.uniform(50_000, -2, 2, 13, oracle.F32)
+    got, _ = oracle.chain_eval(op, oracle.F32, [a, b], a.shape)
+    assert np.array_equal(got, fn(a.astype(np.float64), b.astype(np.float64)))
+
+
+def test_scale_constant_is_the_fp32_of_the_literal():
+    x = np.array([1.0], np.float32)
+    got, _ = oracle.chain_eval("scale:0.1", oracle.F32, [x], x.shape)
+    assert got[0] == float(np.float32(0.1))
+
+
+def test_fp32_working_range_overflows_like_fp32():
+    x = np.array([3.0e38, -3.0e38, 1.7e38, 3.4028234e38], np.float32)
+    y = np.array([2.0, 2.0, 2.0, 1.0], np.float32)
+    got, _ = oracle.chain_eval("mul", oracle.F32, [x, y], x.shape)
+    with np.errstate(over="ignore"):
+        want = (x.astype(np.float64) * y).astype(np.float32).astype(np.float64)
+    assert np.array_equal(got, want)  # inf, -inf, finite, max finite
+
+
+@pytest.mark.parametrize("groups", [1, 2, 4, 8])
+def test_shuffle_prologue_matches_numpy(groups):
+    shape = (2, 8, 3, 3)
+    x = np.arange(np.prod(shape), dtype=np.float32).reshape(shape)
+    got, _ = oracle.chain_eval(f"shuffle:{groups};scale:1.0", oracle.F32, [x.reshape(-1)], shape)
+    n, c, h, w = shape
+    want = x.reshape(n, groups, c // groups, h, w).transpose(0, 2, 1, 3, 4).reshape(-1)
+    assert np.array_equal(got, want.astype(np.float64))
+
+
+def test_shuffle_extra_inputs_are_not_shuffled():
+    shape = (1, 4, 1, 2)
+    x = np.arange(8, dtype=np.float32)
+    y = np.full(8, 100.0, np.float32) + np.arange(8, dtype=np.float32) * 1000
+    got, _ = oracle.chain_eval("shuffle:2;add", oracle.F32, [x, y], shape)
+    sx = x.reshape(1, 2, 2, 1, 2).transpose(0, 2, 1, 3, 4).reshape(-1)
+    assert np.array_equal(got, sx.astype(np.float64) + y)
+
+
+# ------------------------------------------------------------ the acceptance check
+
+def _simulate_fp32_device(spec, in_dtype, inputs, shape, groups=0):
+    """A model of an fp32 device: every step rounds to fp32 once (exp and the
+    sigmoid's exp evaluated in binary64 then rounded, i.e. within 1/2 ulp)."""
+    ch = oracle.parse_spec(spec, in_dtype)
+    vals = [oracle.to_double(a, d).astype(np.float32) for a, d in zip(inputs, ch.in_dtypes)]
+    x = vals[0]
+    if ch.groups:
+        n, c, h, w = shape
+        x = x.reshape(n, ch.groups, c // ch.groups, h, w).transpose(0, 2, 1, 3, 4).reshape(-1)
+    with np.errstate(all="ignore"):
+        for op, arg, j in zip(ch.ops, ch.args, ch.in_idx):
+            if op == oracle.OP_ADD:
+                x = x + vals[j]
+            elif op == oracle.OP_MUL:
+                x = x * vals[j]
+            elif op == oracle.OP_SCALE:
+                x = x * np.float32(arg)
+            elif op == oracle.OP_RELU:
+                x = np.where(x > 0, x, np.float32(0))
+            elif op == oracle.OP_EXP:
+                x = np.exp(x.astype(np.float64)).astype(np.float32)
+            elif op == oracle.OP_SIGMOID:
+                e = np.exp(-x.astype(np.float64)).astype(np.float32)
+                x = np.float32(1) / (np.float32(1) + e)
+            elif op == oracle.OP_CAST:
+                if int(arg) == oracle.F16:
+                    x = x.astype(np.float16).astype(np.float32)
+                elif int(arg) == oracle.BF16:
+                    x = oracle.to_double(oracle.store(x.astype(np.float64), oracle.BF16),
+                                         oracle.BF16).astype(np.float32)
+    if ch.out_dtype == oracle.F32:
+        return x.astype(np.float32)
+    return oracle.store(x.astype(np.float64), ch.out_dtype)
+
+
+@pytest.mark.parametrize("length", [1, 2, 4, 8, 16, 32])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_check_accepts_an_fp32_device(length, seed):
+    spec, dt = workloads.random_chain(length, seed)
+    inputs, _ = workloads.chain_inputs(spec, dt, 4099, seed)
+    dev = _simulate_fp32_device(spec, dt, inputs, (4099,))
+    fails, counts, _ = oracle.chain_check(spec, dt, inputs, (4099,), dev)
+    assert fails == 0, (spec, counts)
+    assert counts[3] <= 4099 // 100, (spec, counts)  # few unpinned
+
+
+def test_check_rejects_perturbed_results():
+    spec, dt = "add;sigmoid;scale:0.75;mul", oracle.F32
+    inputs, _ = workloads.chain_inputs(spec, dt, 5000, 3)
+    dev = _simulate_fp32_device(spec, dt, inputs, (5000,))
+    assert oracle.chain_check(spec, dt, inputs, (5000,), dev)[0] == 0
+    bad = (dev * np.float32(1 + 1e-4)).astype(np.float32)
+    fails, _, cls = oracle.chain_check(spec, dt, inputs, (5000,), bad)
+    assert fails > 4900
+    # fp16 output: 3 ulps away must fail
+    spec16 = "add;exp;cast:f16"
+    inputs, _ = workloads.chain_inputs(spec16, dt, 5000, 4)
+    dev16 = _simulate_fp32_device(spec16, dt, inputs, (5000,))
+    assert oracle.chain_check(spec16, dt, inputs, (5000,), dev16)[0] == 0
+    finite = np.isfinite(dev16.view(np.float16)) & (dev16 & 0x7FFF < 0x7BF0)
+    moved = dev16.copy()
+    moved[finite] += 3
+    fails, _, cls = oracle.chain_check(spec16, dt, inputs, (5000,), moved)
+    assert fails == int(finite.sum())
+
+
+def test_check_branches_at_an_fp16_midpoint():
+    # 1 + (2^-11 + 2^-31): the exact sum lies just above the fp16 midpoint
+    # 1 + 2^-11, but an fp32 device rounds the sum onto the midpoint, whose
+    # cast goes to the even neighbour 1.  Both neighbours must be accepted,
+    # nothing else.
+    spec = "add;cast:f16;cast:f32"
+    a = np.array([1.0], np.float32)
+    b = np.array([2.0 ** -11 + 2.0 ** -31], np.float32)
+    exact, _ = oracle.chain_eval(spec, oracle.F32, [a, b], (1,))
+    assert exact[0] == 1.0 + 2.0 ** -10
+    for dev, ok in [(1.0, True), (1.0 + 2.0 ** -10, True), (1.0 + 2.0 ** -9, False)]:
+        fails, counts, cls = oracle.chain_check(spec, oracle.F32, [a, b], (1,),
+                                                np.array([dev], np.float32))
+        assert (fails == 0) == ok, (dev, counts)
+    _, counts, _ = oracle.chain_check(spec, oracle.F32, [a, b], (1,), np.array([1.0], np.float32))
+    assert counts[1] == 1  # accepted by the error-bound rule, not the flat one
