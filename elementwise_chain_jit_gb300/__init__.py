@@ -1,0 +1,221 @@
+"""Python binding of the fused-chain library (libfusechain.so).
+
+Argument marshalling only: every step of every operation runs in the
+library's generated CUDA kernels.  The functions carry the C ABI's names
+(see include/fuse.h); tensor arguments may be torch tensors (their data
+pointers are passed) or raw integer device addresses.  A nonzero status
+raises FuseError with the library's message.
+
+If the shared library has not been built this module raises ImportError: there
+is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfusechain.so")
+
+F32, F16, BF16 = 0, 1, 2
+DTYPE_NAMES = {F32: "f32", F16: "f16", BF16: "bf16"}
+
+STATUS = {0: "FUSE_OK", -1: "FUSE_E_SPEC", -2: "FUSE_E_SHAPE", -3: "FUSE_E_DTYPE",
+          -4: "FUSE_E_NULL", -5: "FUSE_E_ARCH", -6: "FUSE_E_COMPILE", -7: "FUSE_E_CUDA",
+          -8: "FUSE_E_ARG"}
+
+# every symbol include/fuse.h declares
+EXPORTS = ["fuse_compile", "fuse_num_inputs", "fuse_input_dtypes", "fuse_launch", "fuse_release",
+           "fuse_source", "rmsnorm_residual", "rope_qkv_split", "detect_decode", "channel_shuffle",
+           "fuse_last_error", "fuse_stats", "fuse_device_sms"]
+
+
+class FuseError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: run python elementwise_chain_jit_gb300/buildlib.py "
+                      "(or __graft_entry__.build()) first")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_P, _I, _I64, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+_lib.fuse_compile.argtypes = [ctypes.c_char_p, ctypes.POINTER(_I64), _I, _I, ctypes.POINTER(_P)]
+_lib.fuse_num_inputs.argtypes = [_P, ctypes.POINTER(_I), ctypes.POINTER(_I)]
+_lib.fuse_input_dtypes.argtypes = [_P, ctypes.POINTER(_I), _I]
+_lib.fuse_launch.argtypes = [_P, ctypes.POINTER(_P), _I, _P, _P]
+_lib.fuse_release.argtypes = [_P]
+_lib.fuse_source.argtypes = [ctypes.c_char_p, ctypes.POINTER(_I64), _I, _I, ctypes.c_char_p,
+                             ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
+_lib.rmsnorm_residual.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P]
+_lib.rope_qkv_split.argtypes = [_P, _P, _P, _P, _I64, _I, _I, _I64, _F, _I, _P]
+_lib.detect_decode.argtypes = [ctypes.POINTER(_P), ctypes.POINTER(_I), ctypes.POINTER(_F),
+                               ctypes.POINTER(_F), _I, _I, _I, _I, _P, _P]
+_lib.channel_shuffle.argtypes = [_P, _P, _I64, _I64, _I64, _I64, _I, _I, _P]
+_lib.fuse_last_error.restype = ctypes.c_char_p
+_lib.fuse_stats.argtypes = [ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64),
+                            ctypes.POINTER(ctypes.c_double)]
+_lib.fuse_device_sms.argtypes = [ctypes.POINTER(_I)]
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise FuseError(rc, (_lib.fuse_last_error() or b"").decode(errors="replace"))
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        if torch.cuda.is_available() and torch.cuda.is_initialized():
+            return torch.cuda.current_stream().cuda_stream
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype(dt) -> int:
+    if isinstance(dt, int):
+        return dt
+    import torch
+    return {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}[dt]
+
+
+def _shape(shape):
+    arr = (_I64 * len(shape))(*[int(s) for s in shape])
+    return arr, len(shape)
+
+
+# ---------------------------------------------------------------- chains
+
+class Chain:
+    """A compiled chain (wraps a fuse_handle)."""
+
+    def __init__(self, handle: int, spec: str, shape):
+        self.handle = handle
+        self.spec = spec
+        self.shape = tuple(int(s) for s in shape)
+        n, o = _I(), _I()
+        _check(_lib.fuse_num_inputs(handle, ctypes.byref(n), ctypes.byref(o)))
+        self.n_in, self.out_dtype = n.value, o.value
+        dts = (_I * max(1, self.n_in))()
+        _check(_lib.fuse_input_dtypes(handle, dts, self.n_in))
+        self.in_dtypes = [dts[i] for i in range(self.n_in)]
+
+    def __call__(self, inputs, output, stream=None):
+        fuse_launch(self, inputs, output, stream)
+        return output
+
+    def release(self):
+        if self.handle:
+            fuse_release(self)
+            self.handle = None
+
+
+def fuse_compile(spec: str, shape, in_dtype) -> Chain:
+    h = _P()
+    arr, nd = _shape(shape)
+    _check(_lib.fuse_compile(spec.encode(), arr, nd, _dtype(in_dtype), ctypes.byref(h)))
+    return Chain(h.value, spec, shape)
+
+
+def fuse_launch(chain: Chain, inputs, output, stream=None) -> None:
+    ptrs = (_P * max(1, len(inputs)))(*[_ptr(t) for t in inputs])
+    _check(_lib.fuse_launch(chain.handle, ptrs, len(inputs), _ptr(output), _stream(stream)))
+
+
+def fuse_release(chain: Chain) -> None:
+    _check(_lib.fuse_release(chain.handle))
+
+
+def fuse_source(spec: str, shape, in_dtype) -> str:
+    arr, nd = _shape(shape)
+    n = ctypes.c_size_t()
+    _check(_lib.fuse_source(spec.encode(), arr, nd, _dtype(in_dtype), None, 0, ctypes.byref(n)))
+    buf = ctypes.create_string_buffer(n.value + 1)
+    _check(_lib.fuse_source(spec.encode(), arr, nd, _dtype(in_dtype), buf, n.value + 1,
+                            ctypes.byref(n)))
+    return buf.value.decode()
+
+
+# ---------------------------------------------------------------- fixed entry points
+
+def rmsnorm_residual(x, residual, weight, out, residual_out, eps: float = 1e-6, dt=None,
+                     rows: int | None = None, hidden: int | None = None, stream=None) -> None:
+    if rows is None:
+        rows, hidden = x.shape[0], x.shape[-1]
+    if dt is None:
+        dt = x.dtype
+    _check(_lib.rmsnorm_residual(_ptr(x), _ptr(residual), _ptr(weight), _ptr(out),
+                                 _ptr(residual_out), rows, hidden, eps, _dtype(dt),
+                                 _stream(stream)))
+
+
+def rope_qkv_split(qkv, q, k, v, heads: int, head_dim: int, pos0: int = 0,
+                   base: float = 10000.0, dt=None, tokens: int | None = None, stream=None) -> None:
+    if tokens is None:
+        tokens = qkv.shape[0]
+    if dt is None:
+        dt = qkv.dtype
+    _check(_lib.rope_qkv_split(_ptr(qkv), _ptr(q), _ptr(k), _ptr(v), tokens, heads, head_dim,
+                               pos0, base, _dtype(dt), _stream(stream)))
+
+
+def detect_decode(feats, hw, strides, anchors, na: int, no: int, out, in_dt=None,
+                  stream=None) -> None:
+    ns = len(feats)
+    fp = (_P * ns)(*[_ptr(f) for f in feats])
+    hwa = (_I * (2 * ns))(*[int(d) for pair in hw for d in pair])
+    st = (_F * ns)(*[float(s) for s in strides])
+    flat = [float(a) for a in _flatten(anchors)]
+    an = (_F * len(flat))(*flat)
+    if in_dt is None:
+        in_dt = feats[0].dtype
+    _check(_lib.detect_decode(fp, hwa, st, an, ns, na, no, _dtype(in_dt), _ptr(out),
+                              _stream(stream)))
+
+
+def channel_shuffle(x, out, groups: int, dt=None, shape=None, stream=None) -> None:
+    n, c, h, w = shape if shape is not None else x.shape
+    if dt is None:
+        dt = x.dtype
+    _check(_lib.channel_shuffle(_ptr(x), _ptr(out), n, c, h, w, groups, _dtype(dt),
+                                _stream(stream)))
+
+
+def _flatten(a):
+    try:
+        import numpy as np
+        return np.asarray(a, dtype=float).reshape(-1).tolist()
+    except Exception:  # pragma: no cover
+        return [x for row in a for pair in row for x in pair]
+
+
+# ---------------------------------------------------------------- diagnostics
+
+def fuse_last_error() -> str:
+    return (_lib.fuse_last_error() or b"").decode(errors="replace")
+
+
+def fuse_stats() -> dict:
+    c, h, l = _I64(), _I64(), _I64()
+    ms = ctypes.c_double()
+    _check(_lib.fuse_stats(ctypes.byref(c), ctypes.byref(h), ctypes.byref(l), ctypes.byref(ms)))
+    return {"compiles": c.value, "cache_hits": h.value, "launches": l.value,
+            "compile_ms": ms.value}
+
+
+def fuse_device_sms() -> int:
+    s = _I()
+    _check(_lib.fuse_device_sms(ctypes.byref(s)))
+    return s.value

@@ -1,0 +1,72 @@
+// abi.cpp -- diagnostics entry points and ChannelShuffle.
+//
+// ChannelShuffle ("算子与运行时", section 2) on contiguous NCHW is a
+// permutation of whole H*W planes.  It runs through the chain engine as the
+// spec "shuffle:G" with no ops: a bit copy whose input index is the shuffle's
+// gather, with 16/32-byte coalesced accesses on both sides.  The pages' own
+// remedy for the slow reshape/transpose (shared-memory reordering before
+// coalesced writes, section 2.1) is not needed on NCHW, where each plane is
+// already contiguous in both layouts.
+#include <map>
+#include <tuple>
+
+#include "internal.h"
+
+namespace fuse {
+const char* last_error_cstr();
+void read_stats(int64_t* c, int64_t* h, int64_t* l, double* ms);
+int chain_compile(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dt,
+                  fuse_chain** out);
+int chain_launch(fuse_chain* h, const void* const* inputs, int n_in, void* output, void* stream);
+
+namespace {
+std::mutex g_shuffle_mu;
+std::map<std::tuple<int64_t, int64_t, int64_t, int64_t, int, int>, fuse_chain*> g_shuffle;
+}  // namespace
+}  // namespace fuse
+
+extern "C" {
+
+const char* fuse_last_error(void) { return fuse::last_error_cstr(); }
+
+int fuse_stats(int64_t* compiles, int64_t* cache_hits, int64_t* launches, double* compile_ms) {
+  fuse::read_stats(compiles, cache_hits, launches, compile_ms);
+  return FUSE_OK;
+}
+
+int fuse_device_sms(int* sms) {
+  if (!sms) return fuse::fail(FUSE_E_NULL, "sms is NULL");
+  *sms = fuse::default_sms();
+  return FUSE_OK;
+}
+
+int channel_shuffle(const void* in, void* out, int64_t n, int64_t c, int64_t h, int64_t w,
+                    int groups, fuse_dtype dt, void* stream) {
+  using namespace fuse;
+  if (!valid_dtype(dt)) return fail(FUSE_E_DTYPE, fmt("invalid dtype %d", dt));
+  if (n < 0 || c < 0 || h < 0 || w < 0) return fail(FUSE_E_SHAPE, "negative dimension");
+  if (groups <= 0) return fail(FUSE_E_ARG, "groups must be positive");
+  if (c % groups) return fail(FUSE_E_SHAPE, "channels not divisible by groups");
+  if (n * c * h * w == 0) return FUSE_OK;
+  if (!in || !out) return fail(FUSE_E_NULL, "NULL tensor pointer");
+  if (in == out) return fail(FUSE_E_ARG, "channel_shuffle cannot run in place");
+  fuse_chain* hnd = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_shuffle_mu);
+    auto key = std::make_tuple(n, c, h, w, groups, static_cast<int>(dt));
+    auto it = g_shuffle.find(key);
+    if (it != g_shuffle.end()) {
+      hnd = it->second;
+      stat_hit();
+    } else {
+      int64_t shape[4] = {n, c, h, w};
+      std::string spec = fmt("shuffle:%d", groups);
+      if (int rc = chain_compile(spec.c_str(), shape, 4, dt, &hnd)) return rc;
+      g_shuffle.emplace(key, hnd);
+    }
+  }
+  const void* ins[1] = {in};
+  return chain_launch(hnd, ins, 1, out, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,492 @@
+// chain.cpp -- op-chain IR, planner and CUDA code generator for fused
+// elementwise chains, plus fuse_compile / fuse_launch.
+//
+// Method ("DeepJIT ... 串行小核墙"): section 4.1 fuses a chain of
+// elementwise ops with several inputs into one kernel that reads each input
+// once and writes once; section 4.2 vectorises the accesses (the pages use
+// float4) with an alignment check that falls back to a scalar kernel and a
+// tail handled outside the main loop; section 3.3 bakes the element count,
+// vector width and tail switch into the source as constants.  ChannelShuffle
+// ("算子与运行时", section 2) is fused as the gather index of input 0.
+//
+// GB300 design: 32-byte (ld/st .v8.b32) or 16-byte accesses per tensor per
+// thread, several vectors in flight per thread, a grid of (SMs x resident
+// CTAs) looping over whole chunks, and one CTA finishing the ragged remainder
+// and the scalar tail after its share of the main loop.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <sstream>
+
+#include "internal.h"
+
+namespace fuse {
+
+enum ChainOpCode { OP_ADD, OP_MUL, OP_SCALE, OP_RELU, OP_SIGMOID, OP_EXP, OP_CAST };
+
+struct ChainOp {
+  ChainOpCode op;
+  float c = 0.f;             // scale constant
+  fuse_dtype to = FUSE_F32;  // cast target
+  int input = 0;             // add/mul operand
+};
+
+struct Chain {
+  int groups = 0;  // ChannelShuffle groups on input 0 (0 = none)
+  std::vector<ChainOp> ops;
+  std::vector<fuse_dtype> in_dt;
+  fuse_dtype out_dt = FUSE_F32;
+};
+
+constexpr int kMaxOps = 1024;
+constexpr int kMaxInputs = 128;
+constexpr int64_t kMaxElems = int64_t(1) << 40;
+
+static std::string trim(const std::string& s) {
+  size_t a = s.find_first_not_of(" \t\r\n"), b = s.find_last_not_of(" \t\r\n");
+  return a == std::string::npos ? std::string() : s.substr(a, b - a + 1);
+}
+
+static int parse_dtype(const std::string& s, fuse_dtype* dt) {
+  if (s == "f32") *dt = FUSE_F32;
+  else if (s == "f16") *dt = FUSE_F16;
+  else if (s == "bf16") *dt = FUSE_BF16;
+  else return -1;
+  return 0;
+}
+
+int parse_chain(const char* spec, fuse_dtype in_dt, Chain* out) {
+  if (!spec) return fail(FUSE_E_NULL, "spec is NULL");
+  if (!valid_dtype(in_dt)) return fail(FUSE_E_DTYPE, fmt("invalid input dtype %d", in_dt));
+  Chain ch;
+  ch.in_dt.push_back(in_dt);
+  fuse_dtype cur = in_dt;
+  std::stringstream ss(spec);
+  std::string item;
+  int pos = 0;
+  while (std::getline(ss, item, ';')) {
+    item = trim(item);
+    if (item.empty()) continue;
+    std::string name = item, arg;
+    bool has_arg = false;
+    if (size_t c = item.find(':'); c != std::string::npos) {
+      name = trim(item.substr(0, c));
+      arg = trim(item.substr(c + 1));
+      has_arg = true;
+    }
+    if (name == "shuffle") {
+      if (pos != 0) return fail(FUSE_E_SPEC, "shuffle must be the first item of the spec");
+      char* end = nullptr;
+      long g = has_arg ? strtol(arg.c_str(), &end, 10) : 0;
+      if (!has_arg || arg.empty() || *end || g <= 0 || g > (1 << 20))
+        return fail(FUSE_E_SPEC, fmt("bad shuffle groups '%s'", arg.c_str()));
+      ch.groups = static_cast<int>(g);
+      ++pos;
+      continue;
+    }
+    ChainOp op{};
+    if (name == "add" || name == "mul") {
+      if (has_arg) return fail(FUSE_E_SPEC, fmt("'%s' takes no argument", name.c_str()));
+      op.op = name == "add" ? OP_ADD : OP_MUL;
+      op.input = static_cast<int>(ch.in_dt.size());
+      ch.in_dt.push_back(cur);
+    } else if (name == "scale") {
+      char* end = nullptr;
+      float c = has_arg ? strtof(arg.c_str(), &end) : 0.f;
+      if (!has_arg || arg.empty() || *end || !std::isfinite(c))
+        return fail(FUSE_E_SPEC, fmt("bad scale constant '%s'", arg.c_str()));
+      op.op = OP_SCALE;
+      op.c = c;
+    } else if (name == "relu" || name == "sigmoid" || name == "exp") {
+      if (has_arg) return fail(FUSE_E_SPEC, fmt("'%s' takes no argument", name.c_str()));
+      op.op = name == "relu" ? OP_RELU : name == "sigmoid" ? OP_SIGMOID : OP_EXP;
+    } else if (name == "cast") {
+      if (!has_arg || parse_dtype(arg, &op.to))
+        return fail(FUSE_E_SPEC, fmt("bad cast target '%s' (f16, bf16 or f32)", arg.c_str()));
+      op.op = OP_CAST;
+      cur = op.to;
+    } else {
+      return fail(FUSE_E_SPEC, fmt("unknown op '%s'", item.c_str()));
+    }
+    ch.ops.push_back(op);
+    ++pos;
+    if (static_cast<int>(ch.ops.size()) > kMaxOps)
+      return fail(FUSE_E_SPEC, fmt("more than %d ops", kMaxOps));
+    if (static_cast<int>(ch.in_dt.size()) > kMaxInputs)
+      return fail(FUSE_E_SPEC, fmt("more than %d input tensors", kMaxInputs));
+  }
+  ch.out_dt = cur;
+  *out = std::move(ch);
+  return FUSE_OK;
+}
+
+// ------------------------------------------------------------------ plan
+
+struct ChainPlan {
+  Chain ch;
+  std::vector<int64_t> shape;
+  int64_t n = 0;
+  bool copy = false;  // no ops: bit copy of input 0
+  int vec = 1;        // elements per vector
+  int block = 256;
+  int unroll = 1;
+  bool vec_ok = false;
+  int64_t C = 1, HW = 1;
+  std::string source;
+};
+
+static int env_int(const char* name, int dflt) {
+  const char* e = getenv(name);
+  return e && *e ? atoi(e) : dflt;
+}
+
+int plan_chain(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dt, ChainPlan* p) {
+  if (int rc = parse_chain(spec, in_dt, &p->ch)) return rc;
+  if (!shape && ndim > 0) return fail(FUSE_E_NULL, "shape is NULL");
+  if (ndim < 1 || ndim > 8) return fail(FUSE_E_SHAPE, fmt("ndim %d outside 1..8", ndim));
+  int64_t n = 1;
+  for (int i = 0; i < ndim; ++i) {
+    if (shape[i] < 0) return fail(FUSE_E_SHAPE, fmt("negative dimension %lld", (long long)shape[i]));
+    if (shape[i] && n > kMaxElems / shape[i])
+      return fail(FUSE_E_SHAPE, "more than 2^40 elements");
+    n *= shape[i];
+    p->shape.push_back(shape[i]);
+  }
+  if (n > kMaxElems) return fail(FUSE_E_SHAPE, "more than 2^40 elements");
+  p->n = n;
+  const Chain& ch = p->ch;
+  if (ch.groups) {
+    if (ndim != 4) return fail(FUSE_E_SHAPE, "shuffle needs a 4-D NCHW shape");
+    if (shape[1] % ch.groups)
+      return fail(FUSE_E_SHAPE, fmt("channels %lld not divisible by %d groups",
+                                    (long long)shape[1], ch.groups));
+    p->C = shape[1];
+    p->HW = shape[2] * shape[3];
+  }
+  p->copy = ch.ops.empty();
+  // elements per vector: VEC_BYTES of the narrowest tensor
+  int minb = dtype_bytes(ch.out_dt);
+  int words = 0;
+  for (auto d : ch.in_dt) minb = std::min(minb, dtype_bytes(d));
+  int vec_bytes = env_int("FUSE_CHAIN_VEC_BYTES", 32);
+  if (vec_bytes != 16 && vec_bytes != 32) vec_bytes = 32;
+  p->vec = vec_bytes / minb;
+  for (auto d : ch.in_dt) words += p->vec * dtype_bytes(d) / 4;
+  words += p->vec * dtype_bytes(ch.out_dt) / 4;
+  // vectors in flight per thread: enough to cover latency, bounded registers
+  int max_unroll = env_int("FUSE_CHAIN_UNROLL", 2);
+  p->unroll = 1;
+  while (p->unroll * 2 <= max_unroll && words * p->unroll * 2 <= 64) p->unroll *= 2;
+  p->block = env_int("FUSE_CHAIN_BLOCK", 256);
+  if (p->block < 32 || p->block > 1024 || p->block % 32) p->block = 256;
+  p->vec_ok = !ch.groups || (p->HW % p->vec == 0);
+  return FUSE_OK;
+}
+
+// ------------------------------------------------------------------ codegen
+
+// elem_of_input: expression of an operand element, with "@" standing for the
+// input number
+static std::string operand(const std::string& elem_of_input, int input) {
+  std::string out;
+  for (char c : elem_of_input) out += c == '@' ? std::to_string(input) : std::string(1, c);
+  return out;
+}
+
+static void emit_op(std::ostringstream& s, const ChainOp& op, const std::string& elem_of_input) {
+  switch (op.op) {
+    case OP_ADD: s << "      x = x + " << operand(elem_of_input, op.input) << ";\n"; break;
+    case OP_MUL: s << "      x = x * " << operand(elem_of_input, op.input) << ";\n"; break;
+    case OP_SCALE: s << "      x = x * " << hex_float(op.c) << ";\n"; break;
+    case OP_RELU: s << "      x = x > 0.f ? x : 0.f;\n"; break;
+    case OP_SIGMOID: s << "      x = 1.0f / (1.0f + expf(-x));\n"; break;
+    case OP_EXP: s << "      x = expf(x);\n"; break;
+    case OP_CAST:
+      if (op.to == FUSE_F16) s << "      x = round_f16(x);\n";
+      else if (op.to == FUSE_BF16) s << "      x = round_bf16(x);\n";
+      else s << "      /* cast:f32 keeps the fp32 value */\n";
+      break;
+  }
+}
+
+static std::string gen_chain_source(const ChainPlan& p, const char* spec) {
+  const Chain& ch = p.ch;
+  const int nin = static_cast<int>(ch.in_dt.size());
+  const bool small = p.n < (int64_t(1) << 31);
+  std::ostringstream s;
+  s << "// fused chain: " << spec << "\n";
+  s << "#include \"fuse/common.cuh\"\n";
+  s << "typedef " << (small ? "unsigned" : "long long") << " idx_t;\n";
+  s << "constexpr long long N = " << p.n << "LL;\n";
+  s << "constexpr int VEC = " << p.vec << ";\n";
+  s << "constexpr int BLOCK = " << p.block << ";\n";
+  s << "constexpr int UNROLL = " << p.unroll << ";\n";
+  s << "constexpr long long NVEC = N / VEC;\n";
+  s << "constexpr long long CHUNK = (long long)BLOCK * UNROLL;\n";
+  s << "constexpr long long NFULL = NVEC / CHUNK;\n";
+  s << "constexpr int NREM = (int)(NVEC - NFULL * CHUNK);\n";
+  s << "constexpr int TAIL = (int)(N - NVEC * VEC);\n";
+  s << "constexpr int NIN = " << nin << ";\n";
+  for (int j = 0; j < nin; ++j) {
+    s << "constexpr int DT" << j << " = " << ch.in_dt[j] << ";  // " << dtype_name(ch.in_dt[j])
+      << "\n";
+    s << "constexpr int NW" << j << " = VEC * Dt<DT" << j << ">::bytes / 4;\n";
+  }
+  s << "constexpr int DTO = " << ch.out_dt << ";  // " << dtype_name(ch.out_dt) << "\n";
+  s << "constexpr int NWO = VEC * Dt<DTO>::bytes / 4;\n";
+  s << "struct Args { const void* in[NIN]; void* out; };\n\n";
+
+  // index of input 0 for an output element / vector (ChannelShuffle prologue)
+  if (ch.groups) {
+    s << "// ChannelShuffle: output channel j*G + i reads input channel i*(C/G) + j\n";
+    s << "constexpr idx_t C = " << p.C << ", HW = " << p.HW << ", G = " << ch.groups
+      << ", CPG = C / G;\n";
+    s << "__device__ __forceinline__ idx_t src_elem(idx_t e) {\n"
+         "  const idx_t plane = e / HW, off = e - plane * HW;\n"
+         "  const idx_t nn = plane / C, co = plane - nn * C;\n"
+         "  const idx_t ci = (co % G) * CPG + co / G;\n"
+         "  return (nn * C + ci) * HW + off;\n"
+         "}\n";
+    if (p.vec_ok) {
+      s << "constexpr idx_t VPP = HW / VEC;  // vectors per plane\n";
+      s << "__device__ __forceinline__ idx_t src_vec(idx_t v) {\n"
+           "  const idx_t plane = v / VPP, off = v - plane * VPP;\n"
+           "  const idx_t nn = plane / C, co = plane - nn * C;\n"
+           "  const idx_t ci = (co % G) * CPG + co / G;\n"
+           "  return (nn * C + ci) * VPP + off;\n"
+           "}\n";
+    }
+  } else {
+    s << "__device__ __forceinline__ idx_t src_elem(idx_t e) { return e; }\n";
+    s << "__device__ __forceinline__ idx_t src_vec(idx_t v) { return v; }\n";
+  }
+
+  // per-element chain on register vectors
+  s << "\n// the chain, one element at a time, in fp32 registers\n";
+  s << "__device__ __forceinline__ void apply(";
+  for (int j = 0; j < nin; ++j) s << "const u32 (&w" << j << ")[NW" << j << "], ";
+  s << "u32 (&wo)[NWO]) {\n";
+  if (p.copy) {
+    s << "  static_assert(NWO == NW0, \"copy\");\n"
+         "#pragma unroll\n  for (int i = 0; i < NWO; ++i) wo[i] = w0[i];\n}\n";
+  } else {
+    s << "  float y[VEC];\n#pragma unroll\n  for (int e = 0; e < VEC; ++e) {\n";
+    s << "      float x = get_elem<DT0>(w0, e);\n";
+    for (auto& op : ch.ops) emit_op(s, op, "get_elem<DT@>(w@, e)");
+    s << "      y[e] = x;\n  }\n  pack_vec<DTO>(y, wo);\n}\n";
+  }
+
+  // scalar chain for one element (tail and fallback kernel)
+  s << "\n__device__ __forceinline__ void apply_elem(const Args& a, idx_t e) {\n";
+  if (p.copy) {
+    s << "  static_cast<typename Dt<DTO>::storage*>(a.out)[e] =\n"
+         "      static_cast<const typename Dt<DT0>::storage*>(a.in[0])[src_elem(e)];\n}\n";
+  } else {
+    s << "  float x = load_elem<DT0>(a.in[0], src_elem(e));\n";
+    for (auto& op : ch.ops) emit_op(s, op, "load_elem<DT@>(a.in[@], e)");
+    s << "  store_elem<DTO>(a.out, e, x);\n}\n";
+  }
+
+  // vector kernel
+  if (p.vec_ok) {
+    s << "\n// vectors [v0, v0 + UNROLL*BLOCK) with stride BLOCK; CHECK: bound by NVEC\n";
+    s << "template <bool CHECK>\n__device__ __forceinline__ void do_chunk(const Args& a, idx_t v0) {\n";
+    for (int j = 0; j < nin; ++j) s << "  u32 r" << j << "[UNROLL][NW" << j << "];\n";
+    s << "#pragma unroll\n  for (int u = 0; u < UNROLL; ++u) {\n"
+         "    const idx_t v = v0 + (idx_t)u * BLOCK;\n"
+         "    if (CHECK && v >= (idx_t)NVEC) break;\n";
+    for (int j = 0; j < nin; ++j) {
+      s << "    load_words(static_cast<const u32*>(a.in[" << j << "]) + (idx_t)"
+        << (j == 0 ? "src_vec(v)" : "v") << " * NW" << j << ", r" << j << "[u]);\n";
+    }
+    s << "  }\n#pragma unroll\n  for (int u = 0; u < UNROLL; ++u) {\n"
+         "    const idx_t v = v0 + (idx_t)u * BLOCK;\n"
+         "    if (CHECK && v >= (idx_t)NVEC) break;\n"
+         "    u32 wo[NWO];\n    apply(";
+    for (int j = 0; j < nin; ++j) s << "r" << j << "[u], ";
+    s << "wo);\n    store_words(static_cast<u32*>(a.out) + v * NWO, wo);\n  }\n}\n";
+    s << "\nextern \"C\" __global__ void __launch_bounds__(BLOCK) fuse_chain_vec(const Args a) {\n"
+         "  for (idx_t c = blockIdx.x; c < (idx_t)NFULL; c += gridDim.x)\n"
+         "    do_chunk<false>(a, c * (idx_t)CHUNK + threadIdx.x);\n"
+         "  if constexpr (NREM > 0 || TAIL > 0) {\n"
+         "    // the CTA with the fewest full chunks takes the remainder and the tail\n"
+         "    if (blockIdx.x == (unsigned)(NFULL % gridDim.x)) {\n"
+         "      if constexpr (NREM > 0) do_chunk<true>(a, (idx_t)NFULL * CHUNK + threadIdx.x);\n"
+         "      if constexpr (TAIL > 0)\n"
+         "        if (threadIdx.x < TAIL) apply_elem(a, (idx_t)NVEC * VEC + threadIdx.x);\n"
+         "    }\n  }\n}\n";
+  }
+  // scalar kernel: any alignment
+  s << "\nextern \"C\" __global__ void __launch_bounds__(256) fuse_chain_scalar(const Args a) {\n"
+       "  for (idx_t e = (idx_t)blockIdx.x * 256 + threadIdx.x; e < (idx_t)N;"
+       " e += (idx_t)gridDim.x * 256)\n"
+       "    apply_elem(a, e);\n}\n";
+  return s.str();
+}
+
+// ------------------------------------------------------------------ handle
+
+}  // namespace fuse
+
+struct fuse_chain {
+  fuse::ChainPlan plan;
+  std::shared_ptr<fuse::Module> mod;
+  std::mutex mu;
+  struct PerDevice {
+    int device;
+    CUfunction vec_fn, scalar_fn;
+    unsigned vec_grid, scalar_grid;
+  };
+  std::vector<PerDevice> dev;
+};
+
+namespace fuse {
+
+static int chain_device_state(fuse_chain* h, const DeviceInfo& d, fuse_chain::PerDevice** out) {
+  std::lock_guard<std::mutex> lk(h->mu);
+  for (auto& pd : h->dev)
+    if (pd.device == d.ordinal) {
+      *out = &pd;
+      return FUSE_OK;
+    }
+  fuse_chain::PerDevice pd{};
+  pd.device = d.ordinal;
+  const DriverApi* api;
+  if (int rc = driver(&api)) return rc;
+  const ChainPlan& p = h->plan;
+  if (int rc = jit_function(*h->mod, "fuse_chain_scalar", d, &pd.scalar_fn)) return rc;
+  int occ = 0;
+  CUresult r = api->OccupancyMaxActiveBlocksPerMultiprocessor(&occ, pd.scalar_fn, 256, 0);
+  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuOccupancyMaxActiveBlocksPerMultiprocessor");
+  int64_t want = (p.n + 255) / 256;
+  pd.scalar_grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(d.sms) * std::max(occ, 1))));
+  if (p.vec_ok) {
+    if (int rc = jit_function(*h->mod, "fuse_chain_vec", d, &pd.vec_fn)) return rc;
+    r = api->OccupancyMaxActiveBlocksPerMultiprocessor(&occ, pd.vec_fn, p.block, 0);
+    if (r != CUDA_SUCCESS) return cuda_fail(r, "cuOccupancyMaxActiveBlocksPerMultiprocessor");
+    int per_sm = env_int("FUSE_CHAIN_CTAS_PER_SM", 0);
+    if (per_sm <= 0 || per_sm > occ) per_sm = std::max(occ, 1);
+    int64_t chunk = int64_t(p.block) * p.unroll;
+    int64_t nfull = (p.n / p.vec) / chunk;
+    pd.vec_grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(nfull, int64_t(d.sms) * per_sm)));
+  }
+  h->dev.push_back(pd);
+  *out = &h->dev.back();
+  return FUSE_OK;
+}
+
+int chain_compile(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dt,
+                  fuse_chain** out) {
+  auto h = std::make_unique<fuse_chain>();
+  if (int rc = plan_chain(spec, shape, ndim, in_dt, &h->plan)) return rc;
+  h->plan.source = gen_chain_source(h->plan, spec);
+  if (int rc = jit_compile(h->plan.source, "fuse_chain", &h->mod)) return rc;
+  // load now when a device is present, so that the first launch does no work
+  DeviceInfo d;
+  fuse_chain::PerDevice* pd;
+  if (current_device(&d) == FUSE_OK) {
+    if (int rc = chain_device_state(h.get(), d, &pd)) return rc;
+  }
+  clear_error();
+  *out = h.release();
+  return FUSE_OK;
+}
+
+int chain_source(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dt,
+                 std::string* src) {
+  ChainPlan p;
+  if (int rc = plan_chain(spec, shape, ndim, in_dt, &p)) return rc;
+  *src = gen_chain_source(p, spec);
+  return FUSE_OK;
+}
+
+int chain_launch(fuse_chain* h, const void* const* inputs, int n_in, void* output, void* stream) {
+  const ChainPlan& p = h->plan;
+  const int nin = static_cast<int>(p.ch.in_dt.size());
+  if (n_in != nin) return fail(FUSE_E_ARG, fmt("chain takes %d inputs, got %d", nin, n_in));
+  if (p.n == 0) return FUSE_OK;
+  if (!inputs) return fail(FUSE_E_NULL, "inputs is NULL");
+  if (!output) return fail(FUSE_E_NULL, "output is NULL");
+  bool aligned = aligned16(output);
+  for (int j = 0; j < nin; ++j) {
+    if (!inputs[j]) return fail(FUSE_E_NULL, fmt("input %d is NULL", j));
+    aligned = aligned && aligned16(inputs[j]);
+  }
+  if (p.ch.groups && output == inputs[0])
+    return fail(FUSE_E_ARG, "a shuffled chain cannot write over its input 0");
+  DeviceInfo d;
+  if (int rc = current_device(&d)) return rc;
+  fuse_chain::PerDevice* pd;
+  if (int rc = chain_device_state(h, d, &pd)) return rc;
+  // kernel parameter: the Args struct {in[NIN], out}
+  std::vector<const void*> args(inputs, inputs + nin);
+  args.push_back(output);
+  void* kargs[] = {args.data()};
+  // 32-byte accesses need 32-byte alignment when a vector spans 32 bytes
+  bool use_vec = p.vec_ok && aligned;
+  if (use_vec) {
+    for (int j = 0; j <= nin; ++j) {
+      const void* ptr = j < nin ? inputs[j] : output;
+      fuse_dtype dt = j < nin ? p.ch.in_dt[j] : p.ch.out_dt;
+      int bytes = p.vec * dtype_bytes(dt);
+      int need = bytes >= 32 ? 32 : bytes;
+      if (reinterpret_cast<uintptr_t>(ptr) % need) use_vec = false;
+    }
+  }
+  if (use_vec) return launch(pd->vec_fn, pd->vec_grid, p.block, 0, stream, kargs);
+  return launch(pd->scalar_fn, pd->scalar_grid, 256, 0, stream, kargs);
+}
+
+}  // namespace fuse
+
+// ------------------------------------------------------------------ C ABI
+
+extern "C" {
+
+int fuse_compile(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dtype,
+                 fuse_handle* out) {
+  if (!out) return fuse::fail(FUSE_E_NULL, "out is NULL");
+  *out = nullptr;
+  return fuse::chain_compile(spec, shape, ndim, in_dtype, out);
+}
+
+int fuse_num_inputs(fuse_handle h, int* n_in, fuse_dtype* out_dtype) {
+  if (!h) return fuse::fail(FUSE_E_ARG, "NULL handle");
+  if (n_in) *n_in = static_cast<int>(h->plan.ch.in_dt.size());
+  if (out_dtype) *out_dtype = h->plan.ch.out_dt;
+  return FUSE_OK;
+}
+
+int fuse_input_dtypes(fuse_handle h, fuse_dtype* dts, int cap) {
+  if (!h) return fuse::fail(FUSE_E_ARG, "NULL handle");
+  if (!dts) return fuse::fail(FUSE_E_NULL, "dts is NULL");
+  int n = static_cast<int>(h->plan.ch.in_dt.size());
+  if (cap < n) return fuse::fail(FUSE_E_ARG, fuse::fmt("need room for %d dtypes", n));
+  for (int i = 0; i < n; ++i) dts[i] = h->plan.ch.in_dt[i];
+  return FUSE_OK;
+}
+
+int fuse_launch(fuse_handle h, const void* const* inputs, int n_in, void* output, void* stream) {
+  if (!h) return fuse::fail(FUSE_E_ARG, "NULL handle");
+  return fuse::chain_launch(h, inputs, n_in, output, stream);
+}
+
+int fuse_release(fuse_handle h) {
+  delete h;  // the compiled module stays in the cache for the life of the process
+  return FUSE_OK;
+}
+
+int fuse_source(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dtype, char* buf,
+                size_t cap, size_t* len) {
+  std::string src;
+  if (int rc = fuse::chain_source(spec, shape, ndim, in_dtype, &src)) return rc;
+  if (len) *len = src.size();
+  if (buf && cap) {
+    size_t n = std::min(cap - 1, src.size());
+    memcpy(buf, src.data(), n);
+    buf[n] = '\0';
+  }
+  return FUSE_OK;
+}
+
+}  // extern "C"

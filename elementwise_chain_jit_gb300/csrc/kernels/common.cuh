@@ -1,0 +1,202 @@
+// common.cuh -- device helpers included by every generated kernel.
+//
+// Embedded into the library at build time and handed to NVRTC as the header
+// "fuse/common.cuh".  No CUDA headers are needed: dtype conversions use the
+// PTX cvt instructions (IEEE round-to-nearest-even), memory accesses use
+// explicit 128-bit and 256-bit vector instructions.
+#pragma once
+
+typedef unsigned short u16;
+typedef unsigned int u32;
+typedef unsigned long long u64;
+
+// ---------------------------------------------------------------- dtypes
+// dtype codes match fuse_dtype: 0 = f32, 1 = f16, 2 = bf16
+
+__device__ __forceinline__ float f16_to_f32(u16 h) {
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+  return f;
+}
+__device__ __forceinline__ u16 f32_to_f16(float f) {
+  u16 h;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(f));
+  return h;
+}
+__device__ __forceinline__ float bf16_to_f32(u16 h) { return __uint_as_float(static_cast<u32>(h) << 16); }
+__device__ __forceinline__ u16 f32_to_bf16(float f) {
+  u16 h;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(f));
+  return h;
+}
+// two floats -> one 32-bit word, element `lo` in the low half
+__device__ __forceinline__ u32 pack2_f16(float lo, float hi) {
+  u32 r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ u32 pack2_bf16(float lo, float hi) {
+  u32 r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float round_f16(float x) { return f16_to_f32(f32_to_f16(x)); }
+__device__ __forceinline__ float round_bf16(float x) { return bf16_to_f32(f32_to_bf16(x)); }
+
+template <int DT>
+struct Dt;
+template <>
+struct Dt<0> {
+  static constexpr int bytes = 4;
+  typedef float storage;
+};
+template <>
+struct Dt<1> {
+  static constexpr int bytes = 2;
+  typedef u16 storage;
+};
+template <>
+struct Dt<2> {
+  static constexpr int bytes = 2;
+  typedef u16 storage;
+};
+
+// element e of a register vector of words holding dtype DT
+template <int DT, int NW>
+__device__ __forceinline__ float get_elem(const u32 (&w)[NW], int e) {
+  if constexpr (DT == 0) {
+    return __uint_as_float(w[e]);
+  } else {
+    const u32 x = w[e >> 1];
+    const u16 h = (e & 1) ? static_cast<u16>(x >> 16) : static_cast<u16>(x & 0xffffu);
+    if constexpr (DT == 1) return f16_to_f32(h);
+    else return bf16_to_f32(h);
+  }
+}
+
+// VEC floats -> words of dtype DT
+template <int DT, int VEC, int NW>
+__device__ __forceinline__ void pack_vec(const float (&y)[VEC], u32 (&w)[NW]) {
+  if constexpr (DT == 0) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) w[i] = __float_as_uint(y[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < VEC / 2; ++i)
+      w[i] = DT == 1 ? pack2_f16(y[2 * i], y[2 * i + 1]) : pack2_bf16(y[2 * i], y[2 * i + 1]);
+  }
+}
+
+// scalar element access (fallback kernels)
+template <int DT>
+__device__ __forceinline__ float load_elem(const void* p, long long i) {
+  if constexpr (DT == 0) return static_cast<const float*>(p)[i];
+  else if constexpr (DT == 1) return f16_to_f32(static_cast<const u16*>(p)[i]);
+  else return bf16_to_f32(static_cast<const u16*>(p)[i]);
+}
+template <int DT>
+__device__ __forceinline__ void store_elem(void* p, long long i, float v) {
+  if constexpr (DT == 0) static_cast<float*>(p)[i] = v;
+  else if constexpr (DT == 1) static_cast<u16*>(p)[i] = f32_to_f16(v);
+  else static_cast<u16*>(p)[i] = f32_to_bf16(v);
+}
+
+// ---------------------------------------------------------------- memory
+// Streaming loads of data read once: non-coherent path, no L1 allocation.
+// The caller guarantees alignment to the access width.
+
+__device__ __forceinline__ void ld_words32(const u32* p, u32* w) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                 "=r"(w[6]), "=r"(w[7])
+               : "l"(p));
+}
+__device__ __forceinline__ void ld_words16(const u32* p, u32* w) {
+  asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "l"(p));
+}
+__device__ __forceinline__ void ld_words8(const u32* p, u32* w) {
+  asm volatile("ld.global.nc.L1::no_allocate.v2.b32 {%0,%1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "l"(p));
+}
+__device__ __forceinline__ void st_words32(u32* p, const u32* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+__device__ __forceinline__ void st_words16(u32* p, const u32* w) {
+  asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3])
+               : "memory");
+}
+__device__ __forceinline__ void st_words8(u32* p, const u32* w) {
+  asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(w[0]), "r"(w[1]) : "memory");
+}
+
+// NW consecutive words from p (p aligned to min(4*NW, 32) bytes), widest first
+template <int NW>
+__device__ __forceinline__ void load_words(const u32* p, u32 (&w)[NW]) {
+  if constexpr (NW % 8 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW; i += 8) ld_words32(p + i, w + i);
+  } else if constexpr (NW % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW; i += 4) ld_words16(p + i, w + i);
+  } else if constexpr (NW % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW; i += 2) ld_words8(p + i, w + i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) w[i] = __ldg(p + i);
+  }
+}
+template <int NW>
+__device__ __forceinline__ void store_words(u32* p, const u32 (&w)[NW]) {
+  if constexpr (NW % 8 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW; i += 8) st_words32(p + i, w + i);
+  } else if constexpr (NW % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW; i += 4) st_words16(p + i, w + i);
+  } else if constexpr (NW % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW; i += 2) st_words8(p + i, w + i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) p[i] = w[i];
+  }
+}
+
+// ---------------------------------------------------------------- reductions
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Loads of data many CTAs reuse (weights, tables): read-only path, cached.
+__device__ __forceinline__ void ld_words32_cached(const u32* p, u32* w) {
+  asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                 "=r"(w[6]), "=r"(w[7])
+               : "l"(p));
+}
+__device__ __forceinline__ void ld_words16_cached(const u32* p, u32* w) {
+  asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "l"(p));
+}
+template <int NW>
+__device__ __forceinline__ void load_words_cached(const u32* p, u32 (&w)[NW]) {
+  if constexpr (NW % 8 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW; i += 8) ld_words32_cached(p + i, w + i);
+  } else if constexpr (NW % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW; i += 4) ld_words16_cached(p + i, w + i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) w[i] = __ldg(p + i);
+  }
+}

@@ -1,0 +1,187 @@
+/*
+ * fuse.h -- C ABI of the fused-chain library for GB300 (sm_103a).
+ *
+ * The library fuses a chain of small memory-bound operators into one kernel
+ * that reads its inputs from HBM once, applies every step in registers and
+ * writes once.  Kernels are generated at run time with their sizes, vector
+ * width and tail handling baked into the source, compiled with NVRTC for
+ * sm_103a and cached ("DeepJIT ... 串行小核墙", sections 3.1-3.3: source built
+ * at run time, NVRTC, driver-API loading, constants baked in, a cache keyed
+ * by source + arch + options).
+ *
+ * Conventions ("算子与运行时", section 4.1 and 4.3: C linkage, raw pointers, an
+ * explicit stream, an int status and no exceptions; "DeepJIT" section 6.5:
+ * pointer ownership):
+ *   - Every call returns FUSE_OK (0) or a negative FUSE_E_* code; the
+ *     message for the last failure on the calling thread is fuse_last_error().
+ *   - Tensor arguments are raw DEVICE pointers.  The caller owns them and
+ *     keeps them alive until the work on `stream` has finished (with PyTorch:
+ *     hold the tensor, or record_stream it).
+ *   - `stream` is a cudaStream_t / CUstream passed as void* (NULL = the
+ *     legacy default stream).  Calls enqueue work and return without
+ *     synchronising the device or the stream.
+ *   - The library owns compiled modules.  They stay loaded for the life of
+ *     the process ("DeepJIT" section 6.4: never unload a module a stream may
+ *     still be running); fuse_release() frees only the handle.
+ *   - Kernels are built for sm_103 only; another device gives FUSE_E_ARCH.
+ *   - Code generation and NVRTC compilation need no GPU; the first call on a
+ *     device loads the module there.  Compilation happens once per distinct
+ *     source (50-500 ms) and is never repeated for a cached shape.
+ *   - Thread safety: all calls may be made from several threads; compiles
+ *     are serialised internally.
+ */
+#ifndef FUSE_H
+#define FUSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FUSE_F32 = 0, FUSE_F16 = 1, FUSE_BF16 = 2 } fuse_dtype;
+
+enum {
+  FUSE_OK = 0,
+  FUSE_E_SPEC = -1,    /* malformed op-chain spec */
+  FUSE_E_SHAPE = -2,   /* sizes inconsistent or out of range */
+  FUSE_E_DTYPE = -3,   /* unsupported dtype combination */
+  FUSE_E_NULL = -4,    /* a required pointer is NULL */
+  FUSE_E_ARCH = -5,    /* the current device is not sm_103 */
+  FUSE_E_COMPILE = -6, /* NVRTC failed; the log is in fuse_last_error() */
+  FUSE_E_CUDA = -7,    /* a CUDA driver call failed, or no driver/device */
+  FUSE_E_ARG = -8      /* another invalid argument (count, handle, ...) */
+};
+
+typedef struct fuse_chain* fuse_handle;
+
+/* ------------------------------------------------------------------------
+ * Elementwise chains ("DeepJIT" sections 3.2, 4.1, 4.2; "算子与运行时" 2).
+ *
+ * spec: "[shuffle:G;]op;op;..." with
+ *   add | mul          x = x (+|*) in_j: consumes the next input tensor, whose
+ *                      dtype is the chain's dtype at that op
+ *   scale:<c>          x = x * c, c the fp32 nearest the literal
+ *   relu               x = x > 0 ? x : 0   (NaN and -0 give +0)
+ *   sigmoid            x = 1 / (1 + exp(-x))
+ *   exp                x = exp(x)
+ *   cast:f16|bf16|f32  round x to that dtype; later tensors and the output
+ *                      take it
+ *   shuffle:G          (first item only) ChannelShuffle of input 0 with G
+ *                      groups over an NCHW shape: output channel j*G + i reads
+ *                      input channel i*(C/G) + j ("算子与运行时", section 2)
+ * Every step runs in fp32 registers; only casts and the final store round.
+ * A spec with no ops (only a shuffle, or empty) copies input 0 bit for bit.
+ *
+ * shape/ndim: the tensor shape (1..8 dims, contiguous, row-major); with a
+ *   shuffle it must be 4-D NCHW with C divisible by G.  Up to 2^40 elements.
+ * in_dtype: dtype of input 0.
+ * out: receives the handle.  Returns FUSE_E_SPEC/SHAPE/DTYPE/COMPILE on
+ *   error (no handle is made).
+ */
+int fuse_compile(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dtype,
+                 fuse_handle* out);
+
+/* Number of input tensors the chain takes and the dtype of its output. */
+int fuse_num_inputs(fuse_handle h, int* n_in, fuse_dtype* out_dtype);
+
+/* dtype of each input (dts has room for n_in entries). */
+int fuse_input_dtypes(fuse_handle h, fuse_dtype* dts, int cap);
+
+/* Launch the chain: inputs[0..n_in) and output are device pointers to
+ * contiguous tensors of the compiled shape.  Pointers that are all 16-byte
+ * aligned take the 128-bit vector kernel, otherwise the scalar kernel of the
+ * same module ("DeepJIT" section 4.2).  The output must not overlap an input
+ * unless it is the same pointer as an input that is read at the same index
+ * (not input 0 of a shuffled chain). */
+int fuse_launch(fuse_handle h, const void* const* inputs, int n_in, void* output, void* stream);
+
+/* Free the handle (the compiled module stays cached). */
+int fuse_release(fuse_handle h);
+
+/* Generated CUDA source of a chain, without compiling it.  Writes up to cap
+ * bytes (NUL-terminated) and the full length to *len. */
+int fuse_source(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dtype, char* buf,
+                size_t cap, size_t* len);
+
+/* ------------------------------------------------------------------------
+ * Residual add + RMSNorm + cast ("TeleTron", sections 3.3 and 4.2).
+ * Per row r of [rows, hidden]:
+ *   h = x + residual            (fp32)
+ *   residual_out = dt(h)        (round to nearest even)
+ *   ms = sum(h^2) / hidden      (fp32 accumulation)
+ *   out = dt(h * (1 / sqrt(ms + eps)) * weight)
+ * x, residual, out, residual_out: [rows, hidden]; weight: [hidden]; all of
+ * dtype dt (f16, bf16 or f32).  residual_out may equal residual and out may
+ * equal x (in place); other overlaps are not allowed.
+ * rows >= 0 (0 is a no-op), 1 <= hidden <= 65536.
+ */
+int rmsnorm_residual(const void* x, const void* residual, const void* weight, void* out,
+                     void* residual_out, int64_t rows, int64_t hidden, float eps, fuse_dtype dt,
+                     void* stream);
+
+/* ------------------------------------------------------------------------
+ * QKV split + transpose + rotate-half RoPE ("TeleTron", section 3.1: QKV
+ * projection -> head split -> RoPE).
+ * qkv: [tokens, 3, heads, head_dim] (q block, k block, v block per token).
+ * q, k, v: [heads, tokens, head_dim].  Token t sits at position pos0 + t.
+ * For i < head_dim/2, theta = (pos0 + t) * base^(-2i/head_dim):
+ *   o[i]              = x[i] cos(theta) - x[i + head_dim/2] sin(theta)
+ *   o[i + head_dim/2] = x[i + head_dim/2] cos(theta) + x[i] sin(theta)
+ * on q and k; v is copied bit for bit.  cos/sin come from a table the
+ * library builds on the device in fp64 and keeps (fp32, 2 * positions *
+ * head_dim/2 * 4 bytes) per device, base and head_dim; it grows as larger
+ * positions are asked for.  dt: f16, bf16 or f32.  head_dim even,
+ * 2 <= head_dim <= 1024; heads >= 1; tokens >= 0; 0 <= pos0 and
+ * pos0 + tokens <= 2^24.
+ */
+int rope_qkv_split(const void* qkv, void* q, void* k, void* v, int64_t tokens, int heads,
+                   int head_dim, int64_t pos0, float base, fuse_dtype dt, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Detection-head decode ("DeepJIT" section 1.1: the sigmoid / exp / mul /
+ * add / slice / concat / cast tail of a detection head, fused into one
+ * kernel).
+ * feats[s] (device): [1, na*no, H_s, W_s] of dtype in_dt, channel a*no + k.
+ * hw (host): nscales pairs (H_s, W_s); strides (host): nscales floats;
+ * anchors (host): nscales*na pairs (w, h).
+ * out (device): fp32 [sum_s na*H_s*W_s, no]; row = off_s + a*H_s*W_s +
+ * y*W_s + x with the scales concatenated in order; for p = sigmoid(feat):
+ *   k = 0: (2p - 0.5 + x) * stride    k = 1: (2p - 0.5 + y) * stride
+ *   k = 2: (2p)^2 * anchor_w          k = 3: (2p)^2 * anchor_h
+ *   k >= 4: p
+ * 1 <= nscales <= 8, 1 <= na <= 16, 5 <= no <= 1024.  The strides and
+ * anchors are baked into the kernel (a new set compiles a new kernel).
+ */
+int detect_decode(const void* const* feats, const int* hw, const float* strides,
+                  const float* anchors, int nscales, int na, int no, fuse_dtype in_dt, void* out,
+                  void* stream);
+
+/* ------------------------------------------------------------------------
+ * ChannelShuffle ("算子与运行时", section 2): out[n, j*g + i] =
+ * in[n, i*(c/g) + j] for i < g, j < c/g, on contiguous NCHW; a bit-exact
+ * copy of whole H*W planes.  c % groups == 0.  in and out must not overlap.
+ */
+int channel_shuffle(const void* in, void* out, int64_t n, int64_t c, int64_t h, int64_t w,
+                    int groups, fuse_dtype dt, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics ("算子与运行时", section 6.5: per-operator counters).
+ */
+/* Message of the last failed call on this thread ("" if none).  For
+ * FUSE_E_COMPILE it holds the NVRTC log. */
+const char* fuse_last_error(void);
+
+/* Process-wide counters since load (any pointer may be NULL). */
+int fuse_stats(int64_t* compiles, int64_t* cache_hits, int64_t* launches, double* compile_ms);
+
+/* Number of SMs the library sizes persistent grids for on the current
+ * device (152 on GB300), or 152 when no device is visible. */
+int fuse_device_sms(int* sms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FUSE_H */

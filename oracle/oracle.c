@@ -257,7 +257,7 @@ void oracle_chain_eval(int n_ops, const int* ops, const double* args, const int*
  * 3 = unpinned.  Returns the number of failures; counts[0..3] gets the
  * number of elements in each class.
  */
-#define MAXB 8
+#define MAXB 16
 typedef struct {
   double v, e;
 } branch_t;
@@ -303,7 +303,12 @@ static int step_branch(int op, branch_t s, double b, double c, int out_dt_unused
       break;
     case OP_SIGMOID: {
       vn = 1.0 / (1.0 + exp(-v));
-      En = E / 4 + 8 * U32 * (vn + E / 4) + ETA;
+      /* |sigma'(x)| = sigma(x)(1 - sigma(x)) is largest at x = 0: take its
+         maximum over [v - E, v + E] (mean value theorem) */
+      double xm = (v - E <= 0.0 && v + E >= 0.0) ? 0.0 : (v > 0.0 ? v - E : v + E);
+      double sm = 1.0 / (1.0 + exp(-xm));
+      double dmax = sm * (1.0 - sm);
+      En = dmax * E + 8 * U32 * (vn + dmax * E) + ETA;
       if (-(v - E) >= 88.0) { /* exp(-x) may overflow in fp32: result may be 0 */
         double hi = 1.0 / (1.0 + exp(-(v + E)));
         if (hi * (1 + 8 * U32) > En) En = hi * (1 + 8 * U32) + ETA;
@@ -319,14 +324,19 @@ static int step_branch(int op, branch_t s, double b, double c, int out_dt_unused
         return 1;
       }
       /* the device value rounds to one of the representable values in
-         [lo, hi]; follow the two ends when they are neighbours */
-      double mid_up = round_to(dt, lo + (hi - lo) * 0.5);
-      if (!(mid_up == lo || mid_up == hi)) return -1; /* more than two outcomes */
-      nb[0].v = fp32_range(lo);
-      nb[0].e = 0.0;
-      nb[1].v = fp32_range(hi);
-      nb[1].e = 0.0;
-      return 2;
+         [lo, hi] (rounding is monotone): follow each of them */
+      if (dt == DT_F32) return -1; /* a cast to f32 does not round */
+      int olo = f16_order(dt == DT_F16 ? f16_bits_of(lo) : bf16_bits_of(lo));
+      int ohi = f16_order(dt == DT_F16 ? f16_bits_of(hi) : bf16_bits_of(hi));
+      if (ohi - olo + 1 > MAXB) return -1;
+      int nn = 0;
+      for (int o = olo; o <= ohi; ++o) {
+        uint16_t bits = o >= 0 ? (uint16_t)o : (uint16_t)(0x8000 | (-o));
+        nb[nn].v = fp32_range(dt == DT_F16 ? f16_bits_to_double(bits) : bf16_bits_to_double(bits));
+        nb[nn].e = 0.0;
+        ++nn;
+      }
+      return nn;
     }
     default:
       return -1;
@@ -393,7 +403,7 @@ int64_t oracle_chain_check(int n_ops, const int* ops, const double* args, const 
       cls = 0;
     } else {
       /* rule 2: running error bound with branches */
-      branch_t cur[MAXB], nxt[2 * MAXB];
+      branch_t cur[MAXB], nxt[MAXB * MAXB];
       int nc = 1, unpinned = 0;
       cur[0].v = load_elem(inputs[0], in_dt[0], e0);
       cur[0].e = 0.0;

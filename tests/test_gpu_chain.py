@@ -1,0 +1,207 @@
+"""GPU parity of fused elementwise chains and ChannelShuffle against the oracle.
+
+Every case runs through the C ABI (fuse_compile / fuse_launch /
+channel_shuffle) on seeded inputs from `workloads`, and is compared element by
+element with the fp64 oracle: bit-exact for add -> relu -> scale (whose exact
+result is one fp32 rounding) and for the shuffle copies; the flat tolerance or
+the oracle's running error bound for random chains.  Sizes span several
+chunks plus ragged remainders and tails; odd offsets take the scalar kernel;
+canary bytes after each output catch writes past the end.
+"""
+import numpy as np
+import pytest
+import torch
+
+import elementwise_chain_jit_gb300 as F
+import oracle
+import workloads
+from gpu_util import Guarded, misaligned_copy, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_chain(spec, dt, inputs, shape, offset=0):
+    c = F.fuse_compile(spec, shape, dt)
+    dev = [to_dev(a, d) for a, d in zip(inputs, c.in_dtypes)]
+    if offset:
+        dev = [misaligned_copy(t, offset) for t in dev]
+    n = int(np.prod(shape))
+    out = Guarded(n, c.out_dtype, offset_elems=offset)
+    F.fuse_launch(c, dev, out.t)
+    torch.cuda.synchronize()
+    assert out.canary_ok(), "write outside the output"
+    return to_host(out.t, c.out_dtype), c
+
+
+# ------------------------------------------------------------ add -> relu -> scale
+
+@pytest.mark.parametrize("n", [1 << 20, 1, 7, 67, 4099, (1 << 20) + 7])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_add_relu_scale_bit_exact(n, offset):
+    cfg = workloads.ADD_RELU_SCALE
+    a = workloads.uniform(n, cfg["lo"], cfg["hi"], cfg["seed"], F.F32)
+    b = workloads.uniform(n, cfg["lo"], cfg["hi"], cfg["seed"] + 100, F.F32)
+    got, _ = _run_chain(cfg["spec"], F.F32, [a, b], (n,), offset)
+    want, _ = oracle.chain_eval(cfg["spec"], F.F32, [a, b], (n,))
+    assert np.array_equal(got, oracle.store(want, F.F32))
+
+
+def test_add_relu_scale_golden_on_device():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "add_relu_scale.txt")
+    rows = [l.split("#", 1)[0].split() for l in open(path)]
+    rows = [r for r in rows if r]
+    num = lambda s: float.fromhex(s) if "0x" in s else float(s)  # noqa: E731
+    a = np.array([num(r[0]) for r in rows], np.float32)
+    b = np.array([num(r[1]) for r in rows], np.float32)
+    want = np.array([num(r[2]) for r in rows], np.float32)
+    got, _ = _run_chain("add;relu;scale:0.5", F.F32, [a, b], (len(a),))
+    assert np.array_equal(got, want) and not np.any(np.signbit(got))
+
+
+# ------------------------------------------------------------ random chains
+
+def _check(spec, dt, inputs, shape, got, idx=None):
+    fails, counts, cls = oracle.chain_check(spec, dt, inputs, shape, got, idx)
+    assert fails == 0, (spec, counts, np.nonzero(cls == 2)[0][:10])
+    n = got.size
+    assert counts[3] <= max(2, n // 1000), (spec, counts)  # unpinned elements are rare
+    return counts
+
+
+@pytest.mark.parametrize("length", workloads.CHAIN_LENGTHS)
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+@pytest.mark.parametrize("n", [1, 33, 4099, (1 << 16) + 7])
+def test_random_chain_small(length, seed, n):
+    spec, dt = workloads.random_chain(length, seed)
+    inputs, _ = workloads.chain_inputs(spec, dt, n, seed)
+    got, _ = _run_chain(spec, dt, inputs, (n,))
+    _check(spec, dt, inputs, (n,), got)
+
+
+@pytest.mark.parametrize("length", [2, 8, 32])
+def test_random_chain_unaligned(length):
+    spec, dt = workloads.random_chain(length, 7)
+    n = 10_007
+    inputs, _ = workloads.chain_inputs(spec, dt, n, 7)
+    got, _ = _run_chain(spec, dt, inputs, (n,), offset=1)
+    _check(spec, dt, inputs, (n,), got)
+
+
+@pytest.mark.parametrize("spec,dt", [
+    ("cast:bf16;add;exp;cast:f32", F.F32),
+    ("mul;cast:bf16;sigmoid", F.F16),
+    ("add;mul;add;relu;scale:0.25;add", F.BF16),
+])
+def test_bf16_chains(spec, dt):
+    n = 70_001
+    inputs, _ = workloads.chain_inputs(spec, dt, n, 11)
+    got, _ = _run_chain(spec, dt, inputs, (n,))
+    _check(spec, dt, inputs, (n,), got)
+
+
+@pytest.mark.parametrize("n", workloads.FLAT_SIZES)
+@pytest.mark.parametrize("length", [1, 8, 32])
+def test_flat_chain_full_sizes_sampled(n, length):
+    """Full workload sizes; the oracle checks a sample (first/last elements,
+    the ragged end, and random positions)."""
+    spec, dt = workloads.random_chain(length, 5)
+    c = F.fuse_compile(spec, (n,), dt)
+    dev = [workloads.device_uniform(n, -2.0, 2.0, 1000 * j + length, d)
+           for j, d in enumerate(c.in_dtypes)]
+    out = Guarded(n, c.out_dtype)
+    F.fuse_launch(c, dev, out.t)
+    torch.cuda.synchronize()
+    assert out.canary_ok()
+    g = np.random.default_rng(n + length)
+    idx = np.unique(np.concatenate([np.arange(min(n, 4096)), np.arange(max(0, n - 4096), n),
+                                    g.integers(0, n, 200_000)]))
+    it = torch.from_numpy(idx).cuda()
+    ins = [to_host(t[it], d) for t, d in zip(dev, c.in_dtypes)]
+    got = to_host(out.t[it], c.out_dtype)
+    _check(spec, dt, ins, (len(idx),), got)
+
+
+# ------------------------------------------------------------ ChannelShuffle prologue
+
+@pytest.mark.parametrize("shape,groups", [
+    ((2, 8, 4, 4), 4), ((1, 12, 3, 5), 3), ((3, 6, 1, 1), 2), ((2, 16, 8, 8), 16),
+    ((2, 16, 8, 8), 1), ((1, 4, 7, 9), 2),
+])
+@pytest.mark.parametrize("length", [0, 1, 4])
+def test_shuffle_chain_small(shape, groups, length):
+    body, dt = workloads.random_chain(length, groups, start_dtype=F.F16) if length else ("", F.F16)
+    spec = f"shuffle:{groups};" + body
+    n = int(np.prod(shape))
+    inputs, _ = workloads.chain_inputs(spec, dt, n, 3)
+    got, _ = _run_chain(spec, dt, inputs, shape)
+    if length == 0:
+        assert np.array_equal(got, oracle.channel_shuffle(inputs[0].reshape(shape), groups)
+                              .reshape(-1))
+    else:
+        _check(spec, dt, inputs, shape, got)
+
+
+@pytest.mark.parametrize("length", workloads.CHAIN_LENGTHS)
+def test_shuffle_chain_full_config(length):
+    cfg = workloads.SHUFFLE_CHAIN
+    body, dt = workloads.random_chain(length, 9, start_dtype=F.F16)
+    spec = f"shuffle:{cfg['groups']};{body}"
+    n = int(np.prod(cfg["shape"]))
+    inputs, _ = workloads.chain_inputs(spec, dt, n, cfg["seed"])
+    got, _ = _run_chain(spec, dt, inputs, cfg["shape"])
+    _check(spec, dt, inputs, cfg["shape"], got)
+
+
+# ------------------------------------------------------------ channel_shuffle entry point
+
+@pytest.mark.parametrize("shape,groups,dt", [
+    ((32, 256, 56, 56), 4, F.F16), ((2, 24, 5, 7), 3, F.F16), ((4, 8, 16, 16), 2, F.F32),
+    ((1, 64, 9, 9), 8, F.BF16), ((2, 6, 1, 1), 6, F.F16),
+])
+def test_channel_shuffle_bit_exact(shape, groups, dt):
+    x = workloads.uniform(shape, -2, 2, 17, dt)
+    xd = to_dev(x.reshape(-1), dt)
+    out = Guarded(x.size, dt)
+    F.channel_shuffle(xd, out.t, groups, dt, shape=shape)
+    torch.cuda.synchronize()
+    assert out.canary_ok()
+    want = oracle.channel_shuffle(x, groups).reshape(-1)
+    assert np.array_equal(to_host(out.t, dt), want)
+    # round trip with the inverse group count
+    back = Guarded(x.size, dt)
+    F.channel_shuffle(out.t, back.t, shape[1] // groups, dt, shape=shape)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host(back.t, dt), x.reshape(-1))
+
+
+def test_channel_shuffle_unaligned():
+    shape, groups, dt = (2, 8, 6, 6), 4, F.F16
+    x = workloads.uniform(shape, -2, 2, 18, dt)
+    xd = misaligned_copy(to_dev(x.reshape(-1), dt), 1)
+    out = Guarded(x.size, dt, offset_elems=3)
+    F.channel_shuffle(xd, out.t, groups, dt, shape=shape)
+    torch.cuda.synchronize()
+    assert out.canary_ok()
+    assert np.array_equal(to_host(out.t, dt), oracle.channel_shuffle(x, groups).reshape(-1))
+
+
+def test_empty_chain_is_noop():
+    c = F.fuse_compile("add;relu", [0], F.F32)
+    F.fuse_launch(c, [0, 0], 0)
+    torch.cuda.synchronize()
+
+
+def test_launch_count_is_one_per_chain():
+    spec, dt = workloads.random_chain(16, 1)
+    n = 1 << 20
+    c = F.fuse_compile(spec, (n,), dt)
+    dev = [workloads.device_uniform(n, -2, 2, j, d) for j, d in enumerate(c.in_dtypes)]
+    out = torch.empty(n, dtype={0: torch.float32, 1: torch.float16, 2: torch.bfloat16}[c.out_dtype],
+                      device="cuda")
+    before = F.fuse_stats()
+    for _ in range(5):
+        F.fuse_launch(c, dev, out)
+    after = F.fuse_stats()
+    assert after["launches"] - before["launches"] == 5
+    assert after["compiles"] == before["compiles"]

@@ -1,0 +1,210 @@
+"""GPU parity of the fixed entry points (rmsnorm_residual, rope_qkv_split,
+detect_decode) against the fp64 oracle, through the C ABI.
+
+Tolerances (from the output dtypes): bf16 outputs within 8e-3 relative --
+for RoPE relative to the sum of the magnitudes of the two terms, since a
+rotation can cancel; fp32 detect outputs within 1e-6 relative to the sum of
+the magnitudes of their terms.  Pure copies (v, the updated residual) are
+bit-exact.  Full-size workloads are checked on sampled rows/tokens.
+"""
+import numpy as np
+import pytest
+import torch
+
+import elementwise_chain_jit_gb300 as F
+import oracle
+import workloads
+from gpu_util import Guarded, misaligned_copy, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+# ------------------------------------------------------------ RMSNorm
+
+def _rms_case(rows, hidden, dt, seed, offset=0, inplace=False, eps=1e-6):
+    x = workloads.normal((rows, hidden), 0, 1, seed, dt)
+    r = workloads.normal((rows, hidden), 0, 1, seed + 1, dt)
+    w = workloads.normal(hidden, 1, 0.1, seed + 2, dt)
+    xd, rd, wd = (to_dev(a.reshape(-1), dt) for a in (x, r, w))
+    if offset:
+        xd, rd, wd = (misaligned_copy(t, offset) for t in (xd, rd, wd))
+    out = Guarded(rows * hidden, dt, offset_elems=offset)
+    if inplace:
+        F.rmsnorm_residual(xd, rd, wd, out.t, rd, eps, dt, rows=rows, hidden=hidden)
+        res_out_t = rd
+    else:
+        ro = Guarded(rows * hidden, dt, offset_elems=offset)
+        F.rmsnorm_residual(xd, rd, wd, out.t, ro.t, eps, dt, rows=rows, hidden=hidden)
+        res_out_t = ro.t
+    torch.cuda.synchronize()
+    assert out.canary_ok()
+    y, h = oracle.rmsnorm_residual(x, r, w, dt, eps)
+    got_y = oracle.to_double(to_host(out.t, dt), dt).reshape(rows, hidden)
+    got_r = to_host(res_out_t, dt).reshape(rows, hidden)
+    assert np.array_equal(got_r, oracle.store(h, dt))  # one rounding of an exact sum
+    rel = 8e-3 if dt == F.BF16 else (2e-3 if dt == F.F16 else 1e-5)
+    np.testing.assert_allclose(got_y, y, rtol=rel, atol=0)
+    return got_y
+
+
+@pytest.mark.parametrize("rows,hidden", [(3, 4096), (67, 4096), (5, 1000), (4, 7), (2, 65536),
+                                         (9, 8192), (1, 1)])
+@pytest.mark.parametrize("dt", [F.BF16, F.F16, F.F32])
+def test_rmsnorm_shapes(rows, hidden, dt):
+    _rms_case(rows, hidden, dt, 100 + hidden % 97)
+
+
+def test_rmsnorm_unaligned_and_in_place():
+    _rms_case(11, 4096, F.BF16, 5, offset=1)
+    _rms_case(11, 4096, F.BF16, 6, inplace=True)
+
+
+def test_rmsnorm_unit_weight_rms_is_one():
+    rows, hidden = 256, 4096
+    x = workloads.normal((rows, hidden), 0, 1, 41, F.BF16)
+    r = workloads.normal((rows, hidden), 0, 1, 42, F.BF16)
+    w = oracle.store(np.ones(hidden), F.BF16)
+    out = torch.empty(rows * hidden, dtype=torch.bfloat16, device="cuda")
+    ro = torch.empty_like(out)
+    F.rmsnorm_residual(to_dev(x.reshape(-1), F.BF16), to_dev(r.reshape(-1), F.BF16),
+                       to_dev(w, F.BF16), out, ro, 1e-6, F.BF16, rows=rows, hidden=hidden)
+    y = out.float().view(rows, hidden).double()
+    rms = torch.sqrt((y * y).mean(dim=1))
+    # bf16 rounding of each element moves the row RMS by well under 2^-9
+    assert torch.all((rms - 1).abs() < 2e-3), rms
+
+
+def test_rmsnorm_full_config_sampled_rows():
+    cfg = workloads.RMSNORM
+    rows, hidden = cfg["rows"], cfg["hidden"]
+    x = workloads.device_normal((rows, hidden), 0, 1, cfg["seed"], F.BF16)
+    r = workloads.device_normal((rows, hidden), 0, 1, cfg["seed"] + 1, F.BF16)
+    w = workloads.device_normal((hidden,), 1, 0.1, cfg["seed"] + 2, F.BF16)
+    out = torch.empty_like(x)
+    ro = torch.empty_like(x)
+    F.rmsnorm_residual(x, r, w, out, ro, cfg["eps"], F.BF16)
+    torch.cuda.synchronize()
+    g = np.random.default_rng(3)
+    sel = np.unique(np.concatenate([[0, 1, rows - 1], g.integers(0, rows, 61)]))
+    st = torch.from_numpy(sel).cuda()
+    xs, rs = to_host(x[st], F.BF16), to_host(r[st], F.BF16)
+    y, h = oracle.rmsnorm_residual(xs, rs, to_host(w, F.BF16), F.BF16, cfg["eps"])
+    assert np.array_equal(to_host(ro[st], F.BF16), oracle.store(h, F.BF16))
+    np.testing.assert_allclose(oracle.to_double(to_host(out[st], F.BF16), F.BF16), y, rtol=8e-3)
+
+
+# ------------------------------------------------------------ QKV split + RoPE
+
+def _rope_check(qkv_host, heads, hd, pos0, dt, got_q, got_k, got_v, tokens_idx=None, base=1e4):
+    tokens = qkv_host.shape[0]
+    pos = pos0 + (np.arange(tokens) if tokens_idx is None else tokens_idx)
+    q, k, v, qm, km = oracle.rope_qkv_split(qkv_host, dt, heads, hd, pos, base)
+    rel = 8e-3 if dt == F.BF16 else (2e-3 if dt == F.F16 else 1e-5)
+    for got, want, mag in ((got_q, q, qm), (got_k, k, km)):
+        gd = oracle.to_double(got, dt).reshape(want.shape)
+        err = np.abs(gd - want)
+        bad = err > rel * mag + 1e-30
+        assert not bad.any(), (np.argwhere(bad)[:5], err[bad][:5], mag[bad][:5])
+    assert np.array_equal(got_v.reshape(v.shape), oracle.store(v, dt))
+
+
+@pytest.mark.parametrize("tokens,heads,hd,pos0", [
+    (5, 4, 128, 0), (37, 3, 64, 32000), (8, 2, 80, 7), (3, 1, 6, 100), (16, 32, 128, 32752),
+    (2, 2, 256, 1_000_000),
+])
+@pytest.mark.parametrize("dt", [F.BF16, F.F16, F.F32])
+def test_rope_shapes(tokens, heads, hd, pos0, dt):
+    qkv = workloads.normal((tokens, 3 * heads * hd), 0, 1, tokens + hd, dt)
+    qd = to_dev(qkv.reshape(-1), dt)
+    outs = [Guarded(heads * tokens * hd, dt) for _ in range(3)]
+    F.rope_qkv_split(qd, outs[0].t, outs[1].t, outs[2].t, heads, hd, pos0, 10000.0, dt,
+                     tokens=tokens)
+    torch.cuda.synchronize()
+    assert all(o.canary_ok() for o in outs)
+    _rope_check(qkv, heads, hd, pos0, dt, *(to_host(o.t, dt) for o in outs))
+
+
+def test_rope_unaligned_and_position_zero_identity():
+    tokens, heads, hd, dt = 9, 4, 128, F.BF16
+    qkv = workloads.normal((tokens, 3 * heads * hd), 0, 1, 77, dt)
+    qd = misaligned_copy(to_dev(qkv.reshape(-1), dt), 1)
+    outs = [Guarded(heads * tokens * hd, dt, offset_elems=1) for _ in range(3)]
+    F.rope_qkv_split(qd, outs[0].t, outs[1].t, outs[2].t, heads, hd, 0, 10000.0, dt, tokens=tokens)
+    torch.cuda.synchronize()
+    assert all(o.canary_ok() for o in outs)
+    got = [to_host(o.t, dt) for o in outs]
+    _rope_check(qkv, heads, hd, 0, dt, *got)
+    # token 0 is at position 0: q and k are copied exactly
+    src = qkv.reshape(tokens, 3, heads, hd)
+    assert np.array_equal(got[0].reshape(heads, tokens, hd)[:, 0], src[0, 0])
+    assert np.array_equal(got[1].reshape(heads, tokens, hd)[:, 0], src[0, 1])
+
+
+def test_rope_full_config_sampled_tokens():
+    cfg = workloads.ROPE
+    T, H, D = cfg["tokens"], cfg["heads"], cfg["head_dim"]
+    qkv = workloads.device_normal((T, 3 * H * D), 0, 1, cfg["seed"], F.BF16)
+    q = torch.empty(H * T * D, dtype=torch.bfloat16, device="cuda")
+    k = torch.empty_like(q)
+    v = torch.empty_like(q)
+    F.rope_qkv_split(qkv, q, k, v, H, D, cfg["pos0"], cfg["base"], F.BF16)
+    torch.cuda.synchronize()
+    g = np.random.default_rng(4)
+    sel = np.unique(np.concatenate([[0, 1, T - 1], g.integers(0, T, 61)]))
+    st = torch.from_numpy(sel).cuda()
+    sub = lambda t: to_host(t.view(H, T, D)[:, st].contiguous(), F.BF16)  # noqa: E731
+    _rope_check(to_host(qkv[st], F.BF16), H, D, cfg["pos0"], F.BF16, sub(q), sub(k), sub(v),
+                tokens_idx=sel)
+
+
+# ------------------------------------------------------------ detection decode
+
+def _detect_case(hw, dt, seed, offset=0, na=3, no=85):
+    strides = [8.0 * 2 ** s for s in range(len(hw))]
+    anchors = workloads.detect_anchors(strides, na)
+    feats = [workloads.normal((1, na * no, h, w), 0, 2.0, seed + s, dt) for s, (h, w) in enumerate(hw)]
+    fd = [to_dev(f.reshape(-1), dt) for f in feats]
+    if offset:
+        fd = [misaligned_copy(t, offset) for t in fd]
+    rows = sum(na * h * w for h, w in hw)
+    out = Guarded(rows * no, F.F32, offset_elems=offset)
+    F.detect_decode(fd, hw, strides, anchors, na, no, out.t, dt)
+    torch.cuda.synchronize()
+    assert out.canary_ok()
+    want, mag = oracle.detect_decode(feats, dt, strides, anchors, na, no)
+    got = to_host(out.t, F.F32).reshape(rows, no).astype(np.float64)
+    err = np.abs(got - want)
+    bad = err > 1e-6 * mag
+    assert not bad.any(), (np.argwhere(bad)[:5], err[bad][:5], mag[bad][:5])
+
+
+def test_detect_full_config():
+    cfg = workloads.DETECT
+    _detect_case(cfg["hw"], F.F16, cfg["seed"])
+
+
+@pytest.mark.parametrize("hw", [[(1, 1)], [(3, 3), (2, 1), (1, 2)], [(8, 8), (4, 4), (2, 2)],
+                                [(13, 7), (5, 9)], [(80, 80), (40, 40), (20, 20), (10, 10)]])
+@pytest.mark.parametrize("dt", [F.F16, F.F32, F.BF16])
+def test_detect_shapes(hw, dt):
+    _detect_case(hw, dt, 11)
+
+
+def test_detect_unaligned_and_other_heads():
+    _detect_case([(16, 16), (8, 8)], F.F16, 12, offset=1)
+    _detect_case([(10, 12)], F.F16, 13, na=2, no=6)
+    _detect_case([(4, 6)], F.F32, 14, na=1, no=1024)
+
+
+def test_detect_sigmoid_zero_closed_form():
+    hw = [(8, 8), (4, 4), (2, 2)]
+    strides = [8.0, 16.0, 32.0]
+    anchors = workloads.detect_anchors(strides)
+    fd = [torch.zeros(255 * h * w, dtype=torch.float16, device="cuda") for h, w in hw]
+    rows = sum(3 * h * w for h, w in hw)
+    out = torch.empty(rows * 85, dtype=torch.float32, device="cuda")
+    F.detect_decode(fd, hw, strides, anchors, 3, 85, out, F.F16)
+    o = out.view(rows, 85).cpu().numpy()
+    assert np.all(o[:, 4:] == 0.5)
+    assert o[0, 0] == 4.0 and o[0, 1] == 4.0 and o[0, 2] == anchors[0, 0, 0]
+    assert o[3 * 64, 0] == 8.0  # first row of scale 1: (0.5 + 0) * 16
