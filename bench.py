@@ -1,0 +1,665 @@
+#!/usr/bin/env python
+"""Benchmark of the fused-chain hot path on GB300.
+
+One step runs every fused workload once, at full size, through the C ABI:
+  * the chain sweep on flat tensors of 2^28 + 7 elements, lengths 1..32
+    (random chains over add/mul/sigmoid/exp/relu/scale/cast, inputs U[-2,2]);
+  * the same sweep preceded by ChannelShuffle(4) on fp16 [32,256,56,56];
+  * residual add + RMSNorm + bf16 cast on [16384, 4096];
+  * QKV split + transpose + RoPE on bf16 [32768, 3*32*128];
+  * add -> relu -> scale on two fp32 vectors of 2^20;
+  * the 3-scale detection-head decode into fp32 [1, 25200, 85].
+`value` is the step's algorithmic minimum bytes (each input read once, each
+output written once) divided by the device time of the step.  Inputs are
+larger than L2 (the step streams ~29 GB, which evicts the two small
+workloads' buffers between their uses).
+
+Alongside: per-workload fused time and GB/s, the unfused per-op sequence
+(one kernel per op with a full HBM round trip: the library's own length-1
+chains for elementwise chains, PyTorch eager ops for the structured
+workloads), the roofline of the dominant kernel, an end-to-end number with
+host buffers, and the CPU oracle timed on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused-chain HBM GB/s (% of GB300 peak) and µs/chain vs unfused per-op"
+UNIT = "GB/s"
+WORKLOAD = ("all fused chains at full size: chain sweep L=1..32 on 2^28+7 elements and after "
+            "ChannelShuffle(4) on fp16 [32,256,56,56]; RMSNorm+residual bf16 [16384,4096]; "
+            "QKV split+RoPE bf16 [32768,3x32x128]; add-relu-scale fp32 2^20; detect decode "
+            "3 scales fp16 -> fp32 [1,25200,85]")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- helpers
+
+def launch_overhead(t_unfused: float, t_fused: float, k: int):
+    """Per-call fixed cost L and work T from the unfused time K*L + T and the
+    fused time L + T (the launch-cost model of the NaiveRT analysis):
+    L = (t_unfused - t_fused) / (K - 1), T = t_fused - L."""
+    if k <= 1:
+        return 0.0, t_fused
+    L = (t_unfused - t_fused) / (k - 1)
+    return L, t_fused - L
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.2)
+        self.out = ""
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- workload
+
+class Item:
+    """One fused workload: a single launch of the library."""
+
+    def __init__(self, name, nbytes, fused, unfused=None, n_unfused=0, kernel=None):
+        self.name, self.bytes, self.fused = name, nbytes, fused
+        self.unfused, self.n_unfused = unfused, n_unfused
+        self.kernel = kernel
+        self.inputs, self.outputs = [], []   # device tensors (for the end-to-end copies)
+
+
+def _tdt(dt):
+    import torch
+    return {0: torch.float32, 1: torch.float16, 2: torch.bfloat16}[dt]
+
+
+def _esz(dt):
+    return 4 if dt == 0 else 2
+
+
+def build_items(dev, with_unfused=True, only=None, flat_elems=None):
+    """The step's workloads; `only` (a regex) keeps the matching ones and
+    `flat_elems` changes the flat chains' size (both for profiling a single
+    kernel on a smaller case)."""
+    import re
+
+    import torch
+
+    import elementwise_chain_jit_gb300 as F
+    import workloads as W
+
+    items = []
+
+    def want(name):
+        return only is None or re.search(only, name) is not None
+
+    def chain_item(name, spec, dt, shape, seed, lo=-2.0, hi=2.0, dev_inputs=None):
+        n = int(np.prod(shape))
+        c = F.fuse_compile(spec, shape, dt)
+        ins = dev_inputs or [W.device_uniform(n, lo, hi, seed * 131 + j, d, dev)
+                             for j, d in enumerate(c.in_dtypes)]
+        out = torch.empty(n, dtype=_tdt(c.out_dtype), device=dev)
+        nbytes = sum(n * _esz(d) for d in c.in_dtypes) + n * _esz(c.out_dtype)
+        it = Item(name, nbytes, lambda: F.fuse_launch(c, ins, out), kernel=("chain", spec, shape, dt))
+        it.inputs, it.outputs = ins, [out]
+        if with_unfused:
+            it.unfused, it.n_unfused = unfused_chain(spec, dt, shape, ins, out)
+        return it
+
+    # chain sweep, flat, 2^28 + 7
+    n_flat = flat_elems or W.FLAT_SIZES[-1]
+    for L in W.CHAIN_LENGTHS:
+        spec, dt = W.random_chain(L, 5)
+        if want(f"flat_chain_L{L}_n{n_flat}"):
+            items.append(chain_item(f"flat_chain_L{L}_n{n_flat}", spec, dt, (n_flat,), 100 + L))
+    # chain sweep after ChannelShuffle(4), fp16 [32,256,56,56]
+    cfg = W.SHUFFLE_CHAIN
+    for L in W.CHAIN_LENGTHS:
+        body, dt = W.random_chain(L, 9, start_dtype=W.F16)
+        if want(f"shuffle_chain_L{L}"):
+            items.append(chain_item(f"shuffle_chain_L{L}", f"shuffle:{cfg['groups']};{body}", dt,
+                                    cfg["shape"], 200 + L))
+    if want("rmsnorm_residual_16384x4096_bf16"):
+        items.append(_rms_item(dev, with_unfused))
+    if want("rope_qkv_split_32768x32x128_bf16"):
+        items.append(_rope_item(dev, with_unfused))
+    ac = W.ADD_RELU_SCALE
+    if want("add_relu_scale_1M_f32"):
+        items.append(chain_item("add_relu_scale_1M_f32", ac["spec"], W.F32, (ac["n"],), ac["seed"],
+                                ac["lo"], ac["hi"]))
+    if want("detect_decode_3scale"):
+        items.append(_detect_item(dev, with_unfused))
+    return items
+
+
+def _rms_item(dev, with_unfused):
+    import torch
+
+    import elementwise_chain_jit_gb300 as F
+    import workloads as W
+    rc = W.RMSNORM
+    rows, hidden = rc["rows"], rc["hidden"]
+    x = W.device_normal((rows, hidden), 0, 1, rc["seed"], W.BF16, dev)
+    r = W.device_normal((rows, hidden), 0, 1, rc["seed"] + 1, W.BF16, dev)
+    w = W.device_normal((hidden,), 1, 0.1, rc["seed"] + 2, W.BF16, dev)
+    y = torch.empty_like(x)
+    ro = torch.empty_like(x)
+    it = Item("rmsnorm_residual_16384x4096_bf16", 4 * rows * hidden * 2 + hidden * 2,
+              lambda: F.rmsnorm_residual(x, r, w, y, ro, rc["eps"], W.BF16),
+              kernel=("rmsnorm",))
+    it.inputs, it.outputs = [x, r, w], [y, ro]
+    if with_unfused:
+        def rms_unfused():
+            h = x + r
+            hf = h.float()
+            ms = hf.pow(2).mean(-1, keepdim=True)
+            rstd = torch.rsqrt(ms + rc["eps"])
+            return (hf * rstd * w.float()).to(torch.bfloat16), h
+        it.unfused, it.n_unfused = rms_unfused, 10
+    return it
+
+
+def _rope_item(dev, with_unfused):
+    import torch
+
+    import elementwise_chain_jit_gb300 as F
+    import workloads as W
+    pc = W.ROPE
+    T, H, D = pc["tokens"], pc["heads"], pc["head_dim"]
+    qkv = W.device_normal((T, 3 * H * D), 0, 1, pc["seed"], W.BF16, dev)
+    q, k, v = (torch.empty(H * T * D, dtype=torch.bfloat16, device=dev) for _ in range(3))
+    it = Item("rope_qkv_split_32768x32x128_bf16", 2 * T * 3 * H * D * 2,
+              lambda: F.rope_qkv_split(qkv, q, k, v, H, D, pc["pos0"], pc["base"], W.BF16),
+              kernel=("rope",))
+    it.inputs, it.outputs = [qkv], [q, k, v]
+    if with_unfused:
+        pos = torch.arange(T, device=dev, dtype=torch.float64)
+        inv = pc["base"] ** (-torch.arange(0, D, 2, device=dev, dtype=torch.float64) / D)
+        ang = pos[:, None] * inv[None, :]
+        cos = torch.cat([ang.cos(), ang.cos()], -1).float()
+        sin = torch.cat([ang.sin(), ang.sin()], -1).float()
+
+        def rope_unfused():
+            t = qkv.view(T, 3, H, D)
+            outs = [t[:, i].transpose(0, 1).contiguous() for i in range(3)]
+            for i in range(2):
+                xf = outs[i].float()
+                rh = torch.cat([-xf[..., D // 2:], xf[..., :D // 2]], -1)
+                outs[i] = (xf * cos + rh * sin).to(torch.bfloat16)
+            return outs
+        it.unfused, it.n_unfused = rope_unfused, 15
+    return it
+
+
+def _detect_item(dev, with_unfused):
+    import torch
+
+    import elementwise_chain_jit_gb300 as F
+    import workloads as W
+    dc = W.DETECT
+    anchors = W.detect_anchors(dc["strides"], dc["na"])
+    feats = [W.device_normal((1, dc["na"] * dc["no"], h, w_), 0, dc["sd"], dc["seed"] + s, W.F16, dev)
+             for s, (h, w_) in enumerate(dc["hw"])]
+    nrows = sum(dc["na"] * h * w_ for h, w_ in dc["hw"])
+    dout = torch.empty(nrows * dc["no"], dtype=torch.float32, device=dev)
+    it = Item("detect_decode_3scale", sum(f.numel() * 2 for f in feats) + dout.numel() * 4,
+              lambda: F.detect_decode(feats, dc["hw"], dc["strides"], anchors, dc["na"], dc["no"],
+                                      dout, W.F16),
+              kernel=("detect",))
+    it.inputs, it.outputs = feats, [dout]
+    if with_unfused:
+        an = torch.tensor(anchors, dtype=torch.float32, device=dev)
+        grids = []
+        for h, w_ in dc["hw"]:
+            yy, xx = torch.meshgrid(torch.arange(h, device=dev), torch.arange(w_, device=dev),
+                                    indexing="ij")
+            grids.append(torch.stack([xx, yy], -1).float().view(1, 1, h, w_, 2))
+
+        def detect_unfused():
+            outs = []
+            for s, (h, w_) in enumerate(dc["hw"]):
+                xs = feats[s].view(1, dc["na"], dc["no"], h, w_).permute(0, 1, 3, 4, 2).contiguous()
+                p = xs.float().sigmoid()
+                xy = (p[..., :2] * 2 - 0.5 + grids[s]) * dc["strides"][s]
+                wh = (p[..., 2:4] * 2) ** 2 * an[s].view(1, dc["na"], 1, 1, 2)
+                outs.append(torch.cat([xy, wh, p[..., 4:]], -1).view(1, -1, dc["no"]))
+            return torch.cat(outs, 1)
+        it.unfused, it.n_unfused = detect_unfused, 34
+    return it
+
+
+def unfused_chain(spec, dt, shape, ins, out):
+    """The same chain as one library kernel per op, each writing a full
+    intermediate tensor in the chain's current dtype."""
+    import torch
+
+    import elementwise_chain_jit_gb300 as F
+    steps = []
+    n = int(np.prod(shape))
+    cur_dt, j = dt, 1
+    bufs = {}
+
+    def buf(d, slot):
+        key = (d, slot)
+        if key not in bufs:
+            bufs[key] = torch.empty(n, dtype=_tdt(d), device=out.device)
+        return bufs[key]
+
+    items = [s.strip() for s in spec.split(";") if s.strip()]
+    src = ins[0]
+    slot = 0
+    for pos, item in enumerate(items):
+        name, _, arg = item.partition(":")
+        if name == "shuffle":
+            c = F.fuse_compile(item, shape, cur_dt)
+            operands = [src]
+        elif name in ("add", "mul"):
+            c = F.fuse_compile(name, (n,), cur_dt)
+            operands = [src, ins[j]]
+            j += 1
+        else:
+            c = F.fuse_compile(item, (n,), cur_dt)
+            operands = [src]
+        if name == "cast":
+            cur_dt = {"f32": 0, "f16": 1, "bf16": 2}[arg]
+        last = pos == len(items) - 1
+        dst = out if last else buf(cur_dt, slot)
+        slot ^= 1
+        steps.append((c, list(operands), dst))
+        src = dst
+    if not items:
+        return None, 0
+
+    def run():
+        for c, operands, dst in steps:
+            F.fuse_launch(c, operands, dst)
+    return run, len(steps)
+
+
+# ---------------------------------------------------------------- timing
+
+def time_fn(fn, reps=5, warm=2):
+    import torch
+    s = torch.cuda.current_stream()
+    for _ in range(warm):
+        fn()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        fn()
+        b.record(s)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def kernel_source_hash(item):
+    import elementwise_chain_jit_gb300 as F
+    h = hashlib.sha1()
+    if item.kernel and item.kernel[0] == "chain":
+        _, spec, shape, dt = item.kernel
+        h.update(F.fuse_source(spec, shape, dt).encode())
+        h.update(open(os.path.join(ROOT, "elementwise_chain_jit_gb300", "csrc", "kernels",
+                                   "common.cuh"), "rb").read())
+    else:
+        for f in ("common.cuh", f"{item.kernel[0]}.cuh"):
+            p = os.path.join(ROOT, "elementwise_chain_jit_gb300", "csrc", "kernels", f)
+            if os.path.exists(p):
+                h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(name, src_hash):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (lines 'kernel: <name> source: <hash> traffic_bytes: <B>')."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 6 and parts[0] == "kernel:" and parts[1] == name and parts[3] == src_hash:
+            return float(parts[5])
+    return None
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+
+def cpu_sample(frac_div: int):
+    """The oracle on a bounded sample of every workload; returns (bytes, seconds, description)."""
+    import oracle
+    import workloads as W
+    total_b, total_t, parts = 0, 0.0, []
+
+    def clock(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    n = W.FLAT_SIZES[-1] // frac_div
+    for L in W.CHAIN_LENGTHS:
+        spec, dt = W.random_chain(L, 5)
+        ins, dts = W.chain_inputs(spec, dt, n, L)
+        ch = oracle.parse_spec(spec, dt)
+        total_t += clock(lambda: oracle.store(oracle.chain_eval(spec, dt, ins, (n,))[0], ch.out_dtype))
+        total_b += sum(n * _esz(d) for d in dts) + n * _esz(ch.out_dtype)
+    parts.append(f"flat chains L=1..32 on {n} elements")
+    cfg = W.SHUFFLE_CHAIN
+    nb = max(1, cfg["shape"][0] // min(frac_div, cfg["shape"][0]))
+    shape = (nb,) + tuple(cfg["shape"][1:])
+    ns = int(np.prod(shape))
+    for L in W.CHAIN_LENGTHS:
+        body, dt = W.random_chain(L, 9, start_dtype=W.F16)
+        spec = f"shuffle:{cfg['groups']};{body}"
+        ins, dts = W.chain_inputs(spec, dt, ns, L)
+        ch = oracle.parse_spec(spec, dt)
+        total_t += clock(lambda: oracle.store(oracle.chain_eval(spec, dt, ins, shape)[0], ch.out_dtype))
+        total_b += sum(ns * _esz(d) for d in dts) + ns * _esz(ch.out_dtype)
+    parts.append(f"shuffle chains L=1..32 on batch {nb} of [32,256,56,56]")
+    rc = W.RMSNORM
+    rows = max(1, rc["rows"] // frac_div)
+    x = W.normal((rows, rc["hidden"]), 0, 1, 1, W.BF16)
+    r = W.normal((rows, rc["hidden"]), 0, 1, 2, W.BF16)
+    w = W.normal(rc["hidden"], 1, 0.1, 3, W.BF16)
+
+    def rms():
+        y, h = oracle.rmsnorm_residual(x, r, w, W.BF16, rc["eps"])
+        oracle.store(y, W.BF16), oracle.store(h, W.BF16)
+    total_t += clock(rms)
+    total_b += 4 * rows * rc["hidden"] * 2 + rc["hidden"] * 2
+    parts.append(f"rmsnorm {rows} rows")
+    pc = W.ROPE
+    toks = max(1, pc["tokens"] // frac_div)
+    qkv = W.normal((toks, 3 * pc["heads"] * pc["head_dim"]), 0, 1, 4, W.BF16)
+
+    def rope():
+        q, k, v, _, _ = oracle.rope_qkv_split(qkv, W.BF16, pc["heads"], pc["head_dim"], np.arange(toks))
+        for a in (q, k, v):
+            oracle.store(a, W.BF16)
+    total_t += clock(rope)
+    total_b += 2 * qkv.size * 2
+    parts.append(f"rope {toks} tokens")
+    ac = W.ADD_RELU_SCALE
+    na = max(1, ac["n"] // frac_div)
+    a = W.uniform(na, -1, 1, 5, W.F32)
+    b = W.uniform(na, -1, 1, 6, W.F32)
+    total_t += clock(lambda: oracle.store(oracle.chain_eval(ac["spec"], W.F32, [a, b], (na,))[0], W.F32))
+    total_b += 3 * na * 4
+    parts.append(f"add-relu-scale {na} elements")
+    dc = W.DETECT
+    hw = [(max(1, h // int(np.sqrt(frac_div))), max(1, w_ // int(np.sqrt(frac_div)))) for h, w_ in dc["hw"]]
+    feats = [W.normal((1, 255, h, w_), 0, 2, 7 + s, W.F16) for s, (h, w_) in enumerate(hw)]
+    anchors = W.detect_anchors(dc["strides"])
+    total_t += clock(lambda: oracle.detect_decode(feats, W.F16, dc["strides"], anchors, 3, 85))
+    total_b += sum(f.size * 2 for f in feats) + sum(3 * h * w_ for h, w_ in hw) * 85 * 4
+    parts.append(f"detect decode scales {hw}")
+    return total_b, total_t, "; ".join(parts)
+
+
+# ---------------------------------------------------------------- arms
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    frac = 1024
+    for _ in range(args.warmup):
+        cpu_sample(frac)
+    tb, tt = 0, 0.0
+    desc = ""
+    for _ in range(args.steps):
+        b, t, desc = cpu_sample(frac)
+        tb += b
+        tt += t
+    v = tb / tt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": f"1/{frac} of each workload per step"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args):
+    import torch
+
+    import elementwise_chain_jit_gb300 as F
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    items = build_items(dev, with_unfused=not args.no_unfused, only=args.only,
+                        flat_elems=args.flat_elems)
+    if not items:
+        raise SystemExit(f"--only {args.only!r} matches no workload")
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    step_bytes = sum(it.bytes for it in items)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # warm-up (compiles and loads everything)
+    for _ in range(args.warmup):
+        for it in items:
+            it.fused()
+    barrier()
+    # timed region: events between launches give each kernel's duration
+    nitem = len(items)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nitem + 1)] for _ in range(args.steps)]
+    launches0 = F.fuse_stats()["launches"]
+    with ClockSampler(local) as clocks:
+        barrier()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s in range(args.steps):
+            evs[s][0].record(stream)
+            for i, it in enumerate(items):
+                it.fused()
+                evs[s][i + 1].record(stream)
+        t_end.record(stream)
+        barrier()
+    launches = F.fuse_stats()["launches"] - launches0
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    per_item = [statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps))
+                for i in range(nitem)]
+    ms_per_step = total_ms / args.steps
+    value = world * step_bytes / (ms_per_step / 1e3) / 1e9
+
+    peak, peak_kind = peaks()
+    # unfused per-op sequences (outside the timed region)
+    per_chain = {}
+    for it, ms in zip(items, per_item):
+        d = {"bytes": it.bytes, "us_fused": ms * 1e3, "gbs": it.bytes / (ms / 1e3) / 1e9,
+             "frac_of_" + peak_kind + "_peak": it.bytes / (ms / 1e3) / 1e9 / peak}
+        if it.unfused is not None and not args.no_unfused:
+            ums = time_fn(it.unfused, reps=3, warm=1)
+            L, T = launch_overhead(ums, ms, it.n_unfused)
+            d.update({"us_unfused": ums * 1e3, "unfused_kernels": it.n_unfused,
+                      "speedup": ums / ms, "extra_cost_per_unfused_op_us": L * 1e3})
+        per_chain[it.name] = d
+    # dominant kernel and its roofline
+    dom = max(range(nitem), key=lambda i: per_item[i])
+    dit = items[dom]
+    achieved = dit.bytes / (per_item[dom] / 1e3) / 1e9
+    src_hash = kernel_source_hash(dit)
+    traffic = traffic_record(dit.name, src_hash)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": dit.name,
+                "algorithmic_bytes": dit.bytes, "peak_source": peak_kind + " (burst copy)",
+                "source_hash": src_hash}
+    # end to end: host (pinned) -> device copies of every input, the fused
+    # launches, device -> host copies of every output, each step
+    e2e = None
+    if not args.no_e2e:
+        max_in = max(t.numel() * t.element_size() for it in items for t in it.inputs)
+        max_out = max(t.numel() * t.element_size() for it in items for t in it.outputs)
+        # one pinned staging buffer holds the bytes of the largest input; each
+        # input is copied from it (values do not change the timing)
+        big = max((t for it in items for t in it.inputs), key=lambda t: t.numel() * t.element_size())
+        h_in = torch.empty(max_in, dtype=torch.uint8, pin_memory=True)
+        h_in.copy_(big.reshape(-1).view(torch.uint8))
+        h_out = torch.empty(max_out, dtype=torch.uint8, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for it in items for t in it.inputs)
+        d2h = sum(t.numel() * t.element_size() for it in items for t in it.outputs)
+
+        def e2e_step():
+            for it in items:
+                for t in it.inputs:
+                    nb = t.numel() * t.element_size()
+                    t.view(-1).view(torch.uint8).copy_(h_in[:nb], non_blocking=True)
+                it.fused()
+                for t in it.outputs:
+                    nb = t.numel() * t.element_size()
+                    h_out[:nb].copy_(t.view(-1).view(torch.uint8), non_blocking=True)
+        # the staged input bytes are random: refresh the device inputs after
+        e2e_steps = max(1, min(args.steps, 3))
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        barrier()
+        e_ms = a.elapsed_time(b) / e2e_steps
+        e2e = {"value": world * step_bytes / (e_ms / 1e3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "steps": e2e_steps}
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        b, t, desc = cpu_sample(64)
+        cpu = {"value": b / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": desc + " (1/64 of each workload)", "seconds": t}
+    clk = clocks.summary()
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "bytes_per_step": step_bytes,
+                       "l2": "inputs larger than L2: each step streams "
+                             f"{step_bytes / 1e9:.1f} GB, evicting the small workloads' buffers",
+                       "storage_dtypes": "f32/f16/bf16 per workload, arithmetic in f32"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clk, "per_chain": per_chain,
+            "partial": ({"only": args.only, "flat_elems": args.flat_elems}
+                        if args.only or args.flat_elems else None),
+            "frac_of_peak": value / world / peak, "peak_gbs": peak}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="fused", choices=["fused", "reference"])
+    ap.add_argument("--no-unfused", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", default=None, help="regex: run only the matching workloads")
+    ap.add_argument("--flat-elems", type=int, default=None, help="size of the flat chains")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

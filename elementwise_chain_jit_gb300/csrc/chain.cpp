@@ -164,19 +164,25 @@ int plan_chain(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_d
     p->HW = shape[2] * shape[3];
   }
   p->copy = ch.ops.empty();
-  // elements per vector: VEC_BYTES of the narrowest tensor
-  int minb = dtype_bytes(ch.out_dt);
-  int words = 0;
-  for (auto d : ch.in_dt) minb = std::min(minb, dtype_bytes(d));
+  // Elements per vector: the widest access (32, 16, 8 or 4 bytes of the
+  // narrowest tensor) whose register words -- every input's and the
+  // output's share of one vector -- fit the budget, so that chains with many
+  // inputs keep enough warps resident.
+  int minb = dtype_bytes(ch.out_dt), bytes_per_elem = dtype_bytes(ch.out_dt);
+  for (auto d : ch.in_dt) {
+    minb = std::min(minb, dtype_bytes(d));
+    bytes_per_elem += dtype_bytes(d);
+  }
+  const int budget = env_int("FUSE_CHAIN_WORD_BUDGET", 48);
   int vec_bytes = env_int("FUSE_CHAIN_VEC_BYTES", 32);
-  if (vec_bytes != 16 && vec_bytes != 32) vec_bytes = 32;
+  if (vec_bytes != 4 && vec_bytes != 8 && vec_bytes != 16 && vec_bytes != 32) vec_bytes = 32;
+  while (vec_bytes > 4 && (vec_bytes / minb) * bytes_per_elem / 4 > budget) vec_bytes /= 2;
   p->vec = vec_bytes / minb;
-  for (auto d : ch.in_dt) words += p->vec * dtype_bytes(d) / 4;
-  words += p->vec * dtype_bytes(ch.out_dt) / 4;
+  const int words = p->vec * bytes_per_elem / 4;
   // vectors in flight per thread: enough to cover latency, bounded registers
   int max_unroll = env_int("FUSE_CHAIN_UNROLL", 2);
   p->unroll = 1;
-  while (p->unroll * 2 <= max_unroll && words * p->unroll * 2 <= 64) p->unroll *= 2;
+  while (p->unroll * 2 <= max_unroll && words * p->unroll * 2 <= budget) p->unroll *= 2;
   p->block = env_int("FUSE_CHAIN_BLOCK", 256);
   if (p->block < 32 || p->block > 1024 || p->block % 32) p->block = 256;
   p->vec_ok = !ch.groups || (p->HW % p->vec == 0);
@@ -364,11 +370,15 @@ static int chain_device_state(fuse_chain* h, const DeviceInfo& d, fuse_chain::Pe
     if (int rc = jit_function(*h->mod, "fuse_chain_vec", d, &pd.vec_fn)) return rc;
     r = api->OccupancyMaxActiveBlocksPerMultiprocessor(&occ, pd.vec_fn, p.block, 0);
     if (r != CUDA_SUCCESS) return cuda_fail(r, "cuOccupancyMaxActiveBlocksPerMultiprocessor");
+    // One chunk per CTA: the block scheduler hands chunks to SMs as they free
+    // up, so the last wave is at most one chunk long.  FUSE_CHAIN_CTAS_PER_SM
+    // instead sizes a persistent grid of SMs x that many CTAs.
     int per_sm = env_int("FUSE_CHAIN_CTAS_PER_SM", 0);
-    if (per_sm <= 0 || per_sm > occ) per_sm = std::max(occ, 1);
     int64_t chunk = int64_t(p.block) * p.unroll;
     int64_t nfull = (p.n / p.vec) / chunk;
-    pd.vec_grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(nfull, int64_t(d.sms) * per_sm)));
+    int64_t cap = int64_t(1) << 30;
+    if (per_sm > 0) cap = int64_t(d.sms) * std::min(per_sm, std::max(occ, 1));
+    pd.vec_grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(nfull, cap)));
   }
   h->dev.push_back(pd);
   *out = &h->dev.back();
