@@ -26,8 +26,8 @@ STATUS = {0: "FUSE_OK", -1: "FUSE_E_SPEC", -2: "FUSE_E_SHAPE", -3: "FUSE_E_DTYPE
 
 # every symbol include/fuse.h declares
 EXPORTS = ["fuse_compile", "fuse_num_inputs", "fuse_input_dtypes", "fuse_launch", "fuse_release",
-           "fuse_source", "rmsnorm_residual", "rope_qkv_split", "detect_decode", "channel_shuffle",
-           "fuse_last_error", "fuse_stats", "fuse_device_sms"]
+           "fuse_source", "rmsnorm_residual", "rope_qkv_split", "rope_qkv_split_noalloc",
+           "detect_decode", "channel_shuffle", "fuse_last_error", "fuse_stats", "fuse_device_sms"]
 
 
 class FuseError(RuntimeError):
@@ -51,6 +51,7 @@ _lib.fuse_source.argtypes = [ctypes.c_char_p, ctypes.POINTER(_I64), _I, _I, ctyp
                              ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
 _lib.rmsnorm_residual.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P]
 _lib.rope_qkv_split.argtypes = [_P, _P, _P, _P, _I64, _I, _I, _I64, _F, _I, _P]
+_lib.rope_qkv_split_noalloc.argtypes = [_P, _P, _P, _P, _I64, _I, _I, _I64, _F, _I, _P]
 _lib.detect_decode.argtypes = [ctypes.POINTER(_P), ctypes.POINTER(_I), ctypes.POINTER(_F),
                                ctypes.POINTER(_F), _I, _I, _I, _I, _P, _P]
 _lib.channel_shuffle.argtypes = [_P, _P, _I64, _I64, _I64, _I64, _I, _I, _P]
@@ -169,6 +170,20 @@ def rope_qkv_split(qkv, q, k, v, heads: int, head_dim: int, pos0: int = 0,
         dt = qkv.dtype
     _check(_lib.rope_qkv_split(_ptr(qkv), _ptr(q), _ptr(k), _ptr(v), tokens, heads, head_dim,
                                pos0, base, _dtype(dt), _stream(stream)))
+
+
+def rope_qkv_split_noalloc(qkv, q, k, v, heads: int, head_dim: int, pos0: int = 0,
+                           base: float = 10000.0, dt=None, tokens: int | None = None,
+                           stream=None) -> None:
+    """rope_qkv_split for callers that cannot let the library allocate device
+    memory or compile at run time (see include/fuse.h): the cos/sin rows live
+    in a fixed 4 MB array inside the library; tokens * head_dim <= 2^20."""
+    if tokens is None:
+        tokens = qkv.shape[0]
+    if dt is None:
+        dt = qkv.dtype
+    _check(_lib.rope_qkv_split_noalloc(_ptr(qkv), _ptr(q), _ptr(k), _ptr(v), tokens, heads,
+                                       head_dim, pos0, base, _dtype(dt), _stream(stream)))
 
 
 def detect_decode(feats, hw, strides, anchors, na: int, no: int, out, in_dt=None,

@@ -140,6 +140,30 @@ int rope_qkv_split(const void* qkv, void* q, void* k, void* v, int64_t tokens, i
                    int head_dim, int64_t pos0, float base, fuse_dtype dt, void* stream);
 
 /* ------------------------------------------------------------------------
+ * rope_qkv_split_noalloc -- the same operation as rope_qkv_split, for callers
+ * that must not let the library allocate device memory or compile at run
+ * time: a serving process whose device memory all belongs to its own caching
+ * allocator or arena, code running while a stream is captured into a CUDA
+ * graph (an allocation or the synchronisation it may bring is an error
+ * there), loops that forbid allocation after start-up.  The pages have no
+ * counterpart of this entry point; it is an addition of this library.
+ *
+ * Arguments, layouts and results as rope_qkv_split.  It calls no cudaMalloc,
+ * cudaFree or allocating routine: the cos/sin rows of the call are built into
+ * a fixed array inside the library's module (2^20 fp32 values, 4 MB, held on
+ * every device that has loaded the library until the process exits), and both
+ * of its kernels are compiled ahead of time.
+ *   - tokens * head_dim must be <= 2^20, else FUSE_E_SHAPE.
+ *   - All calls on a device share the array; each call rewrites the rows it
+ *     uses first, so nothing needs clearing, but calls that overlap on the GPU
+ *     (other streams, unordered threads) race on it: order them on one stream.
+ *   - The first call on a device looks up the array's address with that
+ *     device current; make it before any stream capture begins.
+ */
+int rope_qkv_split_noalloc(const void* qkv, void* q, void* k, void* v, int64_t tokens, int heads,
+                           int head_dim, int64_t pos0, float base, fuse_dtype dt, void* stream);
+
+/* ------------------------------------------------------------------------
  * Detection-head decode ("DeepJIT" section 1.1: the sigmoid / exp / mul /
  * add / slice / concat / cast tail of a detection head, fused into one
  * kernel).
