@@ -185,6 +185,17 @@ int plan_chain(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_d
   while (p->unroll * 2 <= max_unroll && words * p->unroll * 2 <= budget) p->unroll *= 2;
   p->block = env_int("FUSE_CHAIN_BLOCK", 256);
   if (p->block < 32 || p->block > 1024 || p->block % 32) p->block = 256;
+  // Small tensors: shrink the chunk (fewer vectors in flight per thread, then
+  // smaller CTAs, then 16-byte vectors) until there are about 8 CTAs per SM,
+  // so that every SM has loads in flight.
+  const int64_t want_ctas = int64_t(8) * default_sms();
+  auto chunks = [&]() { return n / p->vec / (int64_t(p->block) * p->unroll); };
+  while (chunks() < want_ctas) {
+    if (p->unroll > 1) p->unroll /= 2;
+    else if (p->block > 128) p->block /= 2;
+    else if (p->vec * minb > 16) p->vec /= 2;
+    else break;
+  }
   p->vec_ok = !ch.groups || (p->HW % p->vec == 0);
   return FUSE_OK;
 }
@@ -205,7 +216,9 @@ static void emit_op(std::ostringstream& s, const ChainOp& op, const std::string&
     case OP_MUL: s << "      x = x * " << operand(elem_of_input, op.input) << ";\n"; break;
     case OP_SCALE: s << "      x = x * " << hex_float(op.c) << ";\n"; break;
     case OP_RELU: s << "      x = x > 0.f ? x : 0.f;\n"; break;
-    case OP_SIGMOID: s << "      x = 1.0f / (1.0f + expf(-x));\n"; break;
+    // 1 / (1 + exp(-x)) with the IEEE round-to-nearest reciprocal (the same
+    // correctly rounded value as the division 1.0f / y, in fewer instructions)
+    case OP_SIGMOID: s << "      x = __frcp_rn(1.0f + expf(-x));\n"; break;
     case OP_EXP: s << "      x = expf(x);\n"; break;
     case OP_CAST:
       if (op.to == FUSE_F16) s << "      x = round_f16(x);\n";

@@ -11,6 +11,7 @@
 // coalesced.
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <sstream>
@@ -47,7 +48,17 @@ int detect_kernel(const int* hw, const float* strides, const float* anchors, int
     return FUSE_OK;
   }
   DetectKernel k;
+  // cells per tile (multiple of 8; the tile of tc * no floats must fit 48 KB)
+  // and threads per CTA; FUSE_DETECT_TC / FUSE_DETECT_BLOCK override
   int tc = std::min(64, (12288 / no) / 8 * 8);
+  if (const char* e = getenv("FUSE_DETECT_TC"); e && *e) {
+    int v = atoi(e) / 8 * 8;
+    if (v >= 8 && v * no * 4 <= 49152) tc = v;
+  }
+  if (const char* e = getenv("FUSE_DETECT_BLOCK"); e && *e) {
+    int v = atoi(e);
+    if (v >= 32 && v <= 1024 && v % 32 == 0) k.block = v;
+  }
   std::ostringstream s;
   s << "// detection-head decode: " << ns << " scales, " << na << " anchors, " << no
     << " outputs per anchor, " << dtype_name(dt) << " in, f32 out\n";

@@ -67,14 +67,20 @@ def test_chain_typing():
 
 
 def test_source_bakes_sizes_vector_and_tail():
-    src = F.fuse_source("add;relu;scale:0.5", [(1 << 20) + 7], F.F32)
-    assert "constexpr long long N = 1048583LL;" in src
+    src = F.fuse_source("add;relu;scale:0.5", [(1 << 26) + 7], F.F32)
+    assert "constexpr long long N = 67108871LL;" in src
     assert "constexpr int VEC = 8;" in src  # 32 bytes of fp32
+    assert "constexpr int TAIL = (int)(N - NVEC * VEC);" in src
+    # a small tensor gets smaller chunks (about 8 CTAs per SM): 16-byte
+    # vectors, one per thread, 128-thread CTAs
+    small = F.fuse_source("add;relu;scale:0.5", [(1 << 20) + 7], F.F32)
+    assert "constexpr int VEC = 4;" in small and "constexpr int BLOCK = 128;" in small
+    assert "constexpr int UNROLL = 1;" in small
     assert "x = x * 0x1p-1f;" in src       # the scale constant, exact
     assert "x = x > 0.f ? x : 0.f;" in src
     assert "fuse_chain_vec" in src and "fuse_chain_scalar" in src
-    src16 = F.fuse_source("relu", [1 << 20], F.F16)
-    assert "constexpr int VEC = 16;" in src16
+    src16 = F.fuse_source("relu", [1 << 26], F.F16)
+    assert "constexpr int VEC = 16;" in src16  # 32 bytes of fp16
     shf = F.fuse_source("shuffle:4;relu", [32, 256, 56, 56], F.F16)
     assert "G = 4" in shf and "src_vec" in shf and "HW = 3136" in shf
 
