@@ -359,6 +359,59 @@ def time_fn(fn, reps=5, warm=2):
     return statistics.median(ts)
 
 
+def graph_times(item, k=50):
+    """Launch overhead of a small workload ("DeepJIT" section 6.1's per-op /
+    CUDA graph / fused comparison): mean time per pass over k passes of
+    (a) the fused launch from the host, (b) the fused launch replayed from one
+    library graph, (c) the unfused sequence replayed from one CUDA graph.
+    Inputs stay in L2 across the k passes (warm)."""
+    import torch
+
+    import elementwise_chain_jit_gb300 as F
+    s = torch.cuda.Stream()
+    out = {}
+    with torch.cuda.stream(s):
+        item.fused()
+        s.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(k):
+            item.fused()
+        b.record(s)
+        b.synchronize()
+        out["us_fused_host_loop"] = a.elapsed_time(b) / k * 1e3
+    F.fuse_graph_begin(s)
+    with torch.cuda.stream(s):
+        for _ in range(k):
+            item.fused()
+    g = F.fuse_graph_end(s)
+    with torch.cuda.stream(s):
+        g.launch(s)
+        s.synchronize()
+        a.record(s)
+        g.launch(s)
+        b.record(s)
+        b.synchronize()
+    out["us_fused_graph"] = a.elapsed_time(b) / k * 1e3
+    g.release()
+    if item.unfused is not None:
+        with torch.cuda.stream(s):
+            item.unfused()
+        s.synchronize()
+        tg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tg, stream=s):
+            for _ in range(k):
+                item.unfused()
+        tg.replay()
+        torch.cuda.synchronize()
+        a.record()
+        tg.replay()
+        b.record()
+        b.synchronize()
+        out["us_unfused_graph"] = a.elapsed_time(b) / k * 1e3
+    return out
+
+
 def kernel_source_hash(item):
     import elementwise_chain_jit_gb300 as F
     h = hashlib.sha1()
@@ -566,6 +619,8 @@ def run_gpu(args):
             L, T = launch_overhead(ums, ms, it.n_unfused)
             d.update({"us_unfused": ums * 1e3, "unfused_kernels": it.n_unfused,
                       "speedup": ums / ms, "extra_cost_per_unfused_op_us": L * 1e3})
+        if it.bytes < 64e6 and not args.no_unfused:
+            d.update(graph_times(it))
         per_chain[it.name] = d
     # dominant kernel and its roofline
     dom = max(range(nitem), key=lambda i: per_item[i])

@@ -27,7 +27,9 @@ STATUS = {0: "FUSE_OK", -1: "FUSE_E_SPEC", -2: "FUSE_E_SHAPE", -3: "FUSE_E_DTYPE
 # every symbol include/fuse.h declares
 EXPORTS = ["fuse_compile", "fuse_num_inputs", "fuse_input_dtypes", "fuse_launch", "fuse_release",
            "fuse_source", "rmsnorm_residual", "rope_qkv_split", "rope_qkv_split_noalloc",
-           "detect_decode", "channel_shuffle", "fuse_last_error", "fuse_stats", "fuse_device_sms"]
+           "detect_decode", "channel_shuffle", "fuse_graph_begin", "fuse_graph_end",
+           "fuse_graph_launch", "fuse_graph_nodes", "fuse_graph_release", "fuse_last_error",
+           "fuse_stats", "fuse_device_sms"]
 
 
 class FuseError(RuntimeError):
@@ -55,6 +57,11 @@ _lib.rope_qkv_split_noalloc.argtypes = [_P, _P, _P, _P, _I64, _I, _I, _I64, _F, 
 _lib.detect_decode.argtypes = [ctypes.POINTER(_P), ctypes.POINTER(_I), ctypes.POINTER(_F),
                                ctypes.POINTER(_F), _I, _I, _I, _I, _P, _P]
 _lib.channel_shuffle.argtypes = [_P, _P, _I64, _I64, _I64, _I64, _I, _I, _P]
+_lib.fuse_graph_begin.argtypes = [_P]
+_lib.fuse_graph_end.argtypes = [_P, ctypes.POINTER(_P)]
+_lib.fuse_graph_launch.argtypes = [_P, _P]
+_lib.fuse_graph_nodes.argtypes = [_P, ctypes.POINTER(_I64)]
+_lib.fuse_graph_release.argtypes = [_P]
 _lib.fuse_last_error.restype = ctypes.c_char_p
 _lib.fuse_stats.argtypes = [ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64),
                             ctypes.POINTER(ctypes.c_double)]
@@ -214,6 +221,48 @@ def _flatten(a):
         return np.asarray(a, dtype=float).reshape(-1).tolist()
     except Exception:  # pragma: no cover
         return [x for row in a for pair in row for x in pair]
+
+
+# ---------------------------------------------------------------- graphs
+
+class Graph:
+    """A recorded sequence of library launches (wraps a fuse_graph_handle)."""
+
+    def __init__(self, handle: int):
+        self.handle = handle
+        n = _I64()
+        _check(_lib.fuse_graph_nodes(handle, ctypes.byref(n)))
+        self.nodes = n.value
+
+    def launch(self, stream=None) -> None:
+        fuse_graph_launch(self, stream)
+
+    def release(self) -> None:
+        if self.handle:
+            fuse_graph_release(self)
+            self.handle = None
+
+
+def fuse_graph_begin(stream=None) -> None:
+    _check(_lib.fuse_graph_begin(_stream(stream)))
+
+
+def fuse_graph_end(stream=None) -> Graph:
+    h = _P()
+    _check(_lib.fuse_graph_end(_stream(stream), ctypes.byref(h)))
+    return Graph(h.value)
+
+
+def fuse_graph_launch(graph: Graph, stream=None) -> None:
+    _check(_lib.fuse_graph_launch(graph.handle, _stream(stream)))
+
+
+def fuse_graph_nodes(graph: Graph) -> int:
+    return graph.nodes
+
+
+def fuse_graph_release(graph: Graph) -> None:
+    _check(_lib.fuse_graph_release(graph.handle))
 
 
 # ---------------------------------------------------------------- diagnostics

@@ -54,6 +54,13 @@ struct DriverApi {
   decltype(&::cuStreamCreate) StreamCreate;
   decltype(&::cuStreamSynchronize) StreamSynchronize;
   decltype(&::cuStreamDestroy) StreamDestroy;
+  decltype(&::cuStreamBeginCapture) StreamBeginCapture;
+  decltype(&::cuStreamEndCapture) StreamEndCapture;
+  decltype(&::cuGraphInstantiateWithFlags) GraphInstantiateWithFlags;
+  decltype(&::cuGraphLaunch) GraphLaunch;
+  decltype(&::cuGraphExecDestroy) GraphExecDestroy;
+  decltype(&::cuGraphDestroy) GraphDestroy;
+  decltype(&::cuGraphGetNodes) GraphGetNodes;
 };
 
 // Returns FUSE_OK and the API table, or FUSE_E_CUDA (driver missing).

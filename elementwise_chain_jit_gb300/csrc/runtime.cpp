@@ -134,6 +134,13 @@ void load_driver() {
   FUSE_GET(StreamCreate, "cuStreamCreate");
   FUSE_GET(StreamSynchronize, "cuStreamSynchronize");
   FUSE_GET(StreamDestroy, "cuStreamDestroy");
+  FUSE_GET(StreamBeginCapture, "cuStreamBeginCapture");
+  FUSE_GET(StreamEndCapture, "cuStreamEndCapture");
+  FUSE_GET(GraphInstantiateWithFlags, "cuGraphInstantiateWithFlags");
+  FUSE_GET(GraphLaunch, "cuGraphLaunch");
+  FUSE_GET(GraphExecDestroy, "cuGraphExecDestroy");
+  FUSE_GET(GraphDestroy, "cuGraphDestroy");
+  FUSE_GET(GraphGetNodes, "cuGraphGetNodes");
 #undef FUSE_GET
   if (!ok) return;
   CUresult r = g_api.Init(0);

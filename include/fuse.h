@@ -191,6 +191,29 @@ int channel_shuffle(const void* in, void* out, int64_t n, int64_t c, int64_t h, 
                     int groups, fuse_dtype dt, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Sequences replayed as one CUDA graph ("DeepJIT", section 5.3: launch the
+ * fused kernels in order and record them with stream capture; section 3.1: a
+ * graph removes launch overhead, fusion removes the memory round trips).
+ *
+ * fuse_graph_begin(stream) starts capturing `stream` (thread-local capture
+ * mode); every library call on that stream until fuse_graph_end(stream, &g)
+ * becomes a node of the graph instead of running.  fuse_graph_launch(g, s)
+ * replays the whole sequence with one submission on any stream; the tensors
+ * named in the captured calls must stay allocated while g may run.  Calls that
+ * compile a kernel, load a module or build a RoPE table cannot run during a
+ * capture: make each call once before capturing it (fuse_compile loads its
+ * module when a device is present).  A failed capture returns FUSE_E_CUDA
+ * from fuse_graph_end and leaves no graph.
+ */
+typedef struct fuse_graph* fuse_graph_handle;
+int fuse_graph_begin(void* stream);
+int fuse_graph_end(void* stream, fuse_graph_handle* out);
+int fuse_graph_launch(fuse_graph_handle g, void* stream);
+/* Number of nodes (kernel launches) recorded in g. */
+int fuse_graph_nodes(fuse_graph_handle g, int64_t* nodes);
+int fuse_graph_release(fuse_graph_handle g);
+
+/* ------------------------------------------------------------------------
  * Diagnostics ("算子与运行时", section 6.5: per-operator counters).
  */
 /* Message of the last failed call on this thread ("" if none).  For
