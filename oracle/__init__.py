@@ -71,6 +71,7 @@ def lib():
         L.oracle_channel_shuffle.argtypes = [P, P, I64, I64, I64, I64, I, I]
         L.oracle_rmsnorm_residual.argtypes = [P, P, P, I, I64, I64, ctypes.c_float, P, P]
         L.oracle_rope_qkv_split.argtypes = [P, I, I64, I, I, P, D, P, P, P, P, P]
+        L.oracle_layernorm_residual.argtypes = [P, P, P, P, I, I64, I64, ctypes.c_float, P, P, P]
         L.oracle_detect_decode.argtypes = [P, I, P, P, P, I, I, I, P, P]
         _lib = L
     return _lib
@@ -237,6 +238,20 @@ def rmsnorm_residual(x, res, w, dt: int, eps: float):
     lib().oracle_rmsnorm_residual(_p(x), _p(res), _p(w), dt, rows, hidden, ctypes.c_float(eps),
                                   _p(y), _p(r))
     return y, r
+
+
+def layernorm_residual(x, res, gamma, beta, dt: int, eps: float):
+    """LayerNorm of h = x + res (res, gamma, beta may be None).  Returns
+    (y, residual_out or None, term magnitudes) in binary64, shaped like x."""
+    x = np.ascontiguousarray(x)
+    rows, hidden = x.shape
+    res, gamma, beta = (None if a is None else np.ascontiguousarray(a) for a in (res, gamma, beta))
+    y = np.empty((rows, hidden), np.float64)
+    mag = np.empty((rows, hidden), np.float64)
+    ro = np.empty((rows, hidden), np.float64) if res is not None else None
+    lib().oracle_layernorm_residual(_p(x), _p(res), _p(gamma), _p(beta), dt, rows, hidden,
+                                    ctypes.c_float(eps), _p(y), _p(ro), _p(mag))
+    return y, ro, mag
 
 
 def rope_qkv_split(qkv, dt: int, heads: int, head_dim: int, positions, base: float = 10000.0):
