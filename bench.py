@@ -224,6 +224,33 @@ def _rms_item(dev, with_unfused):
     return it
 
 
+def _ln_item(dev, with_unfused):
+    """Residual add + LayerNorm (a next row, measured beside the step)."""
+    import torch
+
+    import elementwise_chain_jit_gb300 as F
+    import workloads as W
+    rows, hidden, eps = 16384, 4096, 1e-5
+    x = W.device_normal((rows, hidden), 0, 1, 61, W.BF16, dev)
+    r = W.device_normal((rows, hidden), 0, 1, 62, W.BF16, dev)
+    g = W.device_normal((hidden,), 1, 0.1, 63, W.BF16, dev)
+    b = W.device_normal((hidden,), 0, 0.1, 64, W.BF16, dev)
+    y, ro = torch.empty_like(x), torch.empty_like(x)
+    it = Item("layernorm_residual_16384x4096_bf16", 4 * rows * hidden * 2 + 2 * hidden * 2,
+              lambda: F.layernorm_residual(x, r, g, b, y, ro, eps, W.BF16), kernel=("layernorm",))
+    it.inputs, it.outputs = [x, r, g, b], [y, ro]
+    if with_unfused:
+        def ln_unfused():
+            h = x + r
+            hf = h.float()
+            mean = hf.mean(-1, keepdim=True)
+            d = hf - mean
+            var = (d * d).mean(-1, keepdim=True)
+            return (d * torch.rsqrt(var + eps) * g.float() + b.float()).to(torch.bfloat16), h
+        it.unfused, it.n_unfused = ln_unfused, 12
+    return it
+
+
 def _rope_item(dev, with_unfused):
     import torch
 
@@ -622,6 +649,19 @@ def run_gpu(args):
         if it.bytes < 64e6 and not args.no_unfused:
             d.update(graph_times(it))
         per_chain[it.name] = d
+    # next rows, measured beside the step (not part of its workload)
+    next_rows = {}
+    if args.only is None:
+        ln = _ln_item(dev, with_unfused=not args.no_unfused)
+        lms = time_fn(ln.fused, reps=20, warm=3)
+        d = {"bytes": ln.bytes, "us_fused": lms * 1e3, "gbs": ln.bytes / (lms / 1e3) / 1e9,
+             "frac_of_" + peak_kind + "_peak": ln.bytes / (lms / 1e3) / 1e9 / peak}
+        if ln.unfused is not None:
+            ums = time_fn(ln.unfused, reps=3, warm=1)
+            d.update({"us_unfused": ums * 1e3, "unfused_kernels": ln.n_unfused,
+                      "speedup": ums / lms})
+        next_rows[ln.name] = d
+        del ln
     # dominant kernel and its roofline
     dom = max(range(nitem), key=lambda i: per_item[i])
     dit = items[dom]
@@ -685,7 +725,7 @@ def run_gpu(args):
                              f"{step_bytes / 1e9:.1f} GB, evicting the small workloads' buffers",
                        "storage_dtypes": "f32/f16/bf16 per workload, arithmetic in f32"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clk, "per_chain": per_chain,
+            "clocks": clk, "per_chain": per_chain, "next_rows": next_rows,
             "partial": ({"only": args.only, "flat_elems": args.flat_elems}
                         if args.only or args.flat_elems else None),
             "frac_of_peak": value / world / peak, "peak_gbs": peak}

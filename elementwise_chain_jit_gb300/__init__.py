@@ -26,7 +26,7 @@ STATUS = {0: "FUSE_OK", -1: "FUSE_E_SPEC", -2: "FUSE_E_SHAPE", -3: "FUSE_E_DTYPE
 
 # every symbol include/fuse.h declares
 EXPORTS = ["fuse_compile", "fuse_num_inputs", "fuse_input_dtypes", "fuse_launch", "fuse_release",
-           "fuse_source", "rmsnorm_residual", "rope_qkv_split", "rope_qkv_split_noalloc",
+           "fuse_source", "rmsnorm_residual", "layernorm_residual", "rope_qkv_split", "rope_qkv_split_noalloc",
            "detect_decode", "channel_shuffle", "fuse_graph_begin", "fuse_graph_end",
            "fuse_graph_launch", "fuse_graph_nodes", "fuse_graph_release", "fuse_last_error",
            "fuse_stats", "fuse_device_sms"]
@@ -52,6 +52,7 @@ _lib.fuse_release.argtypes = [_P]
 _lib.fuse_source.argtypes = [ctypes.c_char_p, ctypes.POINTER(_I64), _I, _I, ctypes.c_char_p,
                              ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
 _lib.rmsnorm_residual.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P]
+_lib.layernorm_residual.argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P]
 _lib.rope_qkv_split.argtypes = [_P, _P, _P, _P, _I64, _I, _I, _I64, _F, _I, _P]
 _lib.rope_qkv_split_noalloc.argtypes = [_P, _P, _P, _P, _I64, _I, _I, _I64, _F, _I, _P]
 _lib.detect_decode.argtypes = [ctypes.POINTER(_P), ctypes.POINTER(_I), ctypes.POINTER(_F),
@@ -167,6 +168,18 @@ def rmsnorm_residual(x, residual, weight, out, residual_out, eps: float = 1e-6, 
     _check(_lib.rmsnorm_residual(_ptr(x), _ptr(residual), _ptr(weight), _ptr(out),
                                  _ptr(residual_out), rows, hidden, eps, _dtype(dt),
                                  _stream(stream)))
+
+
+def layernorm_residual(x, residual, gamma, beta, out, residual_out, eps: float = 1e-5, dt=None,
+                       rows: int | None = None, hidden: int | None = None, stream=None) -> None:
+    """residual/residual_out, gamma, beta may be None."""
+    if rows is None:
+        rows, hidden = x.shape[0], x.shape[-1]
+    if dt is None:
+        dt = x.dtype
+    _check(_lib.layernorm_residual(_ptr(x), _ptr(residual), _ptr(gamma), _ptr(beta), _ptr(out),
+                                   _ptr(residual_out), rows, hidden, eps, _dtype(dt),
+                                   _stream(stream)))
 
 
 def rope_qkv_split(qkv, q, k, v, heads: int, head_dim: int, pos0: int = 0,

@@ -1,0 +1,141 @@
+// layernorm.cuh -- residual add + LayerNorm + cast, one CTA per row.
+//
+// The generated source defines before including this file:
+//   DT, HIDDEN, BLOCK, VEC, R   as for rmsnorm.cuh
+//   HAS_RES, HAS_GAMMA, HAS_BETA  0/1: residual add, scale, shift present
+//   FUSE_LN_VEC  1 when a vector width fits the row
+//
+// Per row ("DeepJIT ... 串行小核墙" section 4.3: one block per row, the
+// statistics reduced in the block, then the normalisation in the same pass
+// over the data):  h = x (+ residual) in fp32; residual_out = dt(h);
+// mean = sum(h)/HIDDEN; var = sum((h - mean)^2)/HIDDEN -- the same quantity
+// as the page's E[h^2] - mean^2, taken in two passes over the registers so
+// that fp32 does not cancel; out = dt((h - mean) * (1/sqrt(var + eps)) *
+// gamma + beta).  Reductions: per-thread sums, a warp shuffle tree, then the
+// warps' partial sums through shared memory.
+#pragma once
+#include "fuse/common.cuh"
+
+constexpr int NWARPS = BLOCK / 32;
+constexpr int NVR = HIDDEN / VEC;
+constexpr int NWV = VEC * Dt<DT>::bytes / 4;
+
+__device__ __forceinline__ float ln_block_sum(float v, float* part) {
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < NWARPS; ++i) t += part[i];
+  return t;
+}
+
+#if FUSE_LN_VEC
+extern "C" __global__ void __launch_bounds__(BLOCK)
+layernorm_vec(const void* x, const void* res, const void* gamma, const void* beta, void* out,
+              void* res_out, long long rows, float eps) {
+  __shared__ float part1[NWARPS], part2[NWARPS];
+  constexpr long long ROW_W = (long long)HIDDEN * Dt<DT>::bytes / 4;
+  for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
+    const u32* xr = static_cast<const u32*>(x) + row * ROW_W;
+    u32 wx[R][NWV], wr[R][NWV], wg[R][NWV], wb[R][NWV];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int v = threadIdx.x + i * BLOCK;
+      if (NVR % BLOCK == 0 || v < NVR) {
+        load_words(xr + v * NWV, wx[i]);
+        if constexpr (HAS_RES) load_words(static_cast<const u32*>(res) + row * ROW_W + v * NWV, wr[i]);
+        if constexpr (HAS_GAMMA) load_words_cached(static_cast<const u32*>(gamma) + v * NWV, wg[i]);
+        if constexpr (HAS_BETA) load_words_cached(static_cast<const u32*>(beta) + v * NWV, wb[i]);
+      }
+    }
+    float h[R][VEC];
+    float s1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int v = threadIdx.x + i * BLOCK;
+      if (NVR % BLOCK == 0 || v < NVR) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          h[i][e] = get_elem<DT>(wx[i], e);
+          if constexpr (HAS_RES) h[i][e] += get_elem<DT>(wr[i], e);
+          s1 += h[i][e];
+        }
+        if constexpr (HAS_RES) {
+          u32 o[NWV];
+          pack_vec<DT>(h[i], o);
+          store_words(static_cast<u32*>(res_out) + row * ROW_W + v * NWV, o);
+        }
+      }
+    }
+    const float mean = ln_block_sum(s1, part1) / HIDDEN;
+    float s2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int v = threadIdx.x + i * BLOCK;
+      if (NVR % BLOCK == 0 || v < NVR) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const float d = h[i][e] - mean;
+          s2 += d * d;
+        }
+      }
+    }
+    const float rstd = 1.0f / sqrtf(ln_block_sum(s2, part2) / HIDDEN + eps);
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int v = threadIdx.x + i * BLOCK;
+      if (NVR % BLOCK == 0 || v < NVR) {
+        float y[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          float t = (h[i][e] - mean) * rstd;
+          if constexpr (HAS_GAMMA) t *= get_elem<DT>(wg[i], e);
+          if constexpr (HAS_BETA) t += get_elem<DT>(wb[i], e);
+          y[e] = t;
+        }
+        u32 o[NWV];
+        pack_vec<DT>(y, o);
+        store_words(static_cast<u32*>(out) + row * ROW_W + v * NWV, o);
+      }
+    }
+    __syncthreads();  // part1/part2 are reused by the next row
+  }
+}
+#endif
+
+// any alignment: three passes over the row, element by element
+extern "C" __global__ void __launch_bounds__(BLOCK)
+layernorm_scalar(const void* x, const void* res, const void* gamma, const void* beta, void* out,
+                 void* res_out, long long rows, float eps) {
+  __shared__ float part1[NWARPS], part2[NWARPS];
+  for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
+    const long long base = row * HIDDEN;
+    float s1 = 0.f;
+    for (int i = threadIdx.x; i < HIDDEN; i += BLOCK) {
+      float hv = load_elem<DT>(x, base + i);
+      if constexpr (HAS_RES) hv += load_elem<DT>(res, base + i);
+      s1 += hv;
+    }
+    const float mean = ln_block_sum(s1, part1) / HIDDEN;
+    float s2 = 0.f;
+    for (int i = threadIdx.x; i < HIDDEN; i += BLOCK) {
+      float hv = load_elem<DT>(x, base + i);
+      if constexpr (HAS_RES) hv += load_elem<DT>(res, base + i);
+      s2 += (hv - mean) * (hv - mean);
+    }
+    const float rstd = 1.0f / sqrtf(ln_block_sum(s2, part2) / HIDDEN + eps);
+    for (int i = threadIdx.x; i < HIDDEN; i += BLOCK) {
+      float hv = load_elem<DT>(x, base + i);
+      if constexpr (HAS_RES) {
+        hv += load_elem<DT>(res, base + i);
+        store_elem<DT>(res_out, base + i, hv);
+      }
+      float t = (hv - mean) * rstd;
+      if constexpr (HAS_GAMMA) t *= load_elem<DT>(gamma, i);
+      if constexpr (HAS_BETA) t += load_elem<DT>(beta, i);
+      store_elem<DT>(out, base + i, t);
+    }
+    __syncthreads();
+  }
+}

@@ -122,6 +122,22 @@ int rmsnorm_residual(const void* x, const void* residual, const void* weight, vo
                      void* stream);
 
 /* ------------------------------------------------------------------------
+ * Residual add + LayerNorm + cast ("DeepJIT", section 4.3: one block per
+ * row, mean and variance reduced in the block, then normalised in the same
+ * pass over the data).  Per row r of [rows, hidden]:
+ *   h = x (+ residual)              (fp32)
+ *   residual_out = dt(h)            (when residual is given)
+ *   mean = sum(h) / hidden, var = sum((h - mean)^2) / hidden
+ *   out = dt((h - mean) / sqrt(var + eps) * gamma + beta)
+ * residual and residual_out are both NULL (plain LayerNorm) or both given;
+ * gamma (treated as 1) and beta (treated as 0) may be NULL.  Layouts, dtypes,
+ * in-place rules and limits as rmsnorm_residual.
+ */
+int layernorm_residual(const void* x, const void* residual, const void* gamma, const void* beta,
+                       void* out, void* residual_out, int64_t rows, int64_t hidden, float eps,
+                       fuse_dtype dt, void* stream);
+
+/* ------------------------------------------------------------------------
  * QKV split + transpose + rotate-half RoPE ("TeleTron", section 3.1: QKV
  * projection -> head split -> RoPE).
  * qkv: [tokens, 3, heads, head_dim] (q block, k block, v block per token).

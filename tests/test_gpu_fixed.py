@@ -93,6 +93,69 @@ def test_rmsnorm_full_config_sampled_rows():
     np.testing.assert_allclose(oracle.to_double(to_host(out[st], F.BF16), F.BF16), y, rtol=8e-3)
 
 
+# ------------------------------------------------------------ LayerNorm
+
+def _ln_case(rows, hidden, dt, seed, flags=7, offset=0, inplace=False, eps=1e-5):
+    has_res, has_g, has_b = bool(flags & 1), bool(flags & 2), bool(flags & 4)
+    x = workloads.normal((rows, hidden), 0.5, 1, seed, dt)
+    r = workloads.normal((rows, hidden), 0, 1, seed + 1, dt) if has_res else None
+    g = workloads.normal(hidden, 1, 0.2, seed + 2, dt) if has_g else None
+    b = workloads.normal(hidden, 0, 0.5, seed + 3, dt) if has_b else None
+    dev = [None if a is None else to_dev(a.reshape(-1), dt) for a in (x, r, g, b)]
+    if offset:
+        dev = [None if t is None else misaligned_copy(t, offset) for t in dev]
+    xd, rd, gd, bd = dev
+    out = Guarded(rows * hidden, dt, offset_elems=offset)
+    ro = None
+    if has_res:
+        ro = rd if inplace else Guarded(rows * hidden, dt, offset_elems=offset).t
+    F.layernorm_residual(xd, rd, gd, bd, out.t, ro, eps, dt, rows=rows, hidden=hidden)
+    torch.cuda.synchronize()
+    assert out.canary_ok()
+    y, h, mag = oracle.layernorm_residual(x, r, g, b, dt, eps)
+    if has_res:
+        assert np.array_equal(to_host(ro, dt).reshape(rows, hidden), oracle.store(h, dt))
+    rel = 8e-3 if dt == F.BF16 else (2e-3 if dt == F.F16 else 2e-5)
+    got = oracle.to_double(to_host(out.t, dt), dt).reshape(rows, hidden)
+    bad = np.abs(got - y) > rel * mag
+    assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], y[bad][:5])
+
+
+@pytest.mark.parametrize("rows,hidden", [(3, 4096), (67, 4096), (5, 1000), (4, 7), (2, 65536),
+                                         (1, 1), (9, 768)])
+@pytest.mark.parametrize("dt", [F.BF16, F.F16, F.F32])
+def test_layernorm_shapes(rows, hidden, dt):
+    _ln_case(rows, hidden, dt, 300 + hidden % 89)
+
+
+@pytest.mark.parametrize("flags", [0, 1, 2, 4, 3, 5, 6, 7])
+def test_layernorm_optional_operands(flags):
+    _ln_case(13, 2048, F.BF16, 40 + flags, flags=flags)
+
+
+def test_layernorm_unaligned_and_in_place():
+    _ln_case(11, 4096, F.BF16, 50, offset=1)
+    _ln_case(11, 4096, F.BF16, 51, inplace=True)
+
+
+def test_layernorm_full_config_sampled_rows():
+    rows, hidden, eps = 16384, 4096, 1e-5
+    x = workloads.device_normal((rows, hidden), 0, 1, 61, F.BF16)
+    r = workloads.device_normal((rows, hidden), 0, 1, 62, F.BF16)
+    g = workloads.device_normal((hidden,), 1, 0.1, 63, F.BF16)
+    b = workloads.device_normal((hidden,), 0, 0.1, 64, F.BF16)
+    out, ro = torch.empty_like(x), torch.empty_like(x)
+    F.layernorm_residual(x, r, g, b, out, ro, eps, F.BF16)
+    torch.cuda.synchronize()
+    sel = np.unique(np.concatenate([[0, rows - 1], np.random.default_rng(5).integers(0, rows, 62)]))
+    st = torch.from_numpy(sel).cuda()
+    y, h, mag = oracle.layernorm_residual(to_host(x[st], F.BF16), to_host(r[st], F.BF16),
+                                          to_host(g, F.BF16), to_host(b, F.BF16), F.BF16, eps)
+    assert np.array_equal(to_host(ro[st], F.BF16), oracle.store(h, F.BF16))
+    got = oracle.to_double(to_host(out[st], F.BF16), F.BF16)
+    assert np.all(np.abs(got - y) <= 8e-3 * mag)
+
+
 # ------------------------------------------------------------ QKV split + RoPE
 
 def _rope_check(qkv_host, heads, hd, pos0, dt, got_q, got_k, got_v, tokens_idx=None, base=1e4):
