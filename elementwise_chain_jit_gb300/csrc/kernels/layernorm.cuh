@@ -30,11 +30,26 @@ __device__ __forceinline__ float ln_block_sum(float v, float* part) {
   return t;
 }
 
+// Pairwise combination of (count, mean, sum of squared deviations) of two
+// disjoint sets (Chan, Golub and LeVeque's parallel variance update):
+// mean = mean_a + d*n_b/n, M2 = M2_a + M2_b + d^2*n_a*n_b/n with
+// d = mean_b - mean_a.  Empty sets (n = 0) leave the other side unchanged.
+__device__ __forceinline__ void chan_merge(float& n, float& mean, float& m2, float nb, float meanb,
+                                           float m2b) {
+  const float nt = n + nb;
+  if (nt == 0.f) return;
+  const float d = meanb - mean;
+  const float f = nb / nt;
+  mean += d * f;
+  m2 += m2b + d * d * n * f;
+  n = nt;
+}
+
 #if FUSE_LN_VEC
 extern "C" __global__ void __launch_bounds__(BLOCK)
 layernorm_vec(const void* x, const void* res, const void* gamma, const void* beta, void* out,
               void* res_out, long long rows, float eps) {
-  __shared__ float part1[NWARPS], part2[NWARPS];
+  __shared__ float pn[NWARPS], pmean[NWARPS], pm2[NWARPS];
   constexpr long long ROW_W = (long long)HIDDEN * Dt<DT>::bytes / 4;
   for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
     const u32* xr = static_cast<const u32*>(x) + row * ROW_W;
@@ -68,8 +83,14 @@ layernorm_vec(const void* x, const void* res, const void* gamma, const void* bet
         }
       }
     }
-    const float mean = ln_block_sum(s1, part1) / HIDDEN;
-    float s2 = 0.f;
+    // this thread's (count, mean, M2) over its registers, then one merge tree:
+    // warp lanes into lane 0, then every thread merges the warps' partials in
+    // the same order (one barrier per row, identical statistics everywhere)
+    float cnt = 0.f;
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      if (NVR % BLOCK == 0 || static_cast<int>(threadIdx.x) + i * BLOCK < NVR) cnt += VEC;
+    float mean = cnt > 0.f ? s1 / cnt : 0.f, m2 = 0.f;
 #pragma unroll
     for (int i = 0; i < R; ++i) {
       const int v = threadIdx.x + i * BLOCK;
@@ -77,11 +98,67 @@ layernorm_vec(const void* x, const void* res, const void* gamma, const void* bet
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
           const float d = h[i][e] - mean;
-          s2 += d * d;
+          m2 += d * d;
         }
       }
     }
-    const float rstd = 1.0f / sqrtf(ln_block_sum(s2, part2) / HIDDEN + eps);
+    if constexpr (NVR % BLOCK == 0 && (NWARPS & (NWARPS - 1)) == 0) {
+      // every thread holds R*VEC values: each merge joins two equal sets, so
+      // mean = (a + b) / 2 and M2 = M2a + M2b + d^2 * n / 2 (n per side)
+      float half_n = 0.5f * cnt;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float mb = __shfl_down_sync(0xffffffffu, mean, o);
+        const float qb = __shfl_down_sync(0xffffffffu, m2, o);
+        const float d = mb - mean;
+        mean = 0.5f * (mean + mb);
+        m2 += qb + d * d * half_n;
+        half_n *= 2.f;
+      }
+      if ((threadIdx.x & 31) == 0) {
+        pmean[threadIdx.x >> 5] = mean;
+        pm2[threadIdx.x >> 5] = m2;
+      }
+      __syncthreads();
+      float wm[NWARPS], wq[NWARPS];
+#pragma unroll
+      for (int w = 0; w < NWARPS; ++w) {
+        wm[w] = pmean[w];
+        wq[w] = pm2[w];
+      }
+#pragma unroll
+      for (int step = 1; step < NWARPS; step *= 2) {
+#pragma unroll
+        for (int w = 0; w + step < NWARPS; w += 2 * step) {
+          const float d = wm[w + step] - wm[w];
+          wm[w] = 0.5f * (wm[w] + wm[w + step]);
+          wq[w] += wq[w + step] + d * d * half_n;
+        }
+        half_n *= 2.f;
+      }
+      mean = wm[0];
+      m2 = wq[0];
+    } else {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float nb = __shfl_down_sync(0xffffffffu, cnt, o);
+        const float mb = __shfl_down_sync(0xffffffffu, mean, o);
+        const float qb = __shfl_down_sync(0xffffffffu, m2, o);
+        chan_merge(cnt, mean, m2, nb, mb, qb);
+      }
+      if ((threadIdx.x & 31) == 0) {
+        pn[threadIdx.x >> 5] = cnt;
+        pmean[threadIdx.x >> 5] = mean;
+        pm2[threadIdx.x >> 5] = m2;
+      }
+      __syncthreads();
+      cnt = pn[0];
+      mean = pmean[0];
+      m2 = pm2[0];
+#pragma unroll
+      for (int w = 1; w < NWARPS; ++w) chan_merge(cnt, mean, m2, pn[w], pmean[w], pm2[w]);
+    }
+    const float rstd = 1.0f / sqrtf(m2 / HIDDEN + eps);
 #pragma unroll
     for (int i = 0; i < R; ++i) {
       const int v = threadIdx.x + i * BLOCK;
@@ -99,7 +176,7 @@ layernorm_vec(const void* x, const void* res, const void* gamma, const void* bet
         store_words(static_cast<u32*>(out) + row * ROW_W + v * NWV, o);
       }
     }
-    __syncthreads();  // part1/part2 are reused by the next row
+    __syncthreads();  // pn/pmean/pm2 are reused by the next row
   }
 }
 #endif
