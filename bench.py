@@ -142,10 +142,10 @@ def _esz(dt):
     return 4 if dt == 0 else 2
 
 
-def build_items(dev, with_unfused=True, only=None, flat_elems=None):
+def build_items(dev, with_unfused=True, only=None, flat_elems=None, spec=None, spec_dtype=0):
     """The step's workloads; `only` (a regex) keeps the matching ones and
     `flat_elems` changes the flat chains' size (both for profiling a single
-    kernel on a smaller case)."""
+    kernel on a smaller case); `spec` replaces them all by one given chain."""
     import re
 
     import torch
@@ -171,8 +171,11 @@ def build_items(dev, with_unfused=True, only=None, flat_elems=None):
             it.unfused, it.n_unfused = unfused_chain(spec, dt, shape, ins, out)
         return it
 
-    # chain sweep, flat, 2^28 + 7
     n_flat = flat_elems or W.FLAT_SIZES[-1]
+    if spec is not None:  # one given chain, flat, as the only workload
+        items.append(chain_item(f"chain[{spec}]_n{n_flat}", spec, spec_dtype, (n_flat,), 7))
+        return items
+    # chain sweep, flat, 2^28 + 7
     for L in W.CHAIN_LENGTHS:
         spec, dt = W.random_chain(L, 5)
         if want(f"flat_chain_L{L}_n{n_flat}"):
@@ -607,7 +610,8 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     items = build_items(dev, with_unfused=not args.no_unfused, only=args.only,
-                        flat_elems=args.flat_elems)
+                        flat_elems=args.flat_elems, spec=args.spec,
+                        spec_dtype={"f32": 0, "f16": 1, "bf16": 2}[args.spec_dtype])
     if not items:
         raise SystemExit(f"--only {args.only!r} matches no workload")
     torch.cuda.synchronize()
@@ -768,8 +772,8 @@ def run_gpu(args):
                        "storage_dtypes": "f32/f16/bf16 per workload, arithmetic in f32"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clk, "per_chain": per_chain, "next_rows": next_rows,
-            "partial": ({"only": args.only, "flat_elems": args.flat_elems}
-                        if args.only or args.flat_elems else None),
+            "partial": ({"only": args.only, "flat_elems": args.flat_elems, "spec": args.spec}
+                        if args.only or args.flat_elems or args.spec else None),
             "frac_of_peak": value / world / peak, "peak_gbs": peak}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -790,6 +794,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only", default=None, help="regex: run only the matching workloads")
     ap.add_argument("--flat-elems", type=int, default=None, help="size of the flat chains")
+    ap.add_argument("--spec", default=None, help="time this one chain (flat) instead")
+    ap.add_argument("--spec-dtype", default="f32", choices=["f32", "f16", "bf16"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

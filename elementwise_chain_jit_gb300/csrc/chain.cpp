@@ -216,9 +216,10 @@ static void emit_op(std::ostringstream& s, const ChainOp& op, const std::string&
     case OP_MUL: s << "      x = x * " << operand(elem_of_input, op.input) << ";\n"; break;
     case OP_SCALE: s << "      x = x * " << hex_float(op.c) << ";\n"; break;
     case OP_RELU: s << "      x = x > 0.f ? x : 0.f;\n"; break;
-    // 1 / (1 + exp(-x)) with the IEEE round-to-nearest reciprocal (the same
-    // correctly rounded value as the division 1.0f / y, in fewer instructions)
-    case OP_SIGMOID: s << "      x = __frcp_rn(1.0f + expf(-x));\n"; break;
+    // 1 / (1 + exp(-x)); the reciprocal of a value >= 1 by one Newton step on
+    // the hardware approximation (common.cuh), a third of the instructions of
+    // the IEEE division for the same result within an ulp
+    case OP_SIGMOID: s << "      x = sigmoid(x);\n"; break;
     case OP_EXP: s << "      x = expf(x);\n"; break;
     case OP_CAST:
       if (op.to == FUSE_F16) s << "      x = round_f16(x);\n";

@@ -243,10 +243,11 @@ void oracle_chain_eval(int n_ops, const int* ops, const double* args, const int*
  *        relu:           E' = E                          (1-Lipschitz, exact)
  *        exp:            E' = e^v (e^E - 1) + 4u e^(v+E) + eta
  *                        (expf is documented to 2 ulp = 4u relative)
- *        sigmoid:        E' = E/4 + 8u (sigma(v) + E/4) + eta
- *                        (|sigma'| <= 1/4; expf 2 ulp, add and divide 1/2 ulp
- *                        each), widened to [0, sigma(v+E)] where exp(-x) can
- *                        overflow fp32
+ *        sigmoid:        E' = D E + 10u (sigma(v) + D E) + eta
+ *                        (D the largest |sigma'| on [v - E, v + E], at most
+ *                        1/4; expf 2 ulp, the add 1/2 ulp, the reciprocal
+ *                        within 1 ulp, with margin), widened to
+ *                        [0, sigma(v + E)] where 1 + exp(-x) can reach 2^126
  *      with u = 2^-24 and eta = 2^-147 covering fp32 underflow.  Where the
  *      interval [v - E, v + E] straddles a rounding boundary of a cast or the
  *      fp32 overflow threshold, each outcome is followed as its own branch;
@@ -308,10 +309,13 @@ static int step_branch(int op, branch_t s, double b, double c, int out_dt_unused
       double xm = (v - E <= 0.0 && v + E >= 0.0) ? 0.0 : (v > 0.0 ? v - E : v + E);
       double sm = 1.0 / (1.0 + exp(-xm));
       double dmax = sm * (1.0 - sm);
-      En = dmax * E + 8 * U32 * (vn + dmax * E) + ETA;
-      if (-(v - E) >= 88.0) { /* exp(-x) may overflow in fp32: result may be 0 */
+      En = dmax * E + 10 * U32 * (vn + dmax * E) + ETA;
+      /* from -x >= 87 on, 1 + exp(-x) may reach 2^126 (or overflow to inf) in
+         fp32 and the device's reciprocal returns 0 for a true value below
+         2^-126: accept any value in [0, sigma(v + E)] there */
+      if (-(v - E) >= 87.0) {
         double hi = 1.0 / (1.0 + exp(-(v + E)));
-        if (hi * (1 + 8 * U32) > En) En = hi * (1 + 8 * U32) + ETA;
+        if (hi * (1 + 10 * U32) > En) En = hi * (1 + 10 * U32) + ETA;
       }
       break;
     }

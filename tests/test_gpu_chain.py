@@ -59,6 +59,23 @@ def test_add_relu_scale_golden_on_device():
     assert np.array_equal(got, want) and not np.any(np.signbit(got))
 
 
+# ------------------------------------------------------------ every fp16 input, one op
+
+@pytest.mark.parametrize("op", ["relu", "sigmoid", "exp", "scale:0.7529296875", "cast:bf16"])
+@pytest.mark.parametrize("out", ["f16", "f32"])
+def test_unary_op_on_every_fp16_value(op, out):
+    """All 65,536 fp16 bit patterns (incl. subnormals, inf, NaN) through one
+    op, stored as fp16 or (after a cast to fp32) as fp32."""
+    x = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    spec = op if out == "f16" else "cast:f32;" + op
+    if op == "cast:bf16":
+        spec = "cast:bf16" if out == "f16" else "cast:bf16;cast:f32"
+    got, c = _run_chain(spec, F.F16, [x], x.shape)
+    fails, counts, cls = oracle.chain_check(spec, F.F16, [x], x.shape, got)
+    assert fails == 0, (spec, counts, x[cls == 2][:8])
+    assert counts[3] == 0, (spec, counts)
+
+
 # ------------------------------------------------------------ random chains
 
 def _check(spec, dt, inputs, shape, got, idx=None):
