@@ -173,14 +173,22 @@ int plan_chain(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_d
     minb = std::min(minb, dtype_bytes(d));
     bytes_per_elem += dtype_bytes(d);
   }
-  const int budget = env_int("FUSE_CHAIN_WORD_BUDGET", 48);
+  bool transcendental = false;
+  for (auto& op : ch.ops) transcendental = transcendental || op.op == OP_EXP || op.op == OP_SIGMOID;
+  // Measured on GB300 (sweep over the chain workloads): chains touching 12 or
+  // more tensors run fastest with a small per-thread footprint (more warps,
+  // the 13-input chain 1.64 ms vs 1.86 ms), others with the widest vectors
+  // (the 6-tensor chain 537 us vs 558 us); chains with exp/sigmoid lose by
+  // unrolling (more registers, fewer warps to hide the arithmetic).
+  const int tensors = static_cast<int>(ch.in_dt.size()) + 1;
+  const int budget = env_int("FUSE_CHAIN_WORD_BUDGET", tensors >= 12 ? 32 : 64);
   int vec_bytes = env_int("FUSE_CHAIN_VEC_BYTES", 32);
   if (vec_bytes != 4 && vec_bytes != 8 && vec_bytes != 16 && vec_bytes != 32) vec_bytes = 32;
   while (vec_bytes > 4 && (vec_bytes / minb) * bytes_per_elem / 4 > budget) vec_bytes /= 2;
   p->vec = vec_bytes / minb;
   const int words = p->vec * bytes_per_elem / 4;
   // vectors in flight per thread: enough to cover latency, bounded registers
-  int max_unroll = env_int("FUSE_CHAIN_UNROLL", 2);
+  int max_unroll = env_int("FUSE_CHAIN_UNROLL", transcendental ? 1 : 2);
   p->unroll = 1;
   while (p->unroll * 2 <= max_unroll && words * p->unroll * 2 <= budget) p->unroll *= 2;
   p->block = env_int("FUSE_CHAIN_BLOCK", 256);
