@@ -365,7 +365,9 @@ struct fuse_chain {
     CUfunction vec_fn, scalar_fn;
     unsigned vec_grid, scalar_grid;
   };
-  std::vector<PerDevice> dev;
+  // one entry per device that launched the chain; entries never move (a
+  // launch keeps using its entry after the lock is released)
+  std::vector<std::unique_ptr<PerDevice>> dev;
 };
 
 namespace fuse {
@@ -373,8 +375,8 @@ namespace fuse {
 static int chain_device_state(fuse_chain* h, const DeviceInfo& d, fuse_chain::PerDevice** out) {
   std::lock_guard<std::mutex> lk(h->mu);
   for (auto& pd : h->dev)
-    if (pd.device == d.ordinal) {
-      *out = &pd;
+    if (pd->device == d.ordinal) {
+      *out = pd.get();
       return FUSE_OK;
     }
   fuse_chain::PerDevice pd{};
@@ -402,8 +404,8 @@ static int chain_device_state(fuse_chain* h, const DeviceInfo& d, fuse_chain::Pe
     if (per_sm > 0) cap = int64_t(d.sms) * std::min(per_sm, std::max(occ, 1));
     pd.vec_grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(nfull, cap)));
   }
-  h->dev.push_back(pd);
-  *out = &h->dev.back();
+  h->dev.push_back(std::make_unique<fuse_chain::PerDevice>(pd));
+  *out = h->dev.back().get();
   return FUSE_OK;
 }
 

@@ -37,17 +37,29 @@ __device__ __forceinline__ void tile_work(const void* feat, float* out, int a, i
   constexpr int G = TC / 8;
   const int ncell = HW - c0 < TC ? HW - c0 : TC;
   if constexpr (VEC && HW % 8 == 0) {
+    // every (channel, 8-cell group) item of this thread: all loads first,
+    // then the decodes, so the loads of a tile are in flight together
     constexpr int NWI = 8 * Dt<DT>::bytes / 4;
-    for (int it = threadIdx.x; it < NO * G; it += BLOCK) {
+    constexpr int PER = (NO * G + BLOCK - 1) / BLOCK;
+    u32 w[PER][NWI];
+#pragma unroll
+    for (int n = 0; n < PER; ++n) {
+      const int it = threadIdx.x + n * BLOCK;
+      const int k = it / G, g = it % G;
+      if (it < NO * G && c0 + g * 8 < HW) {
+        const long long off = static_cast<long long>(a * NO + k) * HW + c0 + g * 8;
+        load_words(static_cast<const u32*>(feat) + off * Dt<DT>::bytes / 4, w[n]);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < PER; ++n) {
+      const int it = threadIdx.x + n * BLOCK;
       const int k = it / G, g = it % G;
       const int cell = c0 + g * 8;
-      if (cell < HW) {
-        const long long off = static_cast<long long>(a * NO + k) * HW + cell;
-        u32 w[NWI];
-        load_words(static_cast<const u32*>(feat) + off * Dt<DT>::bytes / 4, w);
+      if (it < NO * G && cell < HW) {
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-          tile[(g * 8 + e) * NO + k] = decode<W>(k, cell + e, get_elem<DT>(w, e), stride, aw, ah);
+          tile[(g * 8 + e) * NO + k] = decode<W>(k, cell + e, get_elem<DT>(w[n], e), stride, aw, ah);
       }
     }
   } else {
