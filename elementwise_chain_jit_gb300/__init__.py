@@ -26,7 +26,8 @@ STATUS = {0: "FUSE_OK", -1: "FUSE_E_SPEC", -2: "FUSE_E_SHAPE", -3: "FUSE_E_DTYPE
 
 # every symbol include/fuse.h declares
 EXPORTS = ["fuse_compile", "fuse_num_inputs", "fuse_input_dtypes", "fuse_launch", "fuse_release",
-           "fuse_source", "rmsnorm_residual", "layernorm_residual", "rope_qkv_split", "rope_qkv_split_noalloc",
+           "fuse_source", "fuse_compile_bucket", "fuse_launch_rows", "fuse_source_bucket",
+           "fuse_bucket", "rmsnorm_residual", "layernorm_residual", "rope_qkv_split", "rope_qkv_split_noalloc",
            "detect_decode", "channel_shuffle", "fuse_graph_begin", "fuse_graph_end",
            "fuse_graph_launch", "fuse_graph_nodes", "fuse_graph_release", "fuse_last_error",
            "fuse_stats", "fuse_device_sms"]
@@ -51,6 +52,12 @@ _lib.fuse_launch.argtypes = [_P, ctypes.POINTER(_P), _I, _P, _P]
 _lib.fuse_release.argtypes = [_P]
 _lib.fuse_source.argtypes = [ctypes.c_char_p, ctypes.POINTER(_I64), _I, _I, ctypes.c_char_p,
                              ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
+_lib.fuse_compile_bucket.argtypes = [ctypes.c_char_p, ctypes.POINTER(_I64), _I, _I,
+                                     ctypes.POINTER(_P)]
+_lib.fuse_launch_rows.argtypes = [_P, ctypes.POINTER(_P), _I, _P, _I64, _P]
+_lib.fuse_source_bucket.argtypes = [ctypes.c_char_p, ctypes.POINTER(_I64), _I, _I, ctypes.c_char_p,
+                                    ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
+_lib.fuse_bucket.argtypes = [_I64, ctypes.POINTER(_I64)]
 _lib.rmsnorm_residual.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P]
 _lib.layernorm_residual.argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P]
 _lib.rope_qkv_split.argtypes = [_P, _P, _P, _P, _I64, _I, _I, _I64, _F, _I, _P]
@@ -147,14 +154,39 @@ def fuse_release(chain: Chain) -> None:
     _check(_lib.fuse_release(chain.handle))
 
 
-def fuse_source(spec: str, shape, in_dtype) -> str:
+def fuse_source(spec: str, shape, in_dtype, bucket: bool = False) -> str:
+    fn = _lib.fuse_source_bucket if bucket else _lib.fuse_source
     arr, nd = _shape(shape)
     n = ctypes.c_size_t()
-    _check(_lib.fuse_source(spec.encode(), arr, nd, _dtype(in_dtype), None, 0, ctypes.byref(n)))
+    _check(fn(spec.encode(), arr, nd, _dtype(in_dtype), None, 0, ctypes.byref(n)))
     buf = ctypes.create_string_buffer(n.value + 1)
-    _check(_lib.fuse_source(spec.encode(), arr, nd, _dtype(in_dtype), buf, n.value + 1,
-                            ctypes.byref(n)))
+    _check(fn(spec.encode(), arr, nd, _dtype(in_dtype), buf, n.value + 1, ctypes.byref(n)))
     return buf.value.decode()
+
+
+def fuse_source_bucket(spec: str, shape, in_dtype) -> str:
+    return fuse_source(spec, shape, in_dtype, bucket=True)
+
+
+def fuse_compile_bucket(spec: str, shape, in_dtype) -> Chain:
+    """A chain whose leading dimension shape[0] is an upper bound (see
+    fuse_launch_rows)."""
+    h = _P()
+    arr, nd = _shape(shape)
+    _check(_lib.fuse_compile_bucket(spec.encode(), arr, nd, _dtype(in_dtype), ctypes.byref(h)))
+    return Chain(h.value, spec, shape)
+
+
+def fuse_launch_rows(chain: Chain, inputs, output, rows: int, stream=None) -> None:
+    ptrs = (_P * max(1, len(inputs)))(*[_ptr(t) for t in inputs])
+    _check(_lib.fuse_launch_rows(chain.handle, ptrs, len(inputs), _ptr(output), int(rows),
+                                 _stream(stream)))
+
+
+def fuse_bucket(n: int) -> int:
+    b = _I64()
+    _check(_lib.fuse_bucket(int(n), ctypes.byref(b)))
+    return b.value
 
 
 # ---------------------------------------------------------------- fixed entry points

@@ -16,8 +16,9 @@ namespace fuse {
 const char* last_error_cstr();
 void read_stats(int64_t* c, int64_t* h, int64_t* l, double* ms);
 int chain_compile(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dt,
-                  fuse_chain** out);
-int chain_launch(fuse_chain* h, const void* const* inputs, int n_in, void* output, void* stream);
+                  fuse_chain** out, bool bucket);
+int chain_launch(fuse_chain* h, const void* const* inputs, int n_in, void* output, void* stream,
+                 int64_t rows);
 
 namespace {
 std::mutex g_shuffle_mu;
@@ -61,12 +62,12 @@ int channel_shuffle(const void* in, void* out, int64_t n, int64_t c, int64_t h, 
     } else {
       int64_t shape[4] = {n, c, h, w};
       std::string spec = fmt("shuffle:%d", groups);
-      if (int rc = chain_compile(spec.c_str(), shape, 4, dt, &hnd)) return rc;
+      if (int rc = chain_compile(spec.c_str(), shape, 4, dt, &hnd, false)) return rc;
       g_shuffle.emplace(key, hnd);
     }
   }
   const void* ins[1] = {in};
-  return chain_launch(hnd, ins, 1, out, stream);
+  return chain_launch(hnd, ins, 1, out, stream, -1);
 }
 
 }  // extern "C"

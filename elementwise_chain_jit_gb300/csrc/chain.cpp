@@ -132,6 +132,8 @@ struct ChainPlan {
   int unroll = 1;
   bool vec_ok = false;
   int64_t C = 1, HW = 1;
+  bool dynamic = false;  // shape bucket: the leading dimension comes with the launch
+  int64_t inner = 1;     // elements per unit of the leading dimension
   std::string source;
 };
 
@@ -154,6 +156,8 @@ int plan_chain(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_d
   }
   if (n > kMaxElems) return fail(FUSE_E_SHAPE, "more than 2^40 elements");
   p->n = n;
+  p->inner = 1;
+  for (int i = 1; i < ndim; ++i) p->inner *= shape[i];
   const Chain& ch = p->ch;
   if (ch.groups) {
     if (ndim != 4) return fail(FUSE_E_SHAPE, "shuffle needs a 4-D NCHW shape");
@@ -262,7 +266,15 @@ static std::string gen_chain_source(const ChainPlan& p, const char* spec) {
   }
   s << "constexpr int DTO = " << ch.out_dt << ";  // " << dtype_name(ch.out_dt) << "\n";
   s << "constexpr int NWO = VEC * Dt<DTO>::bytes / 4;\n";
-  s << "struct Args { const void* in[NIN]; void* out; };\n\n";
+  if (p.dynamic) {
+    // shape bucket: N above is the largest element count; the launch passes
+    // the actual one
+    s << "struct Args { const void* in[NIN]; void* out; long long n; };\n";
+    s << "#define SIZE_N(a) ((a).n)\n\n";
+  } else {
+    s << "struct Args { const void* in[NIN]; void* out; };\n";
+    s << "#define SIZE_N(a) N\n\n";
+  }
 
   // index of input 0 for an output element / vector (ChannelShuffle prologue)
   if (ch.groups) {
@@ -317,36 +329,41 @@ static std::string gen_chain_source(const ChainPlan& p, const char* spec) {
 
   // vector kernel
   if (p.vec_ok) {
-    s << "\n// vectors [v0, v0 + UNROLL*BLOCK) with stride BLOCK; CHECK: bound by NVEC\n";
-    s << "template <bool CHECK>\n__device__ __forceinline__ void do_chunk(const Args& a, idx_t v0) {\n";
+    s << "\n// vectors [v0, v0 + UNROLL*BLOCK) with stride BLOCK; CHECK: bound by nvec\n";
+    s << "template <bool CHECK>\n__device__ __forceinline__ void do_chunk(const Args& a, idx_t v0, "
+         "idx_t nvec) {\n";
     for (int j = 0; j < nin; ++j) s << "  u32 r" << j << "[UNROLL][NW" << j << "];\n";
     s << "#pragma unroll\n  for (int u = 0; u < UNROLL; ++u) {\n"
          "    const idx_t v = v0 + (idx_t)u * BLOCK;\n"
-         "    if (CHECK && v >= (idx_t)NVEC) break;\n";
+         "    if (CHECK && v >= nvec) break;\n";
     for (int j = 0; j < nin; ++j) {
       s << "    load_words(static_cast<const u32*>(a.in[" << j << "]) + (idx_t)"
         << (j == 0 ? "src_vec(v)" : "v") << " * NW" << j << ", r" << j << "[u]);\n";
     }
     s << "  }\n#pragma unroll\n  for (int u = 0; u < UNROLL; ++u) {\n"
          "    const idx_t v = v0 + (idx_t)u * BLOCK;\n"
-         "    if (CHECK && v >= (idx_t)NVEC) break;\n"
+         "    if (CHECK && v >= nvec) break;\n"
          "    u32 wo[NWO];\n    apply(";
     for (int j = 0; j < nin; ++j) s << "r" << j << "[u], ";
     s << "wo);\n    store_words(static_cast<u32*>(a.out) + v * NWO, wo);\n  }\n}\n";
+    // sizes: compile-time constants for a fixed shape (the compiler folds
+    // every branch below), the launch's element count for a shape bucket
     s << "\nextern \"C\" __global__ void __launch_bounds__(BLOCK) fuse_chain_vec(const Args a) {\n"
-         "  for (idx_t c = blockIdx.x; c < (idx_t)NFULL; c += gridDim.x)\n"
-         "    do_chunk<false>(a, c * (idx_t)CHUNK + threadIdx.x);\n"
-         "  if constexpr (NREM > 0 || TAIL > 0) {\n"
+         "  const idx_t n = (idx_t)SIZE_N(a), nvec = n / VEC, nfull = nvec / (idx_t)CHUNK;\n"
+         "  const idx_t nrem = nvec - nfull * (idx_t)CHUNK, tail = n - nvec * VEC;\n"
+         "  for (idx_t c = blockIdx.x; c < nfull; c += gridDim.x)\n"
+         "    do_chunk<false>(a, c * (idx_t)CHUNK + threadIdx.x, nvec);\n"
+         "  if (nrem > 0 || tail > 0) {\n"
          "    // the CTA with the fewest full chunks takes the remainder and the tail\n"
-         "    if (blockIdx.x == (unsigned)(NFULL % gridDim.x)) {\n"
-         "      if constexpr (NREM > 0) do_chunk<true>(a, (idx_t)NFULL * CHUNK + threadIdx.x);\n"
-         "      if constexpr (TAIL > 0)\n"
-         "        if (threadIdx.x < TAIL) apply_elem(a, (idx_t)NVEC * VEC + threadIdx.x);\n"
+         "    if (blockIdx.x == (unsigned)(nfull % gridDim.x)) {\n"
+         "      if (nrem > 0) do_chunk<true>(a, nfull * (idx_t)CHUNK + threadIdx.x, nvec);\n"
+         "      if (threadIdx.x < tail) apply_elem(a, nvec * VEC + threadIdx.x);\n"
          "    }\n  }\n}\n";
   }
   // scalar kernel: any alignment
   s << "\nextern \"C\" __global__ void __launch_bounds__(256) fuse_chain_scalar(const Args a) {\n"
-       "  for (idx_t e = (idx_t)blockIdx.x * 256 + threadIdx.x; e < (idx_t)N;"
+       "  const idx_t n = (idx_t)SIZE_N(a);\n"
+       "  for (idx_t e = (idx_t)blockIdx.x * 256 + threadIdx.x; e < n;"
        " e += (idx_t)gridDim.x * 256)\n"
        "    apply_elem(a, e);\n}\n";
   return s.str();
@@ -361,9 +378,9 @@ struct fuse_chain {
   std::shared_ptr<fuse::Module> mod;
   std::mutex mu;
   struct PerDevice {
-    int device;
+    int device, sms;
     CUfunction vec_fn, scalar_fn;
-    unsigned vec_grid, scalar_grid;
+    int occ_vec, occ_scalar;  // resident CTAs per SM of each kernel
   };
   // one entry per device that launched the chain; entries never move (a
   // launch keeps using its entry after the lock is released)
@@ -381,38 +398,44 @@ static int chain_device_state(fuse_chain* h, const DeviceInfo& d, fuse_chain::Pe
     }
   fuse_chain::PerDevice pd{};
   pd.device = d.ordinal;
+  pd.sms = d.sms;
   const DriverApi* api;
   if (int rc = driver(&api)) return rc;
   const ChainPlan& p = h->plan;
   if (int rc = jit_function(*h->mod, "fuse_chain_scalar", d, &pd.scalar_fn)) return rc;
-  int occ = 0;
-  CUresult r = api->OccupancyMaxActiveBlocksPerMultiprocessor(&occ, pd.scalar_fn, 256, 0);
+  CUresult r = api->OccupancyMaxActiveBlocksPerMultiprocessor(&pd.occ_scalar, pd.scalar_fn, 256, 0);
   if (r != CUDA_SUCCESS) return cuda_fail(r, "cuOccupancyMaxActiveBlocksPerMultiprocessor");
-  int64_t want = (p.n + 255) / 256;
-  pd.scalar_grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(d.sms) * std::max(occ, 1))));
   if (p.vec_ok) {
     if (int rc = jit_function(*h->mod, "fuse_chain_vec", d, &pd.vec_fn)) return rc;
-    r = api->OccupancyMaxActiveBlocksPerMultiprocessor(&occ, pd.vec_fn, p.block, 0);
+    r = api->OccupancyMaxActiveBlocksPerMultiprocessor(&pd.occ_vec, pd.vec_fn, p.block, 0);
     if (r != CUDA_SUCCESS) return cuda_fail(r, "cuOccupancyMaxActiveBlocksPerMultiprocessor");
-    // One chunk per CTA: the block scheduler hands chunks to SMs as they free
-    // up, so the last wave is at most one chunk long.  FUSE_CHAIN_CTAS_PER_SM
-    // instead sizes a persistent grid of SMs x that many CTAs.
-    int per_sm = env_int("FUSE_CHAIN_CTAS_PER_SM", 0);
-    int64_t chunk = int64_t(p.block) * p.unroll;
-    int64_t nfull = (p.n / p.vec) / chunk;
-    int64_t cap = int64_t(1) << 30;
-    if (per_sm > 0) cap = int64_t(d.sms) * std::min(per_sm, std::max(occ, 1));
-    pd.vec_grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(nfull, cap)));
   }
   h->dev.push_back(std::make_unique<fuse_chain::PerDevice>(pd));
   *out = h->dev.back().get();
   return FUSE_OK;
 }
 
+// Grids for n elements.  Vector kernel: one chunk per CTA, so the block
+// scheduler hands chunks to SMs as they free up and the last wave is at most
+// one chunk long (FUSE_CHAIN_CTAS_PER_SM instead sizes a persistent grid of
+// SMs x that many CTAs).  Scalar kernel: a grid-stride loop over resident CTAs.
+static void chain_grids(const ChainPlan& p, const fuse_chain::PerDevice& pd, int64_t n,
+                        unsigned* vec_grid, unsigned* scalar_grid) {
+  const int64_t want = (n + 255) / 256;
+  *scalar_grid = static_cast<unsigned>(std::max<int64_t>(
+      1, std::min<int64_t>(want, int64_t(pd.sms) * std::max(pd.occ_scalar, 1))));
+  const int per_sm = env_int("FUSE_CHAIN_CTAS_PER_SM", 0);
+  const int64_t nfull = (n / p.vec) / (int64_t(p.block) * p.unroll);
+  int64_t cap = int64_t(1) << 30;
+  if (per_sm > 0) cap = int64_t(pd.sms) * std::min(per_sm, std::max(pd.occ_vec, 1));
+  *vec_grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(nfull, cap)));
+}
+
 int chain_compile(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dt,
-                  fuse_chain** out) {
+                  fuse_chain** out, bool bucket) {
   auto h = std::make_unique<fuse_chain>();
   if (int rc = plan_chain(spec, shape, ndim, in_dt, &h->plan)) return rc;
+  h->plan.dynamic = bucket;
   h->plan.source = gen_chain_source(h->plan, spec);
   if (int rc = jit_compile(h->plan.source, "fuse_chain", &h->mod)) return rc;
   // load now when a device is present, so that the first launch does no work
@@ -427,18 +450,30 @@ int chain_compile(const char* spec, const int64_t* shape, int ndim, fuse_dtype i
 }
 
 int chain_source(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dt,
-                 std::string* src) {
+                 std::string* src, bool bucket) {
   ChainPlan p;
   if (int rc = plan_chain(spec, shape, ndim, in_dt, &p)) return rc;
+  p.dynamic = bucket;
   *src = gen_chain_source(p, spec);
   return FUSE_OK;
 }
 
-int chain_launch(fuse_chain* h, const void* const* inputs, int n_in, void* output, void* stream) {
+// rows < 0: the compiled leading dimension.  A bucket handle accepts any
+// 0 <= rows <= its leading dimension; a fixed handle only its own.
+int chain_launch(fuse_chain* h, const void* const* inputs, int n_in, void* output, void* stream,
+                 int64_t rows) {
   const ChainPlan& p = h->plan;
   const int nin = static_cast<int>(p.ch.in_dt.size());
   if (n_in != nin) return fail(FUSE_E_ARG, fmt("chain takes %d inputs, got %d", nin, n_in));
-  if (p.n == 0) return FUSE_OK;
+  int64_t n = p.n;
+  if (rows >= 0) {
+    if (rows > p.shape[0] || (!p.dynamic && rows != p.shape[0]))
+      return fail(FUSE_E_SHAPE,
+                  fmt("leading dimension %lld: the handle was compiled for %s%lld",
+                      (long long)rows, p.dynamic ? "at most " : "", (long long)p.shape[0]));
+    n = rows * p.inner;
+  }
+  if (n == 0) return FUSE_OK;
   if (!inputs) return fail(FUSE_E_NULL, "inputs is NULL");
   if (!output) return fail(FUSE_E_NULL, "output is NULL");
   bool aligned = aligned16(output);
@@ -452,10 +487,14 @@ int chain_launch(fuse_chain* h, const void* const* inputs, int n_in, void* outpu
   if (int rc = current_device(&d)) return rc;
   fuse_chain::PerDevice* pd;
   if (int rc = chain_device_state(h, d, &pd)) return rc;
-  // kernel parameter: the Args struct {in[NIN], out}
-  std::vector<const void*> args(inputs, inputs + nin);
-  args.push_back(output);
+  // kernel parameter: the Args struct {in[NIN], out[, n]} as 8-byte words
+  std::vector<uint64_t> args(static_cast<size_t>(nin) + 2);
+  for (int j = 0; j < nin; ++j) args[j] = reinterpret_cast<uintptr_t>(inputs[j]);
+  args[nin] = reinterpret_cast<uintptr_t>(output);
+  args[nin + 1] = static_cast<uint64_t>(n);
   void* kargs[] = {args.data()};
+  unsigned vec_grid, scalar_grid;
+  chain_grids(p, *pd, n, &vec_grid, &scalar_grid);
   // 32-byte accesses need 32-byte alignment when a vector spans 32 bytes
   bool use_vec = p.vec_ok && aligned;
   if (use_vec) {
@@ -467,13 +506,23 @@ int chain_launch(fuse_chain* h, const void* const* inputs, int n_in, void* outpu
       if (reinterpret_cast<uintptr_t>(ptr) % need) use_vec = false;
     }
   }
-  if (use_vec) return launch(pd->vec_fn, pd->vec_grid, p.block, 0, stream, kargs);
-  return launch(pd->scalar_fn, pd->scalar_grid, 256, 0, stream, kargs);
+  if (use_vec) return launch(pd->vec_fn, vec_grid, p.block, 0, stream, kargs);
+  return launch(pd->scalar_fn, scalar_grid, 256, 0, stream, kargs);
 }
 
 }  // namespace fuse
 
 // ------------------------------------------------------------------ C ABI
+
+static int copy_source(const std::string& src, char* buf, size_t cap, size_t* len) {
+  if (len) *len = src.size();
+  if (buf && cap) {
+    size_t n = std::min(cap - 1, src.size());
+    memcpy(buf, src.data(), n);
+    buf[n] = '\0';
+  }
+  return FUSE_OK;
+}
 
 extern "C" {
 
@@ -481,7 +530,23 @@ int fuse_compile(const char* spec, const int64_t* shape, int ndim, fuse_dtype in
                  fuse_handle* out) {
   if (!out) return fuse::fail(FUSE_E_NULL, "out is NULL");
   *out = nullptr;
-  return fuse::chain_compile(spec, shape, ndim, in_dtype, out);
+  return fuse::chain_compile(spec, shape, ndim, in_dtype, out, false);
+}
+
+int fuse_compile_bucket(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dtype,
+                        fuse_handle* out) {
+  if (!out) return fuse::fail(FUSE_E_NULL, "out is NULL");
+  *out = nullptr;
+  return fuse::chain_compile(spec, shape, ndim, in_dtype, out, true);
+}
+
+int fuse_bucket(int64_t n, int64_t* bucket) {
+  if (!bucket) return fuse::fail(FUSE_E_NULL, "bucket is NULL");
+  if (n < 0 || n > (int64_t(1) << 40)) return fuse::fail(FUSE_E_SHAPE, "n outside 0..2^40");
+  int64_t b = 1;
+  while (b < n) b <<= 1;
+  *bucket = b;
+  return FUSE_OK;
 }
 
 int fuse_num_inputs(fuse_handle h, int* n_in, fuse_dtype* out_dtype) {
@@ -502,7 +567,14 @@ int fuse_input_dtypes(fuse_handle h, fuse_dtype* dts, int cap) {
 
 int fuse_launch(fuse_handle h, const void* const* inputs, int n_in, void* output, void* stream) {
   if (!h) return fuse::fail(FUSE_E_ARG, "NULL handle");
-  return fuse::chain_launch(h, inputs, n_in, output, stream);
+  return fuse::chain_launch(h, inputs, n_in, output, stream, -1);
+}
+
+int fuse_launch_rows(fuse_handle h, const void* const* inputs, int n_in, void* output,
+                     int64_t rows, void* stream) {
+  if (!h) return fuse::fail(FUSE_E_ARG, "NULL handle");
+  if (rows < 0) return fuse::fail(FUSE_E_SHAPE, "rows < 0");
+  return fuse::chain_launch(h, inputs, n_in, output, stream, rows);
 }
 
 int fuse_release(fuse_handle h) {
@@ -513,14 +585,15 @@ int fuse_release(fuse_handle h) {
 int fuse_source(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dtype, char* buf,
                 size_t cap, size_t* len) {
   std::string src;
-  if (int rc = fuse::chain_source(spec, shape, ndim, in_dtype, &src)) return rc;
-  if (len) *len = src.size();
-  if (buf && cap) {
-    size_t n = std::min(cap - 1, src.size());
-    memcpy(buf, src.data(), n);
-    buf[n] = '\0';
-  }
-  return FUSE_OK;
+  if (int rc = fuse::chain_source(spec, shape, ndim, in_dtype, &src, false)) return rc;
+  return copy_source(src, buf, cap, len);
+}
+
+int fuse_source_bucket(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dtype,
+                       char* buf, size_t cap, size_t* len) {
+  std::string src;
+  if (int rc = fuse::chain_source(spec, shape, ndim, in_dtype, &src, true)) return rc;
+  return copy_source(src, buf, cap, len);
 }
 
 }  // extern "C"

@@ -105,6 +105,25 @@ int fuse_release(fuse_handle h);
 int fuse_source(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dtype, char* buf,
                 size_t cap, size_t* len);
 
+/* Shape buckets ("DeepJIT", section 7.2: quantise dynamic shapes into a few
+ * buckets so that the number of compiles stays bounded, and handle the
+ * excess with a mask or a tail).  fuse_compile_bucket compiles a chain whose
+ * leading dimension is only an upper bound: everything else (dims 1..ndim-1,
+ * vector width, block size) is baked in, and the element count is a kernel
+ * argument, so one compile serves every leading dimension up to shape[0]
+ * with no padding.  fuse_launch_rows runs it on a tensor whose leading
+ * dimension is rows (0 <= rows <= shape[0]; other tensors are read and
+ * written only up to that size).  A handle from fuse_compile accepts only its
+ * own shape[0] there.  fuse_bucket gives the smallest power of two >= n
+ * (>= 1), a bucket size for callers that key compiled handles by bucket. */
+int fuse_compile_bucket(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dtype,
+                        fuse_handle* out);
+int fuse_launch_rows(fuse_handle h, const void* const* inputs, int n_in, void* output,
+                     int64_t rows, void* stream);
+int fuse_source_bucket(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dtype,
+                       char* buf, size_t cap, size_t* len);
+int fuse_bucket(int64_t n, int64_t* bucket);
+
 /* ------------------------------------------------------------------------
  * Residual add + RMSNorm + cast ("TeleTron", sections 3.3 and 4.2).
  * Per row r of [rows, hidden]:

@@ -141,6 +141,30 @@ def test_flat_chain_full_sizes_sampled(n, length):
     _check(spec, dt, ins, (len(idx),), got)
 
 
+# ------------------------------------------------------------ shape buckets
+
+@pytest.mark.parametrize("spec,dt,shape,rows_list", [
+    ("add;relu;scale:0.5", F.F32, ((1 << 16) + 123,), [1, 7, 1000, 4097, (1 << 16) + 123]),
+    ("mul;sigmoid;cast:f16;add", F.F32, (300, 37), [1, 2, 299, 300]),
+    ("shuffle:4;add;sigmoid", F.F16, (8, 16, 7, 7), [1, 3, 8]),
+    ("shuffle:2;exp;scale:0.25", F.F16, (6, 8, 4, 4), [1, 5, 6]),
+])
+def test_bucket_handle_runs_any_leading_dimension(spec, dt, shape, rows_list):
+    c = F.fuse_compile_bucket(spec, shape, dt)
+    inner = int(np.prod(shape[1:]))
+    full = int(np.prod(shape))
+    inputs, _ = workloads.chain_inputs(spec, dt, full, 31)
+    dev = [to_dev(a, d) for a, d in zip(inputs, c.in_dtypes)]
+    for rows in rows_list:
+        n = rows * inner
+        out = Guarded(n, c.out_dtype)
+        F.fuse_launch_rows(c, dev, out.t, rows)
+        torch.cuda.synchronize()
+        assert out.canary_ok()
+        sub = (rows,) + tuple(shape[1:])
+        _check(spec, dt, [a[:n] for a in inputs], sub, to_host(out.t, c.out_dtype))
+
+
 # ------------------------------------------------------------ ChannelShuffle prologue
 
 @pytest.mark.parametrize("shape,groups", [

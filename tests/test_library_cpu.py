@@ -85,6 +85,27 @@ def test_source_bakes_sizes_vector_and_tail():
     assert "G = 4" in shf and "src_vec" in shf and "HW = 3136" in shf
 
 
+def test_bucket_helper_and_source():
+    assert [F.fuse_bucket(n) for n in (0, 1, 2, 3, 5, 1000, 1024, 1025)] == \
+        [1, 1, 2, 4, 8, 1024, 1024, 2048]
+    src = F.fuse_source_bucket("shuffle:4;add;sigmoid", [8, 16, 7, 7], F.F16)
+    assert "long long n; };" in src and "#define SIZE_N(a) ((a).n)" in src
+    fixed = F.fuse_source("shuffle:4;add;sigmoid", [8, 16, 7, 7], F.F16)
+    assert "#define SIZE_N(a) N" in fixed
+
+
+def test_launch_rows_checks_the_leading_dimension():
+    fixed = F.fuse_compile("add;relu", [64, 3], F.F32)
+    with pytest.raises(F.FuseError) as e:
+        F.fuse_launch_rows(fixed, [256, 256], 256, 32, stream=0)
+    assert e.value.code == -2  # a fixed handle runs only its own leading dimension
+    bucket = F.fuse_compile_bucket("add;relu", [64, 3], F.F32)
+    with pytest.raises(F.FuseError) as e:
+        F.fuse_launch_rows(bucket, [256, 256], 256, 65, stream=0)
+    assert e.value.code == -2  # above the bucket
+    F.fuse_launch_rows(bucket, [0, 0], 0, 0, stream=0)  # nothing to do
+
+
 def test_source_of_copy_and_odd_shuffle():
     # no ops: a bit copy; a plane size that is not a vector multiple: scalar only
     src = F.fuse_source("shuffle:2", [1, 4, 3, 3], F.F16)
