@@ -72,6 +72,8 @@ def lib():
         L.oracle_rmsnorm_residual.argtypes = [P, P, P, I, I64, I64, ctypes.c_float, P, P]
         L.oracle_rope_qkv_split.argtypes = [P, I, I64, I, I, P, D, P, P, P, P, P]
         L.oracle_layernorm_residual.argtypes = [P, P, P, P, I, I64, I64, ctypes.c_float, P, P, P]
+        L.oracle_rmsnorm_linear.argtypes = [P, P, P, P, I, I64, I64, P, I64, ctypes.c_float,
+                                            ctypes.c_float, P, P]
         L.oracle_detect_decode.argtypes = [P, I, P, P, P, I, I, I, P, P]
         _lib = L
     return _lib
@@ -238,6 +240,22 @@ def rmsnorm_residual(x, res, w, dt: int, eps: float):
     lib().oracle_rmsnorm_residual(_p(x), _p(res), _p(w), dt, rows, hidden, ctypes.c_float(eps),
                                   _p(y), _p(r))
     return y, r
+
+
+def rmsnorm_linear(x, gamma, w, bias, dt: int, eps: float, scale: float, rows=None):
+    """scale * (RMSNorm(x) * gamma @ w.T + bias) for the given rows of x
+    [M, K] (all rows if None); w is [N, K]; bias may be None.  Returns
+    (out, term magnitudes), both [len(rows), N] in binary64."""
+    x, gamma, w = (np.ascontiguousarray(a) for a in (x, gamma, w))
+    bias = None if bias is None else np.ascontiguousarray(bias)
+    M, K = x.shape
+    N = w.shape[0]
+    rows = np.arange(M, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    out = np.empty((len(rows), N), np.float64)
+    mag = np.empty((len(rows), N), np.float64)
+    lib().oracle_rmsnorm_linear(_p(x), _p(gamma), _p(w), _p(bias), dt, K, N, _p(rows), len(rows),
+                                ctypes.c_float(eps), ctypes.c_float(scale), _p(out), _p(mag))
+    return out, mag
 
 
 def layernorm_residual(x, res, gamma, beta, dt: int, eps: float):

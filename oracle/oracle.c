@@ -496,6 +496,44 @@ void oracle_rmsnorm_residual(const void* x, const void* res, const void* w, int 
 }
 
 /* ------------------------------------------------------------------ */
+/* RMSNorm feeding a Linear layer, then an elementwise scale             */
+/* ------------------------------------------------------------------ */
+
+/* "TeleTron" section 4.2 (RMSNorm + Linear + scale): per row m of x [M, K]
+ *   s_m = 1 / sqrt(sum_k x[m,k]^2 / K + eps)          (the RMSNorm factor)
+ *   out[m, n] = scale * (sum_k x[m,k] * s_m * gamma[k] * w[n,k] + bias[n])
+ * with w in [N, K] (the transposed layout the page recommends for the
+ * weight).  Reading: the statistics are taken on x, as RMSNorm defines them
+ * (the page's pseudo-code squares x * gamma).  rows: the row indices to
+ * evaluate (nrows of them); out and mag are [nrows, N]; mag gets
+ * |scale| * (s_m * sum_k |x gamma w| + |bias|), the scale of the terms. */
+void oracle_rmsnorm_linear(const void* x, const void* gamma, const void* w, const void* bias,
+                           int dt, int64_t K, int64_t N, const int64_t* rows, int64_t nrows,
+                           float eps, float scale, double* out, double* mag) {
+  for (int64_t i = 0; i < nrows; ++i) {
+    int64_t m = rows[i];
+    double ss = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      double v = load_elem(x, dt, m * K + k);
+      ss += v * v;
+    }
+    double s = 1.0 / sqrt(ss / (double)K + (double)eps);
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0, absacc = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        double t = load_elem(x, dt, m * K + k) * s * load_elem(gamma, dt, k) *
+                   load_elem(w, dt, n * K + k);
+        acc += t;
+        absacc += fabs(t);
+      }
+      double b = bias ? load_elem(bias, dt, n) : 0.0;
+      out[i * N + n] = (double)scale * (acc + b);
+      if (mag) mag[i * N + n] = fabs((double)scale) * (absacc + fabs(b));
+    }
+  }
+}
+
+/* ------------------------------------------------------------------ */
 /* Residual add + LayerNorm                                             */
 /* ------------------------------------------------------------------ */
 
