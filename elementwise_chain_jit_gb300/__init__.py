@@ -27,7 +27,7 @@ STATUS = {0: "FUSE_OK", -1: "FUSE_E_SPEC", -2: "FUSE_E_SHAPE", -3: "FUSE_E_DTYPE
 # every symbol include/fuse.h declares
 EXPORTS = ["fuse_compile", "fuse_num_inputs", "fuse_input_dtypes", "fuse_launch", "fuse_release",
            "fuse_source", "fuse_compile_bucket", "fuse_launch_rows", "fuse_source_bucket",
-           "fuse_bucket", "rmsnorm_residual", "layernorm_residual", "rope_qkv_split", "rope_qkv_split_noalloc",
+           "fuse_bucket", "rmsnorm_linear", "fuse_device_error", "rmsnorm_residual", "layernorm_residual", "rope_qkv_split", "rope_qkv_split_noalloc",
            "detect_decode", "channel_shuffle", "fuse_graph_begin", "fuse_graph_end",
            "fuse_graph_launch", "fuse_graph_nodes", "fuse_graph_release", "fuse_last_error",
            "fuse_stats", "fuse_device_sms"]
@@ -59,6 +59,8 @@ _lib.fuse_source_bucket.argtypes = [ctypes.c_char_p, ctypes.POINTER(_I64), _I, _
                                     ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
 _lib.fuse_bucket.argtypes = [_I64, ctypes.POINTER(_I64)]
 _lib.rmsnorm_residual.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P]
+_lib.rmsnorm_linear.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, _I, _P]
+_lib.fuse_device_error.argtypes = [ctypes.POINTER(_I)]
 _lib.layernorm_residual.argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P]
 _lib.rope_qkv_split.argtypes = [_P, _P, _P, _P, _I64, _I, _I, _I64, _F, _I, _P]
 _lib.rope_qkv_split_noalloc.argtypes = [_P, _P, _P, _P, _I64, _I, _I, _I64, _F, _I, _P]
@@ -200,6 +202,26 @@ def rmsnorm_residual(x, residual, weight, out, residual_out, eps: float = 1e-6, 
     _check(_lib.rmsnorm_residual(_ptr(x), _ptr(residual), _ptr(weight), _ptr(out),
                                  _ptr(residual_out), rows, hidden, eps, _dtype(dt),
                                  _stream(stream)))
+
+
+def rmsnorm_linear(x, gamma, w, bias, out, eps: float = 1e-6, scale: float = 1.0, dt=None,
+                   M: int | None = None, N: int | None = None, K: int | None = None,
+                   stream=None) -> None:
+    """out = scale * (RMSNorm(x) * gamma @ w.T + bias) on the tensor cores;
+    x [M, K], w [N, K], bias may be None."""
+    if M is None:
+        M, K = x.shape
+        N = w.shape[0]
+    if dt is None:
+        dt = x.dtype
+    _check(_lib.rmsnorm_linear(_ptr(x), _ptr(gamma), _ptr(w), _ptr(bias), _ptr(out), M, N, K, eps,
+                               scale, _dtype(dt), _stream(stream)))
+
+
+def fuse_device_error() -> int:
+    c = _I()
+    _check(_lib.fuse_device_error(ctypes.byref(c)))
+    return c.value
 
 
 def layernorm_residual(x, residual, gamma, beta, out, residual_out, eps: float = 1e-5, dt=None,

@@ -61,6 +61,10 @@ struct DriverApi {
   decltype(&::cuGraphExecDestroy) GraphExecDestroy;
   decltype(&::cuGraphDestroy) GraphDestroy;
   decltype(&::cuGraphGetNodes) GraphGetNodes;
+  decltype(&::cuTensorMapEncodeTiled) TensorMapEncodeTiled;
+  decltype(&::cuCtxSynchronize) CtxSynchronize;
+  decltype(&::cuMemcpyDtoH) MemcpyDtoH;
+  decltype(&::cuMemsetD32) MemsetD32;
 };
 
 // Returns FUSE_OK and the API table, or FUSE_E_CUDA (driver missing).

@@ -1,0 +1,146 @@
+// rms_linear.cpp -- RMSNorm -> Linear -> scale entry point (tcgen05).
+//
+// "TeleTron" section 4.2 ("RMSNorm + Linear + scale" fused): the RMSNorm
+// factor of each row is computed inside the GEMM's tile loop and applied in
+// the epilogue, gamma is applied to the A operand in shared memory, and the
+// contraction runs on the tensor cores (tcgen05.mma with a TMEM accumulator,
+// operands staged by TMA).  The kernel is generated per (K, N, dtype, bias)
+// and compiled by NVRTC for sm_103a like every other kernel of the library.
+#include <algorithm>
+#include <cmath>
+#include <map>
+#include <tuple>
+
+#include "internal.h"
+
+namespace fuse {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kBM = 128, kBN = 256, kBK = 64;
+
+struct RlKernel {
+  std::shared_ptr<Module> mod;
+  int smem = 0;
+};
+
+std::mutex g_mu;
+std::map<std::tuple<int64_t, int64_t, int, int>, RlKernel> g_kernels;
+CUdeviceptr g_err[64];  // per-device error word of the kernels' bounded waits
+
+int rl_kernel(int64_t K, int64_t N, fuse_dtype dt, bool has_bias, RlKernel* out) {
+  auto key = std::make_tuple(K, N, static_cast<int>(dt), has_bias ? 1 : 0);
+  if (auto it = g_kernels.find(key); it != g_kernels.end()) {
+    stat_hit();
+    *out = it->second;
+    return FUSE_OK;
+  }
+  RlKernel k;
+  k.smem = 1024 + kStages * (kBM + kBN) * kBK * 2 + 8 * (3 * kStages + 1) + 16;
+  std::string src = fmt(
+      "// RMSNorm -> Linear -> scale, K %lld, N %lld, %s, tcgen05\n"
+      "constexpr int DT = %d;\nconstexpr long long KDIM = %lldLL;\nconstexpr long long NDIM = %lldLL;\n"
+      "constexpr int STAGES = %d;\nconstexpr bool HAS_BIAS = %s;\n#include \"fuse/rms_linear.cuh\"\n",
+      (long long)K, (long long)N, dtype_name(dt), static_cast<int>(dt), (long long)K, (long long)N,
+      kStages, has_bias ? "true" : "false");
+  if (int rc = jit_compile(src, "rmsnorm_linear", &k.mod)) return rc;
+  g_kernels.emplace(key, k);
+  *out = k;
+  return FUSE_OK;
+}
+
+int encode_kmajor(const DriverApi* api, CUtensorMap* map, const void* ptr, fuse_dtype dt,
+                  int64_t rows, int64_t K, uint32_t box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  cuuint32_t elem[2] = {1, 1};
+  CUresult r = api->TensorMapEncodeTiled(
+      map, dt == FUSE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+      const_cast<void*>(ptr), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuTensorMapEncodeTiled");
+  return FUSE_OK;
+}
+
+int error_word(const DriverApi* api, int device, CUdeviceptr* out) {
+  if (!g_err[device]) {
+    CUdeviceptr p;
+    CUresult r = api->MemAlloc(&p, 16);
+    if (r != CUDA_SUCCESS) return cuda_fail(r, "cuMemAlloc(error word)");
+    if ((r = api->MemsetD32(p, 0, 4)) != CUDA_SUCCESS) return cuda_fail(r, "cuMemsetD32");
+    g_err[device] = p;
+  }
+  *out = g_err[device];
+  return FUSE_OK;
+}
+
+}  // namespace
+}  // namespace fuse
+
+extern "C" int rmsnorm_linear(const void* x, const void* gamma, const void* w, const void* bias,
+                              void* out, int64_t M, int64_t N, int64_t K, float eps, float scale,
+                              fuse_dtype dt, void* stream) {
+  using namespace fuse;
+  if (dt != FUSE_F16 && dt != FUSE_BF16)
+    return fail(FUSE_E_DTYPE, "rmsnorm_linear runs on the tensor cores: f16 or bf16 only");
+  if (M < 0 || N < 0 || K < 0) return fail(FUSE_E_SHAPE, "negative size");
+  if (M % kBM || N % kBN || K % kBK || K == 0)
+    return fail(FUSE_E_SHAPE, fmt("need M %% %d == 0, N %% %d == 0, K %% %d == 0 and K > 0 "
+                                  "(got M %lld, N %lld, K %lld)",
+                                  kBM, kBN, kBK, (long long)M, (long long)N, (long long)K));
+  if (M / kBM > 65535 || K > (int64_t(1) << 20)) return fail(FUSE_E_SHAPE, "M or K too large");
+  if (!(eps >= 0.f) || !std::isfinite(scale)) return fail(FUSE_E_ARG, "bad eps or scale");
+  if (M == 0 || N == 0) return FUSE_OK;
+  if (!x || !gamma || !w || !out) return fail(FUSE_E_NULL, "NULL tensor pointer");
+  for (const void* p : {x, gamma, w, bias, static_cast<const void*>(out)})
+    if (reinterpret_cast<uintptr_t>(p) % 16)
+      return fail(FUSE_E_ARG, "rmsnorm_linear needs 16-byte aligned tensors (TMA)");
+  RlKernel k;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (int rc = rl_kernel(K, N, dt, bias != nullptr, &k)) return rc;
+  }
+  DeviceInfo d;
+  if (int rc = current_device(&d)) return rc;
+  const DriverApi* api;
+  if (int rc = driver(&api)) return rc;
+  CUfunction fn;
+  if (int rc = jit_function(*k.mod, "rms_linear_kernel", d, &fn)) return rc;
+  CUdeviceptr err;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (int rc = error_word(api, d.ordinal, &err)) return rc;
+  }
+  CUresult r = api->FuncSetAttribute(fn, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, k.smem);
+  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuFuncSetAttribute(shared memory)");
+  alignas(64) CUtensorMap mx, mw;
+  if (int rc = encode_kmajor(api, &mx, x, dt, M, K, kBM)) return rc;
+  if (int rc = encode_kmajor(api, &mw, w, dt, N, K, kBN)) return rc;
+  void* args[] = {&mx, &mw, &gamma, &bias, &out, &eps, &scale, &err};
+  r = api->LaunchKernel(fn, static_cast<unsigned>(N / kBN), static_cast<unsigned>(M / kBM), 1, 192,
+                        1, 1, k.smem, reinterpret_cast<CUstream>(stream), args, nullptr);
+  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuLaunchKernel(rmsnorm_linear)");
+  stat_launch();
+  return FUSE_OK;
+}
+
+extern "C" int fuse_device_error(int* code) {
+  using namespace fuse;
+  if (!code) return fail(FUSE_E_NULL, "code is NULL");
+  *code = 0;
+  DeviceInfo d;
+  if (int rc = current_device(&d)) return rc;
+  const DriverApi* api;
+  if (int rc = driver(&api)) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err[d.ordinal]) return FUSE_OK;
+  CUresult r = api->CtxSynchronize();
+  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuCtxSynchronize");
+  if ((r = api->MemcpyDtoH(code, g_err[d.ordinal], 4)) != CUDA_SUCCESS)
+    return cuda_fail(r, "cuMemcpyDtoH(error word)");
+  if ((r = api->MemsetD32(g_err[d.ordinal], 0, 4)) != CUDA_SUCCESS)
+    return cuda_fail(r, "cuMemsetD32(error word)");
+  return FUSE_OK;
+}

@@ -141,6 +141,10 @@ void load_driver() {
   FUSE_GET(GraphExecDestroy, "cuGraphExecDestroy");
   FUSE_GET(GraphDestroy, "cuGraphDestroy");
   FUSE_GET(GraphGetNodes, "cuGraphGetNodes");
+  FUSE_GET(TensorMapEncodeTiled, "cuTensorMapEncodeTiled");
+  FUSE_GET(CtxSynchronize, "cuCtxSynchronize");
+  FUSE_GET(MemcpyDtoH, "cuMemcpyDtoH");
+  FUSE_GET(MemsetD32, "cuMemsetD32");
 #undef FUSE_GET
   if (!ok) return;
   CUresult r = g_api.Init(0);

@@ -141,6 +141,27 @@ int rmsnorm_residual(const void* x, const void* residual, const void* weight, vo
                      void* stream);
 
 /* ------------------------------------------------------------------------
+ * RMSNorm -> Linear -> scale on the tensor cores ("TeleTron", section 4.2:
+ * the RMSNorm factor computed in the block and used directly in the linear
+ * layer's accumulation, followed by an elementwise scale):
+ *   s_m = 1 / sqrt(sum_k x[m,k]^2 / K + eps)
+ *   out[m, n] = scale * (s_m * sum_k (x[m,k] * gamma[k]) * w[n,k] + bias[n])
+ * x [M, K], gamma [K], w [N, K] (K-major, the layout of a Linear weight),
+ * bias [N] (may be NULL), out [M, N]; dt f16 or bf16 (x * gamma is rounded
+ * to dt before the product, accumulation is fp32).  M % 128 == 0,
+ * N % 256 == 0, K % 64 == 0, all tensors 16-byte aligned.  Every wait inside
+ * the kernel is bounded: a wait that runs out records an error that
+ * fuse_device_error() reports instead of hanging the device.
+ */
+int rmsnorm_linear(const void* x, const void* gamma, const void* w, const void* bias, void* out,
+                   int64_t M, int64_t N, int64_t K, float eps, float scale, fuse_dtype dt,
+                   void* stream);
+
+/* Synchronise the current device and return (and clear) the error word of
+ * the kernels with bounded waits: 0, or nonzero if a wait ran out. */
+int fuse_device_error(int* code);
+
+/* ------------------------------------------------------------------------
  * Residual add + LayerNorm + cast ("DeepJIT", section 4.3: one block per
  * row, mean and variance reduced in the block, then normalised in the same
  * pass over the data).  Per row r of [rows, hidden]:

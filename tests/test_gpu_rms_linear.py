@@ -1,0 +1,62 @@
+"""GPU parity of rmsnorm_linear (RMSNorm -> Linear -> scale on tcgen05) against
+the oracle, through the C ABI.  Tolerance: 8e-3 (bf16) or 2e-3 (f16) relative
+to the sum of the magnitudes of the dot product's terms (the product x*gamma
+is rounded to the operand dtype, accumulation is fp32, the output is rounded
+once).  Each case also checks that no bounded wait inside the kernel ran out."""
+import numpy as np
+import pytest
+import torch
+
+import elementwise_chain_jit_gb300 as F
+import oracle
+import workloads
+from gpu_util import Guarded, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(M, N, K, dt, seed, bias=True, scale=0.75, rows=None):
+    x = workloads.normal((M, K), 0, 1, seed, dt)
+    g = workloads.normal(K, 1, 0.1, seed + 1, dt)
+    w = workloads.normal((N, K), 0, 1 / np.sqrt(K), seed + 2, dt)
+    b = workloads.normal(N, 0, 0.5, seed + 3, dt) if bias else None
+    out = Guarded(M * N, dt)
+    F.rmsnorm_linear(to_dev(x.reshape(-1), dt), to_dev(g, dt), to_dev(w.reshape(-1), dt),
+                     None if b is None else to_dev(b, dt), out.t, 1e-6, scale, dt, M=M, N=N, K=K)
+    torch.cuda.synchronize()
+    assert F.fuse_device_error() == 0
+    assert out.canary_ok()
+    sel = np.arange(M) if rows is None else np.asarray(rows)
+    want, mag = oracle.rmsnorm_linear(x, g, w, b, dt, 1e-6, scale, rows=sel)
+    got = oracle.to_double(to_host(out.t, dt), dt).reshape(M, N)[sel]
+    rel = 8e-3 if dt == F.BF16 else 2e-3
+    bad = np.abs(got - want) > rel * mag
+    assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], want[bad][:5])
+
+
+def test_tiny_one_tile_one_k_step():
+    _case(128, 256, 64, F.BF16, 1)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 512), (256, 512, 256), (384, 768, 1024)])
+@pytest.mark.parametrize("dt", [F.BF16, F.F16])
+def test_small_shapes(M, N, K, dt):
+    _case(M, N, K, dt, 10 + K % 97)
+
+
+def test_no_bias_and_negative_scale():
+    _case(256, 256, 320, F.BF16, 20, bias=False, scale=-1.5)
+
+
+def test_full_size_sampled_rows():
+    M, N, K = 16384, 4096, 4096
+    _case(M, N, K, F.BF16, 30, rows=[0, 1, 127, 128, 5000, 16383])
+
+
+def test_rejects_unsupported_shapes_and_dtypes():
+    with pytest.raises(F.FuseError) as e:
+        F.rmsnorm_linear(256, 256, 256, 256, 256, 1e-6, 1.0, F.BF16, M=100, N=256, K=64)
+    assert e.value.code == -2
+    with pytest.raises(F.FuseError) as e:
+        F.rmsnorm_linear(256, 256, 256, 256, 256, 1e-6, 1.0, F.F32, M=128, N=256, K=64)
+    assert e.value.code == -3
