@@ -69,6 +69,16 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def tensor_peak():
+    """Dense bf16 tensor peak (TFLOP/s) for a kernel timed alone: the measured
+    cuBLAS burst figure, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (cuBLAS burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples during the timed region."""
 
@@ -251,6 +261,36 @@ def _ln_item(dev, with_unfused):
             var = (d * d).mean(-1, keepdim=True)
             return (d * torch.rsqrt(var + eps) * g.float() + b.float()).to(torch.bfloat16), h
         it.unfused, it.n_unfused = ln_unfused, 12
+    return it
+
+
+def _rms_linear_item(dev, with_unfused):
+    """RMSNorm -> Linear -> scale on the tensor cores (a next row, measured
+    beside the step); unfused: the PyTorch RMSNorm ops, then F.linear
+    (cuBLAS), then the scale."""
+    import torch
+
+    import elementwise_chain_jit_gb300 as F
+    import workloads as W
+    M, N, K, eps, scale = 16384, 4096, 4096, 1e-6, 0.5
+    x = W.device_normal((M, K), 0, 1, 71, W.BF16, dev)
+    g = W.device_normal((K,), 1, 0.1, 72, W.BF16, dev)
+    w = W.device_normal((N, K), 0, K ** -0.5, 73, W.BF16, dev)
+    b = W.device_normal((N,), 0, 0.5, 74, W.BF16, dev)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    wf = torch.empty_like(w)  # gamma folded into the weight once, like loading weights
+    F.rmsnorm_linear_fold(w, g, wf, W.BF16)
+    it = Item(f"rmsnorm_linear_{M}x{N}x{K}_bf16", 2 * (M * K + N * K + M * N),
+              lambda: F.rmsnorm_linear(x, None, wf, b, out, eps, scale, W.BF16),
+              kernel=("rms_linear",))
+    it.flops = 2 * M * N * K
+    it.inputs, it.outputs = [x, g, w, b], [out]
+    if with_unfused:
+        def unfused():
+            xf = x.float()
+            y = (xf * torch.rsqrt(xf.pow(2).mean(-1, keepdim=True) + eps) * g.float()).to(torch.bfloat16)
+            return torch.nn.functional.linear(y, w, b) * scale
+        it.unfused, it.n_unfused = unfused, 9
     return it
 
 
@@ -680,6 +720,19 @@ def run_gpu(args):
                       "speedup": ums / lms})
         next_rows[ln.name] = d
         del ln
+    if args.only is None or re.search(args.only, "rmsnorm_linear"):
+        rl = _rms_linear_item(dev, with_unfused=not args.no_unfused)
+        tf_peak = tensor_peak()
+        rms = time_fn(rl.fused, reps=10, warm=3)
+        d = {"flops": rl.flops, "us_fused": rms * 1e3, "tflops": rl.flops / (rms / 1e3) / 1e12,
+             "frac_of_bf16_peak": rl.flops / (rms / 1e3) / 1e12 / tf_peak[0],
+             "bf16_peak_tflops": tf_peak[0], "peak_source": tf_peak[1]}
+        if rl.unfused is not None:
+            ums = time_fn(rl.unfused, reps=5, warm=2)
+            d.update({"us_unfused": ums * 1e3, "unfused_kernels": rl.n_unfused,
+                      "speedup": ums / rms})
+        next_rows[rl.name] = d
+        del rl
     # dominant kernel and its roofline
     dom = max(range(nitem), key=lambda i: per_item[i])
     dit = items[dom]

@@ -27,7 +27,7 @@ STATUS = {0: "FUSE_OK", -1: "FUSE_E_SPEC", -2: "FUSE_E_SHAPE", -3: "FUSE_E_DTYPE
 # every symbol include/fuse.h declares
 EXPORTS = ["fuse_compile", "fuse_num_inputs", "fuse_input_dtypes", "fuse_launch", "fuse_release",
            "fuse_source", "fuse_compile_bucket", "fuse_launch_rows", "fuse_source_bucket",
-           "fuse_bucket", "rmsnorm_linear", "fuse_device_error", "rmsnorm_residual", "layernorm_residual", "rope_qkv_split", "rope_qkv_split_noalloc",
+           "fuse_bucket", "rmsnorm_linear", "rmsnorm_linear_fold", "fuse_device_error", "rmsnorm_residual", "layernorm_residual", "rope_qkv_split", "rope_qkv_split_noalloc",
            "detect_decode", "channel_shuffle", "fuse_graph_begin", "fuse_graph_end",
            "fuse_graph_launch", "fuse_graph_nodes", "fuse_graph_release", "fuse_last_error",
            "fuse_stats", "fuse_device_sms"]
@@ -61,6 +61,7 @@ _lib.fuse_bucket.argtypes = [_I64, ctypes.POINTER(_I64)]
 _lib.rmsnorm_residual.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P]
 _lib.rmsnorm_linear.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, _I, _P]
 _lib.fuse_device_error.argtypes = [ctypes.POINTER(_I)]
+_lib.rmsnorm_linear_fold.argtypes = [_P, _P, _P, _I64, _I64, _I, _P]
 _lib.layernorm_residual.argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P]
 _lib.rope_qkv_split.argtypes = [_P, _P, _P, _P, _I64, _I, _I, _I64, _F, _I, _P]
 _lib.rope_qkv_split_noalloc.argtypes = [_P, _P, _P, _P, _I64, _I, _I, _I64, _F, _I, _P]
@@ -216,6 +217,18 @@ def rmsnorm_linear(x, gamma, w, bias, out, eps: float = 1e-6, scale: float = 1.0
         dt = x.dtype
     _check(_lib.rmsnorm_linear(_ptr(x), _ptr(gamma), _ptr(w), _ptr(bias), _ptr(out), M, N, K, eps,
                                scale, _dtype(dt), _stream(stream)))
+
+
+def rmsnorm_linear_fold(w, gamma, w_out, dt=None, N: int | None = None, K: int | None = None,
+                        stream=None) -> None:
+    """w_out = w * gamma (per column k): gamma folded into the weight for the
+    fast path of rmsnorm_linear (call it with gamma=None)."""
+    if N is None:
+        N, K = w.shape
+    if dt is None:
+        dt = w.dtype
+    _check(_lib.rmsnorm_linear_fold(_ptr(w), _ptr(gamma), _ptr(w_out), N, K, _dtype(dt),
+                                    _stream(stream)))
 
 
 def fuse_device_error() -> int:

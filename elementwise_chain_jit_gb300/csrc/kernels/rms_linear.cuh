@@ -25,9 +25,20 @@
 // frees its TMEM) instead of hanging.
 //
 // The generated source defines: DT (1 f16, 2 bf16), KDIM, NDIM, STAGES,
-// HAS_BIAS.
+// HAS_BIAS, APPLY_GAMMA.  With APPLY_GAMMA false, gamma has already been
+// folded into w (rms_linear_fold below): the row warps only read the x tile
+// for the sum of squares, and the MMA consumes the TMA tiles as they land.
 #pragma once
 #include "fuse/common.cuh"
+
+// w'[n, k] = dt(w[n, k] * gamma[k]): gamma folded into the weight once, so
+// that the tile loop needs no transform of the A operand.
+extern "C" __global__ void rms_linear_fold(const u16* __restrict__ w, const u16* __restrict__ gamma,
+                                           u16* __restrict__ wout, long long total) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x)
+    store_elem<DT>(wout, i, load_elem<DT>(w, i) * load_elem<DT>(gamma, i % KDIM));
+}
 
 constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
@@ -172,7 +183,10 @@ rms_linear_kernel(const __grid_constant__ TensorMap tmap_x, const __grid_constan
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full(s), 1);
       mbar_init(ready(s), 128);
-      mbar_init(empty(s), 1);
+      // with gamma applied in place the MMA's commit frees a stage (the row
+      // warps finished before "ready"); with gamma folded into w the four
+      // row warps, which only read the stage, arrive as well
+      mbar_init(empty(s), APPLY_GAMMA ? 1 : 5);
     }
     mbar_init(accum, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -204,7 +218,7 @@ rms_linear_kernel(const __grid_constant__ TensorMap tmap_x, const __grid_constan
     if (lane == 0) {
       for (int kt = 0; kt < KT; ++kt) {
         const int s = kt % STAGES;
-        if (!mbar_wait(ready(s), (kt / STAGES) & 1)) { ok = false; break; }
+        if (!mbar_wait(APPLY_GAMMA ? ready(s) : full(s), (kt / STAGES) & 1)) { ok = false; break; }
         tc_fence_after();
         const unsigned long long a = sw128_desc(stage_a(s)), b = sw128_desc(stage_b(s));
 #pragma unroll
@@ -221,27 +235,45 @@ rms_linear_kernel(const __grid_constant__ TensorMap tmap_x, const __grid_constan
     for (int kt = 0; kt < KT; ++kt) {
       const int s = kt % STAGES;
       if (!mbar_wait(full(s), (kt / STAGES) & 1)) { ok = false; break; }
-      // the row's 128 bytes hold its 64 values in 16-byte chunks, chunk c at
-      // position c ^ (r % 8) (the 128-byte swizzle)
+      // the row's 128 bytes hold its 64 values in 16-byte chunks, logical
+      // chunk c at position c ^ (r % 8) (the 128-byte swizzle); step p visits
+      // logical chunk p, so the 8 rows of a swizzle group hit 8 different
+      // bank groups
       uint4* row = reinterpret_cast<uint4*>(base_ptr + (stage_a(s) - base) + r * 128);
+      if constexpr (APPLY_GAMMA) {
 #pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        const int c = p ^ (r & 7);
-        const uint4 g4 = __ldg(reinterpret_cast<const uint4*>(gamma + kt * BK + c * 8));
-        uint4 v4 = row[p];
-        u32 wv[4] = {v4.x, v4.y, v4.z, v4.w}, gw[4] = {g4.x, g4.y, g4.z, g4.w};
-        float y[8];
+        for (int p = 0; p < 8; ++p) {
+          const uint4 g4 = __ldg(reinterpret_cast<const uint4*>(gamma + kt * BK + p * 8));
+          uint4& slot = row[p ^ (r & 7)];
+          uint4 v4 = slot;
+          u32 wv[4] = {v4.x, v4.y, v4.z, v4.w}, gw[4] = {g4.x, g4.y, g4.z, g4.w};
+          float y[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float xv = get_elem<DT>(wv, e);
-          ss += xv * xv;
-          y[e] = xv * get_elem<DT>(gw, e);
+          for (int e = 0; e < 8; ++e) {
+            const float xv = get_elem<DT>(wv, e);
+            ss += xv * xv;
+            y[e] = xv * get_elem<DT>(gw, e);
+          }
+          pack_vec<DT>(y, wv);
+          slot = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
-        pack_vec<DT>(y, wv);
-        row[p] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(ready(s));
+      } else {
+        // gamma is folded into w: only the sum of squares, read-only
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          const uint4 v4 = row[p ^ (r & 7)];
+          const u32 wv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float xv = get_elem<DT>(wv, e);
+            ss += xv * xv;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(s));
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(ready(s));
     }
     const float rs = 1.0f / sqrtf(ss / KDIM + eps);
     if (!mbar_wait(accum, 0)) ok = false;

@@ -25,11 +25,11 @@ struct RlKernel {
 };
 
 std::mutex g_mu;
-std::map<std::tuple<int64_t, int64_t, int, int>, RlKernel> g_kernels;
+std::map<std::tuple<int64_t, int64_t, int, int, int>, RlKernel> g_kernels;
 CUdeviceptr g_err[64];  // per-device error word of the kernels' bounded waits
 
-int rl_kernel(int64_t K, int64_t N, fuse_dtype dt, bool has_bias, RlKernel* out) {
-  auto key = std::make_tuple(K, N, static_cast<int>(dt), has_bias ? 1 : 0);
+int rl_kernel(int64_t K, int64_t N, fuse_dtype dt, bool has_bias, bool apply_gamma, RlKernel* out) {
+  auto key = std::make_tuple(K, N, static_cast<int>(dt), has_bias ? 1 : 0, apply_gamma ? 1 : 0);
   if (auto it = g_kernels.find(key); it != g_kernels.end()) {
     stat_hit();
     *out = it->second;
@@ -40,9 +40,10 @@ int rl_kernel(int64_t K, int64_t N, fuse_dtype dt, bool has_bias, RlKernel* out)
   std::string src = fmt(
       "// RMSNorm -> Linear -> scale, K %lld, N %lld, %s, tcgen05\n"
       "constexpr int DT = %d;\nconstexpr long long KDIM = %lldLL;\nconstexpr long long NDIM = %lldLL;\n"
-      "constexpr int STAGES = %d;\nconstexpr bool HAS_BIAS = %s;\n#include \"fuse/rms_linear.cuh\"\n",
+      "constexpr int STAGES = %d;\nconstexpr bool HAS_BIAS = %s, APPLY_GAMMA = %s;\n"
+      "#include \"fuse/rms_linear.cuh\"\n",
       (long long)K, (long long)N, dtype_name(dt), static_cast<int>(dt), (long long)K, (long long)N,
-      kStages, has_bias ? "true" : "false");
+      kStages, has_bias ? "true" : "false", apply_gamma ? "true" : "false");
   if (int rc = jit_compile(src, "rmsnorm_linear", &k.mod)) return rc;
   g_kernels.emplace(key, k);
   *out = k;
@@ -93,14 +94,14 @@ extern "C" int rmsnorm_linear(const void* x, const void* gamma, const void* w, c
   if (M / kBM > 65535 || K > (int64_t(1) << 20)) return fail(FUSE_E_SHAPE, "M or K too large");
   if (!(eps >= 0.f) || !std::isfinite(scale)) return fail(FUSE_E_ARG, "bad eps or scale");
   if (M == 0 || N == 0) return FUSE_OK;
-  if (!x || !gamma || !w || !out) return fail(FUSE_E_NULL, "NULL tensor pointer");
+  if (!x || !w || !out) return fail(FUSE_E_NULL, "NULL tensor pointer");
   for (const void* p : {x, gamma, w, bias, static_cast<const void*>(out)})
     if (reinterpret_cast<uintptr_t>(p) % 16)
       return fail(FUSE_E_ARG, "rmsnorm_linear needs 16-byte aligned tensors (TMA)");
   RlKernel k;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (int rc = rl_kernel(K, N, dt, bias != nullptr, &k)) return rc;
+    if (int rc = rl_kernel(K, N, dt, bias != nullptr, gamma != nullptr, &k)) return rc;
   }
   DeviceInfo d;
   if (int rc = current_device(&d)) return rc;
@@ -124,6 +125,28 @@ extern "C" int rmsnorm_linear(const void* x, const void* gamma, const void* w, c
   if (r != CUDA_SUCCESS) return cuda_fail(r, "cuLaunchKernel(rmsnorm_linear)");
   stat_launch();
   return FUSE_OK;
+}
+
+extern "C" int rmsnorm_linear_fold(const void* w, const void* gamma, void* w_out, int64_t N,
+                                   int64_t K, fuse_dtype dt, void* stream) {
+  using namespace fuse;
+  if (dt != FUSE_F16 && dt != FUSE_BF16) return fail(FUSE_E_DTYPE, "f16 or bf16 only");
+  if (N < 0 || K < 1 || K > (int64_t(1) << 20)) return fail(FUSE_E_SHAPE, "bad N or K");
+  if (N == 0) return FUSE_OK;
+  if (!w || !gamma || !w_out) return fail(FUSE_E_NULL, "NULL tensor pointer");
+  RlKernel k;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (int rc = rl_kernel(K, kBN, dt, false, false, &k)) return rc;
+  }
+  DeviceInfo d;
+  if (int rc = current_device(&d)) return rc;
+  CUfunction fn;
+  if (int rc = jit_function(*k.mod, "rms_linear_fold", d, &fn)) return rc;
+  long long total = N * K;
+  void* args[] = {&w, &gamma, &w_out, &total};
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(d.sms * 8LL, (total + 255) / 256));
+  return launch(fn, grid, 256, 0, stream, args);
 }
 
 extern "C" int fuse_device_error(int* code) {

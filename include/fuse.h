@@ -147,15 +147,23 @@ int rmsnorm_residual(const void* x, const void* residual, const void* weight, vo
  *   s_m = 1 / sqrt(sum_k x[m,k]^2 / K + eps)
  *   out[m, n] = scale * (s_m * sum_k (x[m,k] * gamma[k]) * w[n,k] + bias[n])
  * x [M, K], gamma [K], w [N, K] (K-major, the layout of a Linear weight),
- * bias [N] (may be NULL), out [M, N]; dt f16 or bf16 (x * gamma is rounded
- * to dt before the product, accumulation is fp32).  M % 128 == 0,
- * N % 256 == 0, K % 64 == 0, all tensors 16-byte aligned.  Every wait inside
- * the kernel is bounded: a wait that runs out records an error that
- * fuse_device_error() reports instead of hanging the device.
+ * bias [N] (may be NULL), out [M, N]; dt f16 or bf16 (accumulation fp32).
+ * M % 128 == 0, N % 256 == 0, K % 64 == 0, all tensors 16-byte aligned.
+ * gamma NULL means gamma is already folded into w (rmsnorm_linear_fold): the
+ * fast path, where the tensor cores consume the tiles as they arrive.  With
+ * gamma given, x * gamma is formed (rounded to dt) on the tiles in shared
+ * memory before each product.  Every wait inside the kernel is bounded: a
+ * wait that runs out records an error that fuse_device_error() reports
+ * instead of hanging the device.
  */
 int rmsnorm_linear(const void* x, const void* gamma, const void* w, const void* bias, void* out,
                    int64_t M, int64_t N, int64_t K, float eps, float scale, fuse_dtype dt,
                    void* stream);
+
+/* w_out[n, k] = dt(w[n, k] * gamma[k]) for w [N, K]: gamma folded into the
+ * weight once, for rmsnorm_linear's fast path (w_out may equal w). */
+int rmsnorm_linear_fold(const void* w, const void* gamma, void* w_out, int64_t N, int64_t K,
+                        fuse_dtype dt, void* stream);
 
 /* Synchronise the current device and return (and clear) the error word of
  * the kernels with bounded waits: 0, or nonzero if a wait ran out. */

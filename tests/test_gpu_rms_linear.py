@@ -60,3 +60,38 @@ def test_rejects_unsupported_shapes_and_dtypes():
     with pytest.raises(F.FuseError) as e:
         F.rmsnorm_linear(256, 256, 256, 256, 256, 1e-6, 1.0, F.F32, M=128, N=256, K=64)
     assert e.value.code == -3
+
+
+def _folded_case(M, N, K, dt, seed, rows=None):
+    x = workloads.normal((M, K), 0, 1, seed, dt)
+    g = workloads.normal(K, 1, 0.1, seed + 1, dt)
+    w = workloads.normal((N, K), 0, 1 / np.sqrt(K), seed + 2, dt)
+    b = workloads.normal(N, 0, 0.5, seed + 3, dt)
+    wd = to_dev(w.reshape(-1), dt)
+    wf = torch.empty_like(wd)
+    F.rmsnorm_linear_fold(wd, to_dev(g, dt), wf, dt, N=N, K=K)
+    out = Guarded(M * N, dt)
+    F.rmsnorm_linear(to_dev(x.reshape(-1), dt), None, wf, to_dev(b, dt), out.t, 1e-6, 0.5, dt,
+                     M=M, N=N, K=K)
+    torch.cuda.synchronize()
+    assert F.fuse_device_error() == 0
+    assert out.canary_ok()
+    # the folded weight is w * gamma rounded once
+    assert np.array_equal(to_host(wf, dt).reshape(N, K),
+                          oracle.store(oracle.to_double(w, dt) * oracle.to_double(g, dt), dt))
+    sel = np.arange(M) if rows is None else np.asarray(rows)
+    want, mag = oracle.rmsnorm_linear(x, g, w, b, dt, 1e-6, 0.5, rows=sel)
+    got = oracle.to_double(to_host(out.t, dt), dt).reshape(M, N)[sel]
+    rel = 8e-3 if dt == F.BF16 else 2e-3
+    bad = np.abs(got - want) > rel * mag
+    assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], want[bad][:5])
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 1024), (384, 256, 448)])
+@pytest.mark.parametrize("dt", [F.BF16, F.F16])
+def test_folded_gamma_fast_path(M, N, K, dt):
+    _folded_case(M, N, K, dt, 40 + K % 89)
+
+
+def test_folded_full_size_sampled_rows():
+    _folded_case(16384, 4096, 4096, F.BF16, 50, rows=[0, 3, 129, 8191, 16383])
