@@ -264,7 +264,7 @@ def _ln_item(dev, with_unfused):
     return it
 
 
-def _rms_linear_item(dev, with_unfused):
+def _rms_linear_item(dev, with_unfused, M=16384):
     """RMSNorm -> Linear -> scale on the tensor cores (a next row, measured
     beside the step); unfused: the PyTorch RMSNorm ops, then F.linear
     (cuBLAS), then the scale."""
@@ -272,7 +272,7 @@ def _rms_linear_item(dev, with_unfused):
 
     import elementwise_chain_jit_gb300 as F
     import workloads as W
-    M, N, K, eps, scale = 16384, 4096, 4096, 1e-6, 0.5
+    N, K, eps, scale = 4096, 4096, 1e-6, 0.5
     x = W.device_normal((M, K), 0, 1, 71, W.BF16, dev)
     g = W.device_normal((K,), 1, 0.1, 72, W.BF16, dev)
     w = W.device_normal((N, K), 0, K ** -0.5, 73, W.BF16, dev)
@@ -721,7 +721,7 @@ def run_gpu(args):
         next_rows[ln.name] = d
         del ln
     if args.only is None or re.search(args.only, "rmsnorm_linear"):
-        rl = _rms_linear_item(dev, with_unfused=not args.no_unfused)
+        rl = _rms_linear_item(dev, with_unfused=not args.no_unfused, M=args.rl_m)
         tf_peak = tensor_peak()
         rms = time_fn(rl.fused, reps=10, warm=3)
         d = {"flops": rl.flops, "us_fused": rms * 1e3, "tflops": rl.flops / (rms / 1e3) / 1e12,
@@ -848,6 +848,7 @@ def main():
     ap.add_argument("--only", default=None, help="regex: run only the matching workloads")
     ap.add_argument("--flat-elems", type=int, default=None, help="size of the flat chains")
     ap.add_argument("--spec", default=None, help="time this one chain (flat) instead")
+    ap.add_argument("--rl-m", type=int, default=16384, help="M of the RMSNorm -> Linear row")
     ap.add_argument("--spec-dtype", default="f32", choices=["f32", "f16", "bf16"])
     args = ap.parse_args()
     if args.warmup < 3:

@@ -65,6 +65,7 @@ struct DriverApi {
   decltype(&::cuCtxSynchronize) CtxSynchronize;
   decltype(&::cuMemcpyDtoH) MemcpyDtoH;
   decltype(&::cuMemsetD32) MemsetD32;
+  decltype(&::cuOccupancyMaxActiveClusters) OccupancyMaxActiveClusters;
 };
 
 // Returns FUSE_OK and the API table, or FUSE_E_CUDA (driver missing).

@@ -1,5 +1,7 @@
 // rms_linear.cuh -- RMSNorm -> Linear -> scale on the 5th-generation tensor
-// cores (tcgen05), one 128 x 256 output tile per CTA.
+// cores (tcgen05).  rms_linear_kernel: one 128 x 256 output tile per CTA,
+// gamma applied to the x tiles in shared memory; rms_linear_persistent
+// (further down): gamma folded into w, persistent CTA pairs on the 2-SM MMA.
 //
 // "TeleTron" section 4.2 fuses RMSNorm into the linear layer: the row's RMS
 // factor is computed in the block and used directly in the accumulation, so
@@ -9,7 +11,7 @@
 // with x [M, K], w [N, K] (K-major, as the MMA wants both operands), gamma
 // [K], bias [N], out [M, N], all f16 or all bf16, fp32 accumulation in TMEM.
 //
-// Roles (6 warps):
+// Roles of rms_linear_kernel (6 warps):
 //   warp 0     TMA producer: x tile 128 x 64 and w tile 256 x 64 per stage
 //              (128-byte swizzle), STAGES-deep ring, mbarrier complete_tx.
 //   warps 2-5  one tile row per thread: sum of squares of the row's x, then
@@ -84,6 +86,12 @@ __device__ __forceinline__ bool mbar_wait(u32 bar, u32 parity) {
   for (u32 i = 0; i < kMaxSpins; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
+}
+// the same wait in all 32 lanes with one outcome for the warp: a lane that
+// gave up makes the whole warp give up, so the .aligned tcgen05 loads after
+// it are always executed by the full warp
+__device__ __forceinline__ bool mbar_wait_warp(u32 bar, u32 parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
 // ---------------------------------------------------------------- TMA
@@ -234,7 +242,7 @@ rms_linear_kernel(const __grid_constant__ TensorMap tmap_x, const __grid_constan
     float ss = 0.f;
     for (int kt = 0; kt < KT; ++kt) {
       const int s = kt % STAGES;
-      if (!mbar_wait(full(s), (kt / STAGES) & 1)) { ok = false; break; }
+      if (!mbar_wait_warp(full(s), (kt / STAGES) & 1)) { ok = false; break; }
       // the row's 128 bytes hold its 64 values in 16-byte chunks, logical
       // chunk c at position c ^ (r % 8) (the 128-byte swizzle); step p visits
       // logical chunk p, so the 8 rows of a swizzle group hit 8 different
@@ -276,7 +284,7 @@ rms_linear_kernel(const __grid_constant__ TensorMap tmap_x, const __grid_constan
       }
     }
     const float rs = 1.0f / sqrtf(ss / KDIM + eps);
-    if (!mbar_wait(accum, 0)) ok = false;
+    if (!mbar_wait_warp(accum, 0)) ok = false;
     tc_fence_after();
     u16* orow = out + (long long)(m0 + r) * NDIM + n0;
 #pragma unroll 1
@@ -303,4 +311,363 @@ rms_linear_kernel(const __grid_constant__ TensorMap tmap_x, const __grid_constan
     tmem_dealloc(tmem, TMEM_COLS);
   }
   if (!ok) atomicExch(err, 1);
+}
+
+// ---------------------------------------------------------------- CTA pairs
+__device__ __forceinline__ u32 cluster_rank() {
+  u32 r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// the shared::cluster address of this CTA's shared variable `addr` in the
+// cluster's CTA `rank`
+__device__ __forceinline__ u32 peer_addr(u32 addr, u32 rank) {
+  u32 r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(u32 cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+// a bare signal to a barrier of the partner CTA: it orders nothing, so it
+// only relays an event whose data the barrier's waiters read afterwards
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(u32 cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// TMA load into this CTA's shared memory whose completion is signalled on an
+// mbarrier of either CTA of the pair (a shared::cluster address)
+__device__ __forceinline__ void tma_load_2d_pair(u32 dst, const TensorMap* map, u32 bar_cluster,
+                                                 int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<unsigned long long>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(u32 slot, u32 ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(u32 taddr, u32 ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void umma_pair(u32 d_tmem, unsigned long long a, unsigned long long b,
+                                          u32 idesc, u32 accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, "
+      "p; }" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive on the mbarrier at offset `bar` of both CTAs once the pair's
+// outstanding MMAs have completed
+__device__ __forceinline__ void umma_commit_pair(u32 bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(bar),
+      "h"((unsigned short)0x3)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- TMA store
+__device__ __forceinline__ void tma_store_2d(const TensorMap* map, u32 src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<unsigned long long>(map)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// until at most one committed store group still reads shared memory
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared16(u32 addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// ---------------------------------------------------------------- persistent
+// The fast path (gamma folded into w) as a persistent kernel on CTA pairs
+// with the 2-SM MMA.  A cluster of two CTAs owns 256 x 256 blocks of the
+// output; CTA `rank` stages the 128 rows of x of its own 128 x 256 tile and
+// the 128-row half `rank` of the w tile, and one thread of CTA 0 issues
+// tcgen05.mma.cta_group::2 (M 256, N 256, K 16): each SM's tensor core reads
+// its own x rows and both halves of w, and writes its tile's accumulator into
+// its own TMEM.  Per k-step an SM writes and reads 32 KB of shared memory
+// where a 128 x 256 tile on one SM moves 48 KB each way.
+//
+// Work: runs of PAIR_RUN consecutive 256-column blocks of one pair of row
+// tiles; cluster c takes runs c, c + nclusters, ...  The row statistics of a
+// run are computed once, on its first block, and kept by the epilogue for
+// the others; runs taken at the same time cover few row tiles, so x stays in
+// L2 for all the blocks that read it.
+//
+// 10 warps per CTA:
+//   warp 0     TMA producer; both CTAs' copies complete on CTA 0's "full"
+//   warp 1     TMEM allocation (both CTAs, collectively); in CTA 0 one thread
+//              issues the MMAs of every block
+//   warps 2-5  epilogue of this CTA's tile, 32 rows each (TMEM lane quarter
+//              warp % 4): TMEM -> registers -> s_m * acc + bias, * scale ->
+//              a 32 x 32 block in shared memory -> TMA bulk store
+//   warps 6-9  row statistics of this CTA's x rows, handed to the epilogue in
+//              shared memory (rstd[buffer][row])
+// Signals: CTA 0's "full" completes when both CTAs' copies of a stage have
+// landed; its row warps read their x from then on, and the MMA thread relays
+// the event to CTA 1's "xfull" (the TMA writes were done before their
+// completion reached "full"), so both CTAs' row warps read x while the tensor
+// cores work on the stage.  A stage is free again ("empty", count 5) once the
+// pair's MMAs are done with it (commit to both CTAs) and this CTA's four row
+// warps have passed it.  The accumulator's commit goes to "acc_full" in both
+// CTAs; all 8 epilogue warps of the pair free it on CTA 0's "acc_empty".
+// With an odd number of 128-row tiles the last pair's second tile lies past
+// M: that CTA loads no x, its rows are computed from stale shared memory and
+// never stored.
+constexpr int NT_TILES = NDIM / BN;
+constexpr int B_HALF = B_BYTES / 2;
+constexpr int PSTAGE_BYTES = A_BYTES + B_HALF;  // per CTA and stage
+constexpr int NACC = PAIR_NACC;                 // accumulator buffers in TMEM
+constexpr int RUN = PAIR_RUN;                   // column blocks per run
+constexpr int RUNS_PER_MP = (NT_TILES + RUN - 1) / RUN;
+constexpr int OUT_BLOCK = 32 * 32 * 2;  // one epilogue warp's staged 32 x 32 block
+// instruction descriptor of the pair's MMA: M 256, N 256
+constexpr u32 kIdescPair = (1u << 4) | ((DT == 2 ? 1u : 0u) << 7) | ((DT == 2 ? 1u : 0u) << 10) |
+                           ((u32)(BN >> 3) << 17) | ((u32)((2 * BM) >> 4) << 24);
+
+extern "C" __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
+rms_linear_persistent(const __grid_constant__ TensorMap tmap_x,
+                      const __grid_constant__ TensorMap tmap_w,
+                      const __grid_constant__ TensorMap tmap_out, const u16* __restrict__ bias,
+                      int m_tiles, float eps, float scale, int* err) {
+  extern __shared__ unsigned char smem_raw[];
+  const u32 raw = smem_u32(smem_raw);
+  const u32 base = (raw + 1023u) & ~1023u;
+  unsigned char* const base_ptr = smem_raw + (base - raw);
+  float* const rstd_buf = reinterpret_cast<float*>(base_ptr + PSTAGES * PSTAGE_BYTES);  // [2][128]
+  const u32 staging = base + PSTAGES * PSTAGE_BYTES + 2 * 128 * 4;  // [4 warps][2][32 x 32]
+  const u32 bars = staging + 4 * 2 * OUT_BLOCK;
+  auto stage_a = [&](int s) { return base + s * PSTAGE_BYTES; };
+  auto stage_b = [&](int s) { return base + s * PSTAGE_BYTES + A_BYTES; };
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (PSTAGES + s); };
+  auto xfull = [&](int s) { return bars + 8u * (2 * PSTAGES + s); };
+  auto acc_full = [&](int b) { return bars + 8u * (3 * PSTAGES + b); };
+  auto acc_empty = [&](int b) { return bars + 8u * (3 * PSTAGES + 2 + b); };
+  auto rs_full = [&](int b) { return bars + 8u * (3 * PSTAGES + 4 + b); };
+  auto rs_empty = [&](int b) { return bars + 8u * (3 * PSTAGES + 6 + b); };
+  const u32 tmem_slot = bars + 8u * (3 * PSTAGES + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const u32 rank = cluster_rank();
+  const int m_pairs = (m_tiles + 1) / 2;
+  const int runs = m_pairs * RUNS_PER_MP;
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  // run -> its pair of row tiles, first column block and number of blocks
+  auto run_mp = [&](int run) { return run / RUNS_PER_MP; };
+  auto run_n = [&](int run) { return (run % RUNS_PER_MP) * RUN; };
+  auto run_len = [&](int run) { return min(RUN, NT_TILES - run_n(run)); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PSTAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 5);
+      mbar_init(xfull(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 8);
+      mbar_init(rs_full(b), 128);
+      mbar_init(rs_empty(b), 4);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, NACC * TMEM_COLS);
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers and TMEM exist before the first copy
+  tc_fence_after();
+  const u32 tmem = *reinterpret_cast<volatile u32*>(base_ptr + (tmem_slot - base));
+
+  bool ok = true;
+  if (warp == 0) {
+    if (lane == 0) {
+      const u32 full0 = peer_addr(full(0), 0);  // CTA 0's "full" barriers
+      long long g = 0;                          // stage uses so far
+      for (int run = cluster; run < runs && ok; run += nclusters) {
+        const int mp = run_mp(run), nb = run_n(run), len = run_len(run);
+        const int mt = 2 * mp + static_cast<int>(rank);
+        const bool has_x = mt < m_tiles;
+        const u32 tx = (2 * mp + 1 < m_tiles ? 2 : 1) * A_BYTES + 2 * B_HALF;
+        for (int t = 0; t < len && ok; ++t) {
+          const int n0 = (nb + t) * BN;
+          for (int kt = 0; kt < KT; ++kt, ++g) {
+            const int s = static_cast<int>(g % PSTAGES);
+            if (!mbar_wait(empty(s), ((g / PSTAGES) & 1) ^ 1)) { ok = false; break; }
+            if (rank == 0) mbar_expect_tx(full(s), tx);  // what both CTAs land
+            if (has_x) tma_load_2d_pair(stage_a(s), &tmap_x, full0 + 8u * s, kt * BK, mt * BM);
+            tma_load_2d_pair(stage_b(s), &tmap_w, full0 + 8u * s, kt * BK,
+                             n0 + static_cast<int>(rank) * (BN / 2));
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      const u32 xfull1 = peer_addr(xfull(0), 1);  // CTA 1's "xfull" barriers
+      long long g = 0;
+      int i = 0;  // blocks so far
+      for (int run = cluster; run < runs && ok; run += nclusters) {
+        const int len = run_len(run);
+        for (int t = 0; t < len && ok; ++t, ++i) {
+          const int b = i % NACC;
+          if (!mbar_wait(acc_empty(b), ((i / NACC) & 1) ^ 1)) { ok = false; break; }
+          tc_fence_after();
+          const u32 d = tmem + b * TMEM_COLS;
+          for (int kt = 0; kt < KT; ++kt, ++g) {
+            const int s = static_cast<int>(g % PSTAGES);
+            if (!mbar_wait(full(s), (g / PSTAGES) & 1)) { ok = false; break; }
+            mbar_arrive_cluster_relaxed(xfull1 + 8u * s);
+            tc_fence_after();
+            const unsigned long long a = sw128_desc(stage_a(s)), bd = sw128_desc(stage_b(s));
+#pragma unroll
+            for (int j = 0; j < BK / 16; ++j)
+              umma_pair(d, a + 2ull * j, bd + 2ull * j, kIdescPair, (kt | j) != 0);
+            umma_commit_pair(empty(s));
+          }
+          umma_commit_pair(acc_full(b));
+        }
+      }
+    }
+  } else if (warp < 6) {
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const u32 acc_empty0 = peer_addr(acc_empty(0), 0);
+    const u32 stg = staging + q * 2 * OUT_BLOCK;
+    int i = 0, j = 0, sc = 0;  // blocks, runs, staged 32 x 32 blocks so far
+    for (int run = cluster; run < runs && ok; run += nclusters, ++j) {
+      const int mp = run_mp(run), nb = run_n(run), len = run_len(run);
+      const int mt = 2 * mp + static_cast<int>(rank);
+      const bool store = mt < m_tiles;
+      if (!mbar_wait_warp(rs_full(j & 1), (j >> 1) & 1)) { ok = false; break; }
+      const float rs = rstd_buf[(j & 1) * 128 + r];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(rs_empty(j & 1));
+      for (int t = 0; t < len; ++t, ++i) {
+        const int n0 = (nb + t) * BN, b = i % NACC;
+        if (!mbar_wait_warp(acc_full(b), (i / NACC) & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (store) {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c, ++sc) {
+            u32 acc[32];
+            tmem_ld32(tmem + b * TMEM_COLS + ((u32)(q * 32) << 16) + c * 32, acc);
+            u32 bw[16];
+            if constexpr (HAS_BIAS) {
+              const uint4* bp = reinterpret_cast<const uint4*>(bias + n0 + c * 32);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const uint4 t4 = __ldg(bp + v);
+                bw[4 * v] = t4.x; bw[4 * v + 1] = t4.y; bw[4 * v + 2] = t4.z; bw[4 * v + 3] = t4.w;
+              }
+            }
+            float y[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              float v = __uint_as_float(acc[e]) * rs;
+              if constexpr (HAS_BIAS) v += get_elem<DT>(bw, e);
+              y[e] = v * scale;
+            }
+            u32 o[16];
+            pack_vec<DT>(y, o);
+            // this buffer's store from two blocks ago must have read it
+            const u32 buf = stg + (sc & 1) * OUT_BLOCK;
+            if (sc >= 2 && lane == 0) bulk_wait_read1();
+            __syncwarp();
+            // row `lane` of the 32 x 32 block, 4 chunks of 16 bytes; lanes
+            // 2l and 2l+1 start at chunk l, so 8 lanes cover all 32 banks
+            const uint4 v0 = make_uint4(o[0], o[1], o[2], o[3]);
+            const uint4 v1 = make_uint4(o[4], o[5], o[6], o[7]);
+            const uint4 v2 = make_uint4(o[8], o[9], o[10], o[11]);
+            const uint4 v3 = make_uint4(o[12], o[13], o[14], o[15]);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int cc = (h + (lane >> 1)) & 3;
+              const uint4 v = cc == 0 ? v0 : cc == 1 ? v1 : cc == 2 ? v2 : v3;
+              st_shared16(buf + lane * 64 + cc * 16, v);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmap_out, buf, n0 + c * 32, mt * BM + q * 32);
+              bulk_commit();
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8u * b);
+      }
+    }
+    if (lane == 0) bulk_wait_all();  // the stores have read shared memory and landed
+    __syncwarp();
+  } else {
+    const int r = (warp - 6) * 32 + lane;
+    long long g = 0;
+    int j = 0;  // runs so far
+    for (int run = cluster; run < runs && ok; run += nclusters, ++j) {
+      const int len = run_len(run);
+      for (int t = 0; t < len && ok; ++t) {
+        // the first block of a run reads x for the statistics; the others
+        // only pass their stages
+        float ss = 0.f;
+        for (int kt = 0; kt < KT; ++kt, ++g) {
+          const int s = static_cast<int>(g % PSTAGES);
+          if (!mbar_wait_warp(rank == 0 ? full(s) : xfull(s), (g / PSTAGES) & 1)) {
+            ok = false;
+            break;
+          }
+          if (t == 0) {
+            const uint4* row =
+                reinterpret_cast<const uint4*>(base_ptr + (stage_a(s) - base) + r * 128);
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+              const uint4 v4 = row[p ^ (r & 7)];
+              const u32 wv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float xv = get_elem<DT>(wv, e);
+                ss += xv * xv;
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty(s));
+        }
+        if (!ok || t != 0) continue;
+        if (!mbar_wait_warp(rs_empty(j & 1), ((j >> 1) & 1) ^ 1)) { ok = false; break; }
+        rstd_buf[(j & 1) * 128 + r] = 1.0f / sqrtf(ss / KDIM + eps);
+        mbar_arrive(rs_full(j & 1));
+      }
+    }
+  }
+  if (!ok) atomicExch(err, 1);
+  tc_fence_before();
+  cluster_sync();  // both CTAs are done with TMEM and with each other's barriers
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, NACC * TMEM_COLS);
+  }
 }

@@ -18,6 +18,11 @@ namespace {
 
 constexpr int kStages = 4;
 constexpr int kBM = 128, kBN = 256, kBK = 64;
+// the persistent CTA-pair kernel: stages of x (128 x 64) and half a w tile
+// (128 x 64) per CTA, accumulator buffers of 256 TMEM columns, runs of
+// column blocks that share one computation of the row statistics, and a
+// 32 x 32 output block per epilogue warp staged for the TMA store
+constexpr int kPairStages = 6, kPairAcc = 2, kPairRun = 2, kOutBox = 32;
 
 struct RlKernel {
   std::shared_ptr<Module> mod;
@@ -40,10 +45,11 @@ int rl_kernel(int64_t K, int64_t N, fuse_dtype dt, bool has_bias, bool apply_gam
   std::string src = fmt(
       "// RMSNorm -> Linear -> scale, K %lld, N %lld, %s, tcgen05\n"
       "constexpr int DT = %d;\nconstexpr long long KDIM = %lldLL;\nconstexpr long long NDIM = %lldLL;\n"
-      "constexpr int STAGES = %d;\nconstexpr bool HAS_BIAS = %s, APPLY_GAMMA = %s;\n"
+      "constexpr int STAGES = %d, PSTAGES = %d, PAIR_NACC = %d, PAIR_RUN = %d;\n"
+      "constexpr bool HAS_BIAS = %s, APPLY_GAMMA = %s;\n"
       "#include \"fuse/rms_linear.cuh\"\n",
       (long long)K, (long long)N, dtype_name(dt), static_cast<int>(dt), (long long)K, (long long)N,
-      kStages, has_bias ? "true" : "false", apply_gamma ? "true" : "false");
+      kStages, kPairStages, kPairAcc, kPairRun, has_bias ? "true" : "false", apply_gamma ? "true" : "false");
   if (int rc = jit_compile(src, "rmsnorm_linear", &k.mod)) return rc;
   g_kernels.emplace(key, k);
   *out = k;
@@ -65,6 +71,21 @@ int encode_kmajor(const DriverApi* api, CUtensorMap* map, const void* ptr, fuse_
   return FUSE_OK;
 }
 
+// The output [M, N] as the destination of 32 x 32 TMA stores (no swizzle).
+int encode_out(const DriverApi* api, CUtensorMap* map, void* ptr, fuse_dtype dt, int64_t M,
+               int64_t N) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2};
+  cuuint32_t box[2] = {kOutBox, kOutBox};
+  cuuint32_t elem[2] = {1, 1};
+  CUresult r = api->TensorMapEncodeTiled(
+      map, dt == FUSE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+      ptr, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuTensorMapEncodeTiled(out)");
+  return FUSE_OK;
+}
+
 int error_word(const DriverApi* api, int device, CUdeviceptr* out) {
   if (!g_err[device]) {
     CUdeviceptr p;
@@ -74,6 +95,29 @@ int error_word(const DriverApi* api, int device, CUdeviceptr* out) {
     g_err[device] = p;
   }
   *out = g_err[device];
+  return FUSE_OK;
+}
+
+// How many 2-CTA clusters of the persistent kernel fit on the device at
+// once (some SMs may be left over when a GPC has an odd number of them).
+int max_clusters(const DriverApi* api, CUfunction fn, int smem, int* out) {
+  static std::map<CUfunction, int> cache;
+  if (auto it = cache.find(fn); it != cache.end()) {
+    *out = it->second;
+    return FUSE_OK;
+  }
+  CUlaunchConfig cfg = {};
+  cfg.gridDimX = 2;
+  cfg.gridDimY = cfg.gridDimZ = 1;
+  cfg.blockDimX = 320;
+  cfg.blockDimY = cfg.blockDimZ = 1;
+  cfg.sharedMemBytes = static_cast<unsigned>(smem);
+  int n = 0;
+  CUresult r = api->OccupancyMaxActiveClusters(&n, fn, &cfg);
+  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuOccupancyMaxActiveClusters");
+  if (n < 1) return fail(FUSE_E_CUDA, "no 2-CTA cluster of rmsnorm_linear fits on this device");
+  cache.emplace(fn, n);
+  *out = n;
   return FUSE_OK;
 }
 
@@ -91,7 +135,8 @@ extern "C" int rmsnorm_linear(const void* x, const void* gamma, const void* w, c
     return fail(FUSE_E_SHAPE, fmt("need M %% %d == 0, N %% %d == 0, K %% %d == 0 and K > 0 "
                                   "(got M %lld, N %lld, K %lld)",
                                   kBM, kBN, kBK, (long long)M, (long long)N, (long long)K));
-  if (M / kBM > 65535 || K > (int64_t(1) << 20)) return fail(FUSE_E_SHAPE, "M or K too large");
+  if (M / kBM > 65535 || K > (int64_t(1) << 20) || (M / kBM) * (N / kBN) > INT32_MAX)
+    return fail(FUSE_E_SHAPE, "M, K or the tile count too large");
   if (!(eps >= 0.f) || !std::isfinite(scale)) return fail(FUSE_E_ARG, "bad eps or scale");
   if (M == 0 || N == 0) return FUSE_OK;
   if (!x || !w || !out) return fail(FUSE_E_NULL, "NULL tensor pointer");
@@ -107,18 +152,46 @@ extern "C" int rmsnorm_linear(const void* x, const void* gamma, const void* w, c
   if (int rc = current_device(&d)) return rc;
   const DriverApi* api;
   if (int rc = driver(&api)) return rc;
+  // gamma folded into w: the persistent kernel (CTA pairs sharing the w
+  // tiles, double-buffered accumulator); gamma given: one CTA per tile,
+  // gamma applied to the x tiles in shared memory
+  const bool persistent = gamma == nullptr;
   CUfunction fn;
-  if (int rc = jit_function(*k.mod, "rms_linear_kernel", d, &fn)) return rc;
+  if (int rc = jit_function(*k.mod, persistent ? "rms_linear_persistent" : "rms_linear_kernel", d,
+                            &fn))
+    return rc;
   CUdeviceptr err;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (int rc = error_word(api, d.ordinal, &err)) return rc;
   }
-  CUresult r = api->FuncSetAttribute(fn, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, k.smem);
+  const int smem = persistent ? 1024 + kPairStages * (kBM + kBN / 2) * kBK * 2 + 2 * 128 * 4 +
+                                    4 * 2 * kOutBox * kOutBox * 2 + 8 * (3 * kPairStages + 8) + 16
+                              : k.smem;
+  CUresult r = api->FuncSetAttribute(fn, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, smem);
   if (r != CUDA_SUCCESS) return cuda_fail(r, "cuFuncSetAttribute(shared memory)");
   alignas(64) CUtensorMap mx, mw;
   if (int rc = encode_kmajor(api, &mx, x, dt, M, K, kBM)) return rc;
-  if (int rc = encode_kmajor(api, &mw, w, dt, N, K, kBN)) return rc;
+  // the CTA pairs of the persistent kernel each load one 128-row half of a w tile
+  if (int rc = encode_kmajor(api, &mw, w, dt, N, K, persistent ? kBN / 2 : kBN)) return rc;
+  if (persistent) {
+    int clusters = 0;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if (int rc = max_clusters(api, fn, smem, &clusters)) return rc;
+    }
+    alignas(64) CUtensorMap mo;
+    if (int rc = encode_out(api, &mo, out, dt, M, N)) return rc;
+    int m_tiles = static_cast<int>(M / kBM);
+    const int64_t runs = (M / kBM + 1) / 2 * ((N / kBN + kPairRun - 1) / kPairRun);
+    const unsigned grid = 2u * static_cast<unsigned>(std::min<int64_t>(runs, clusters));
+    void* args[] = {&mx, &mw, &mo, &bias, &m_tiles, &eps, &scale, &err};
+    r = api->LaunchKernel(fn, grid, 1, 1, 320, 1, 1, smem, reinterpret_cast<CUstream>(stream), args,
+                          nullptr);
+    if (r != CUDA_SUCCESS) return cuda_fail(r, "cuLaunchKernel(rmsnorm_linear)");
+    stat_launch();
+    return FUSE_OK;
+  }
   void* args[] = {&mx, &mw, &gamma, &bias, &out, &eps, &scale, &err};
   r = api->LaunchKernel(fn, static_cast<unsigned>(N / kBN), static_cast<unsigned>(M / kBM), 1, 192,
                         1, 1, k.smem, reinterpret_cast<CUstream>(stream), args, nullptr);

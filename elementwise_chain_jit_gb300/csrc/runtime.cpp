@@ -145,6 +145,7 @@ void load_driver() {
   FUSE_GET(CtxSynchronize, "cuCtxSynchronize");
   FUSE_GET(MemcpyDtoH, "cuMemcpyDtoH");
   FUSE_GET(MemsetD32, "cuMemsetD32");
+  FUSE_GET(OccupancyMaxActiveClusters, "cuOccupancyMaxActiveClusters");
 #undef FUSE_GET
   if (!ok) return;
   CUresult r = g_api.Init(0);

@@ -62,17 +62,17 @@ def test_rejects_unsupported_shapes_and_dtypes():
     assert e.value.code == -3
 
 
-def _folded_case(M, N, K, dt, seed, rows=None):
+def _folded_case(M, N, K, dt, seed, rows=None, bias=True):
     x = workloads.normal((M, K), 0, 1, seed, dt)
     g = workloads.normal(K, 1, 0.1, seed + 1, dt)
     w = workloads.normal((N, K), 0, 1 / np.sqrt(K), seed + 2, dt)
-    b = workloads.normal(N, 0, 0.5, seed + 3, dt)
+    b = workloads.normal(N, 0, 0.5, seed + 3, dt) if bias else None
     wd = to_dev(w.reshape(-1), dt)
     wf = torch.empty_like(wd)
     F.rmsnorm_linear_fold(wd, to_dev(g, dt), wf, dt, N=N, K=K)
     out = Guarded(M * N, dt)
-    F.rmsnorm_linear(to_dev(x.reshape(-1), dt), None, wf, to_dev(b, dt), out.t, 1e-6, 0.5, dt,
-                     M=M, N=N, K=K)
+    F.rmsnorm_linear(to_dev(x.reshape(-1), dt), None, wf, None if b is None else to_dev(b, dt),
+                     out.t, 1e-6, 0.5, dt, M=M, N=N, K=K)
     torch.cuda.synchronize()
     assert F.fuse_device_error() == 0
     assert out.canary_ok()
@@ -87,7 +87,7 @@ def _folded_case(M, N, K, dt, seed, rows=None):
     assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], want[bad][:5])
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 1024), (384, 256, 448)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 1024), (384, 256, 448), (640, 768, 128)])
 @pytest.mark.parametrize("dt", [F.BF16, F.F16])
 def test_folded_gamma_fast_path(M, N, K, dt):
     _folded_case(M, N, K, dt, 40 + K % 89)
@@ -95,3 +95,11 @@ def test_folded_gamma_fast_path(M, N, K, dt):
 
 def test_folded_full_size_sampled_rows():
     _folded_case(16384, 4096, 4096, F.BF16, 50, rows=[0, 3, 129, 8191, 16383])
+
+
+@pytest.mark.parametrize("bias", [True, False])
+def test_folded_many_tiles_per_cta(bias):
+    # 80 x 8 = 640 output tiles on at most one CTA per SM: every CTA of the
+    # persistent kernel takes several tiles, so both TMEM accumulator buffers
+    # and both phases of their barriers are reused; every row is checked
+    _folded_case(10240, 2048, 128, F.BF16, 60, bias=bias)
