@@ -291,6 +291,10 @@ def _rms_linear_item(dev, with_unfused, M=16384):
             y = (xf * torch.rsqrt(xf.pow(2).mean(-1, keepdim=True) + eps) * g.float()).to(torch.bfloat16)
             return torch.nn.functional.linear(y, w, b) * scale
         it.unfused, it.n_unfused = unfused, 9
+        # the bare GEMM of the same shape in the vendor library, no norm, no
+        # bias, no scale: what the fused kernel's contraction is held against
+        gemm_out = torch.empty_like(out)
+        it.library_gemm = lambda: torch.matmul(x, wf.t(), out=gemm_out)
     return it
 
 
@@ -731,6 +735,8 @@ def run_gpu(args):
             ums = time_fn(rl.unfused, reps=5, warm=2)
             d.update({"us_unfused": ums * 1e3, "unfused_kernels": rl.n_unfused,
                       "speedup": ums / rms})
+            gms = time_fn(rl.library_gemm, reps=10, warm=3)
+            d.update({"us_cublas_gemm_only": gms * 1e3, "fused_vs_cublas_gemm": gms / rms})
         next_rows[rl.name] = d
         del rl
     # dominant kernel and its roofline
