@@ -133,6 +133,17 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workload
 
+# Special-function unit (MUFU) work of a chain: exp is one ex2, sigmoid one
+# ex2 and one rcp (the generated code's exp and sigmoid); the unit retires 16
+# of these per SM and clock.
+MUFU_PER_SM_CLK = 16
+
+
+def mufu_per_element(spec):
+    ops = [o.split(":")[0] for o in spec.split(";")]
+    return ops.count("exp") + 2 * ops.count("sigmoid")
+
+
 class Item:
     """One fused workload: a single launch of the library."""
 
@@ -141,6 +152,7 @@ class Item:
         self.unfused, self.n_unfused = unfused, n_unfused
         self.kernel = kernel
         self.inputs, self.outputs = [], []   # device tensors (for the end-to-end copies)
+        self.mufu_ops = 0
 
 
 def _tdt(dt):
@@ -177,6 +189,7 @@ def build_items(dev, with_unfused=True, only=None, flat_elems=None, spec=None, s
         nbytes = sum(n * _esz(d) for d in c.in_dtypes) + n * _esz(c.out_dtype)
         it = Item(name, nbytes, lambda: F.fuse_launch(c, ins, out), kernel=("chain", spec, shape, dt))
         it.inputs, it.outputs = ins, [out]
+        it.mufu_ops = n * mufu_per_element(spec)
         if with_unfused:
             it.unfused, it.n_unfused = unfused_chain(spec, dt, shape, ins, out)
         return it
@@ -709,6 +722,16 @@ def run_gpu(args):
                       "speedup": ums / ms, "extra_cost_per_unfused_op_us": L * 1e3})
         if it.bytes < 64e6 and not args.no_unfused:
             d.update(graph_times(it))
+        if it.mufu_ops:
+            # two rooflines: HBM bytes and special-function unit operations
+            # at the clock sampled during the timed region
+            mhz = clocks.summary().get("sm_mhz") or 2070.0
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            mufu_us = it.mufu_ops / (MUFU_PER_SM_CLK * sms * mhz * 1e6) * 1e6
+            hbm_us = it.bytes / (peak * 1e9) * 1e6
+            d.update({"mufu_ops": it.mufu_ops, "mufu_bound_us": mufu_us, "hbm_bound_us": hbm_us,
+                      "bound": "mufu" if mufu_us > hbm_us else "hbm",
+                      "frac_of_bound": max(mufu_us, hbm_us) / (ms * 1e3)})
         per_chain[it.name] = d
     # next rows, measured beside the step (not part of its workload)
     next_rows = {}

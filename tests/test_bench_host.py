@@ -33,3 +33,12 @@ def test_reference_arm_prints_one_json_line(capsys):
     line = json.loads(out[0])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_mufu_count_of_a_chain():
+    # exp: one ex2; sigmoid: one ex2 and one rcp; the prologue, scale
+    # constants and the other ops use no special-function unit
+    assert bench.mufu_per_element("shuffle:4;exp") == 1
+    assert bench.mufu_per_element("relu;sigmoid") == 2
+    assert bench.mufu_per_element("exp;sigmoid;relu;mul") == 3
+    assert bench.mufu_per_element("cast:f32;scale:0.5;add;mul") == 0
