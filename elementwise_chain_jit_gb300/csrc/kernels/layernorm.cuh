@@ -45,23 +45,24 @@ __device__ __forceinline__ void chan_merge(float& n, float& mean, float& m2, flo
   n = nt;
 }
 
+#ifndef LN_MAX_REGS
+#define LN_MAX_REGS 255
+#endif
 #if FUSE_LN_VEC
-extern "C" __global__ void __launch_bounds__(BLOCK)
+extern "C" __global__ void __maxnreg__(LN_MAX_REGS)
 layernorm_vec(const void* x, const void* res, const void* gamma, const void* beta, void* out,
               void* res_out, long long rows, float eps) {
   __shared__ float pn[NWARPS], pmean[NWARPS], pm2[NWARPS];
   constexpr long long ROW_W = (long long)HIDDEN * Dt<DT>::bytes / 4;
   for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
     const u32* xr = static_cast<const u32*>(x) + row * ROW_W;
-    u32 wx[R][NWV], wr[R][NWV], wg[R][NWV], wb[R][NWV];
+    u32 wx[R][NWV], wr[R][NWV];
 #pragma unroll
     for (int i = 0; i < R; ++i) {
       const int v = threadIdx.x + i * BLOCK;
       if (NVR % BLOCK == 0 || v < NVR) {
         load_words(xr + v * NWV, wx[i]);
         if constexpr (HAS_RES) load_words(static_cast<const u32*>(res) + row * ROW_W + v * NWV, wr[i]);
-        if constexpr (HAS_GAMMA) load_words_cached(static_cast<const u32*>(gamma) + v * NWV, wg[i]);
-        if constexpr (HAS_BETA) load_words_cached(static_cast<const u32*>(beta) + v * NWV, wb[i]);
       }
     }
     float h[R][VEC];
@@ -120,24 +121,21 @@ layernorm_vec(const void* x, const void* res, const void* gamma, const void* bet
         pm2[threadIdx.x >> 5] = m2;
       }
       __syncthreads();
-      float wm[NWARPS], wq[NWARPS];
-#pragma unroll
-      for (int w = 0; w < NWARPS; ++w) {
-        wm[w] = pmean[w];
-        wq[w] = pm2[w];
-      }
+      // the warps' partials merged by a butterfly over lanes (lane % NWARPS
+      // holds warp lane % NWARPS); both partners of a step compute
+      // mean = (a + b) / 2 and M2 = (M2a + M2b) + d^2 * n / 2, which do not
+      // depend on the operand order, so every lane ends with the same bits
+      mean = pmean[(threadIdx.x & 31) % NWARPS];
+      m2 = pm2[(threadIdx.x & 31) % NWARPS];
 #pragma unroll
       for (int step = 1; step < NWARPS; step *= 2) {
-#pragma unroll
-        for (int w = 0; w + step < NWARPS; w += 2 * step) {
-          const float d = wm[w + step] - wm[w];
-          wm[w] = 0.5f * (wm[w] + wm[w + step]);
-          wq[w] += wq[w + step] + d * d * half_n;
-        }
+        const float mb = __shfl_xor_sync(0xffffffffu, mean, step);
+        const float qb = __shfl_xor_sync(0xffffffffu, m2, step);
+        const float d = mb - mean;
+        mean = 0.5f * (mean + mb);
+        m2 = (m2 + qb) + d * d * half_n;
         half_n *= 2.f;
       }
-      mean = wm[0];
-      m2 = wq[0];
     } else {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -159,16 +157,26 @@ layernorm_vec(const void* x, const void* res, const void* gamma, const void* bet
       for (int w = 1; w < NWARPS; ++w) chan_merge(cnt, mean, m2, pn[w], pmean[w], pm2[w]);
     }
     const float rstd = 1.0f / sqrtf(m2 / HIDDEN + eps);
+    // gamma and beta (the same for every row, cache-resident) are read only
+    // now: the pointers pass through an empty asm that takes rstd, so the
+    // compiler cannot hoist their loads above the reductions, where they would
+    // hold registers
+    const u32* gp = static_cast<const u32*>(gamma);
+    const u32* bp = static_cast<const u32*>(beta);
+    asm volatile("" : "+l"(gp), "+l"(bp) : "f"(rstd));
 #pragma unroll
     for (int i = 0; i < R; ++i) {
       const int v = threadIdx.x + i * BLOCK;
       if (NVR % BLOCK == 0 || v < NVR) {
+        u32 wg[NWV], wb[NWV];
+        if constexpr (HAS_GAMMA) load_words_cached(gp + v * NWV, wg);
+        if constexpr (HAS_BETA) load_words_cached(bp + v * NWV, wb);
         float y[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
           float t = (h[i][e] - mean) * rstd;
-          if constexpr (HAS_GAMMA) t *= get_elem<DT>(wg[i], e);
-          if constexpr (HAS_BETA) t += get_elem<DT>(wb[i], e);
+          if constexpr (HAS_GAMMA) t *= get_elem<DT>(wg, e);
+          if constexpr (HAS_BETA) t += get_elem<DT>(wb, e);
           y[e] = t;
         }
         u32 o[NWV];

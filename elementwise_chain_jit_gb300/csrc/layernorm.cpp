@@ -9,6 +9,8 @@
 #include <map>
 #include <tuple>
 
+#include <cstdlib>
+
 #include "internal.h"
 
 namespace fuse {
@@ -22,6 +24,20 @@ struct LnKernel {
 
 std::mutex g_mu;
 std::map<std::tuple<int64_t, int, int>, LnKernel> g_kernels;
+
+// Registers a thread may use.  With one vector a thread (rows up to 16384
+// bf16 elements) the compiler left to itself takes 72 (3 CTAs of 256 threads
+// per SM); capped at 48 (5 CTAs) it holds the row's values without spilling.
+// Measured on GB300 at hidden 4096 bf16: 100.1 us with 72 registers, 93.0
+// with 64, 90.9 with 48, 90.9 with 40 (spilling), 94.2 with 36.  Longer rows
+// keep several vectors a thread in 1024-thread blocks and get the most those
+// blocks allow (64).  FUSE_LN_MAX_REGS overrides.
+int max_regs(int block, int64_t r) {
+  const int limit = std::min(255, 65536 / block / 8 * 8);
+  const char* e = getenv("FUSE_LN_MAX_REGS");
+  const int want = e && *e ? atoi(e) : (r == 1 ? 48 : limit);
+  return std::min(limit, std::max(24, want));
+}
 
 int ln_kernel(int64_t hidden, fuse_dtype dt, int flags, LnKernel* out) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -45,10 +61,10 @@ int ln_kernel(int64_t hidden, fuse_dtype dt, int flags, LnKernel* out) {
       "constexpr int DT = %d;\nconstexpr int HIDDEN = %lld;\nconstexpr int BLOCK = %d;\n"
       "constexpr int VEC = %d;\nconstexpr int R = %lld;\n"
       "constexpr bool HAS_RES = %s, HAS_GAMMA = %s, HAS_BETA = %s;\n#define FUSE_LN_VEC %d\n"
-      "#include \"fuse/layernorm.cuh\"\n",
+      "#define LN_MAX_REGS %d\n#include \"fuse/layernorm.cuh\"\n",
       (long long)hidden, dtype_name(dt), static_cast<int>(dt), (long long)hidden, k.block, k.vec,
       (long long)r, (flags & 1) ? "true" : "false", (flags & 2) ? "true" : "false",
-      (flags & 4) ? "true" : "false", k.has_vec ? 1 : 0);
+      (flags & 4) ? "true" : "false", k.has_vec ? 1 : 0, max_regs(k.block, r));
   if (int rc = jit_compile(src, "layernorm_residual", &k.mod)) return rc;
   g_kernels.emplace(key, k);
   *out = k;
