@@ -21,7 +21,7 @@ struct Feats {
 
 template <int W>
 __device__ __forceinline__ float decode(int k, int cell, float v, float stride, float aw, float ah) {
-  const float p = 1.0f / (1.0f + expf(-v));
+  const float p = sigmoid(v);  // rcp_ge1 of 1 + exp(-v): within an ulp of the division
   if (k == 0) return (2.0f * p - 0.5f + static_cast<float>(cell % W)) * stride;
   if (k == 1) return (2.0f * p - 0.5f + static_cast<float>(cell / W)) * stride;
   if (k == 2) { const float t = 2.0f * p; return t * t * aw; }
