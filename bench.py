@@ -530,6 +530,36 @@ def traffic_record(name, src_hash):
 
 # ---------------------------------------------------------------- CPU oracle baseline
 
+def cpu_sample_all_cores(frac_div: int):
+    """The flat-chain part of the sample on every host core: the elements split
+    into one contiguous slice per core, one thread each, the same oracle call
+    per slice (ctypes releases the GIL while the C oracle runs).  Returns
+    (bytes, seconds, threads, description)."""
+    import concurrent.futures as cf
+
+    import oracle
+    import workloads as W
+    cores = os.cpu_count() or 1
+    n = W.FLAT_SIZES[-1] // frac_div
+    bounds = np.linspace(0, n, cores + 1).astype(np.int64)
+    total_b, total_t = 0, 0.0
+    with cf.ThreadPoolExecutor(cores) as ex:
+        for L in W.CHAIN_LENGTHS:
+            spec, dt = W.random_chain(L, 5)
+            ins, dts = W.chain_inputs(spec, dt, n, L)
+            ch = oracle.parse_spec(spec, dt)
+
+            def part(i, spec=spec, dt=dt, ins=ins, ch=ch):
+                lo, hi = int(bounds[i]), int(bounds[i + 1])
+                vals = oracle.chain_eval(spec, dt, [a[lo:hi] for a in ins], (hi - lo,))[0]
+                return oracle.store(vals, ch.out_dtype)
+            t0 = time.perf_counter()
+            list(ex.map(part, range(cores)))
+            total_t += time.perf_counter() - t0
+            total_b += sum(n * _esz(d) for d in dts) + n * _esz(ch.out_dtype)
+    return total_b, total_t, cores, f"flat chains L=1..32 on {n} elements, {cores} slices, one thread each"
+
+
 def cpu_sample(frac_div: int):
     """The oracle on a bounded sample of every workload; returns (bytes, seconds, description)."""
     import oracle
@@ -704,17 +734,20 @@ def run_gpu(args):
         barrier()
     launches = F.fuse_stats()["launches"] - launches0
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
-    per_item = [statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps))
+    per_step = [[evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps)]
                 for i in range(nitem)]
+    per_item = [statistics.mean(t) for t in per_step]
     ms_per_step = total_ms / args.steps
     value = job_gbs(step_bytes, world, ms_per_step)
 
     peak, peak_kind = peaks()
     # unfused per-op sequences (outside the timed region)
     per_chain = {}
-    for it, ms in zip(items, per_item):
+    for it, ms, ts in zip(items, per_item, per_step):
         d = {"bytes": it.bytes, "us_fused": ms * 1e3, "gbs": it.bytes / (ms / 1e3) / 1e9,
              "frac_of_" + peak_kind + "_peak": it.bytes / (ms / 1e3) / 1e9 / peak}
+        q = np.percentile(ts, [10, 50, 90])
+        d.update({"us_p10": q[0] * 1e3, "us_median": q[1] * 1e3, "us_p90": q[2] * 1e3})
         if it.unfused is not None and not args.no_unfused:
             ums = time_fn(it.unfused, reps=3, warm=1)
             L, T = launch_overhead(ums, ms, it.n_unfused)
@@ -843,7 +876,11 @@ def run_gpu(args):
     if rank == 0 and not args.no_cpu:
         b, t, desc = cpu_sample(64)
         cpu = {"value": b / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": desc + " (1/64 of each workload)", "seconds": t}
+               "sample": desc + " (1/64 of each workload)", "seconds": t,
+               "host_cores": os.cpu_count(), "nproc": len(os.sched_getaffinity(0))}
+        ab, at, athreads, adesc = cpu_sample_all_cores(64)
+        cpu["all_cores"] = {"value": ab / at / 1e9, "unit": UNIT, "cores": athreads,
+                            "sample": adesc, "seconds": at}
     clk = clocks.summary()
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,

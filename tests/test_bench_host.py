@@ -42,3 +42,8 @@ def test_mufu_count_of_a_chain():
     assert bench.mufu_per_element("relu;sigmoid") == 2
     assert bench.mufu_per_element("exp;sigmoid;relu;mul") == 3
     assert bench.mufu_per_element("cast:f32;scale:0.5;add;mul") == 0
+
+
+def test_cpu_all_cores_sample_uses_every_core():
+    b, t, threads, desc = bench.cpu_sample_all_cores(4096)
+    assert b > 0 and t > 0 and threads == (os.cpu_count() or 1) and "slices" in desc
