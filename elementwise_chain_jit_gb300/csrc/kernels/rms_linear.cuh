@@ -55,6 +55,12 @@ struct __align__(64) TensorMap {
   unsigned long long v[16];
 };
 
+__device__ __forceinline__ u32 dynamic_smem_bytes() {
+  u32 r;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+  return r;
+}
+
 __device__ __forceinline__ u32 smem_u32(const void* p) {
   u32 r;
   asm("{ .reg .u64 t; cvta.to.shared.u64 t, %1; cvt.u32.u64 %0, t; }" : "=r"(r) : "l"(p));
@@ -171,6 +177,13 @@ extern "C" __global__ void __launch_bounds__(192, 1)
 rms_linear_kernel(const __grid_constant__ TensorMap tmap_x, const __grid_constant__ TensorMap tmap_w,
                   const u16* __restrict__ gamma, const u16* __restrict__ bias, u16* __restrict__ out,
                   float eps, float scale, int* err) {
+  // the layout below, from a base rounded up to 1024 bytes: refuse a launch
+  // that gave less (the same answer in every CTA: launch constants only)
+  constexpr u32 kNeed = 1023 + STAGES * STAGE_BYTES + 8 * (3 * STAGES + 1) + 4;
+  if (dynamic_smem_bytes() < kNeed) {
+    if (threadIdx.x == 0) atomicExch(err, 2);
+    return;
+  }
   extern __shared__ unsigned char smem_raw[];
   const u32 raw = smem_u32(smem_raw);
   const u32 base = (raw + 1023u) & ~1023u;  // tiles 1024-aligned for the swizzle
@@ -453,6 +466,15 @@ rms_linear_persistent(const __grid_constant__ TensorMap tmap_x,
                       const __grid_constant__ TensorMap tmap_w,
                       const __grid_constant__ TensorMap tmap_out, const u16* __restrict__ bias,
                       int m_tiles, float eps, float scale, int* err) {
+  // the layout below, from a base rounded up to 1024 bytes: refuse a launch
+  // that gave less.  Launch constants only, so both CTAs of a pair return
+  // together and neither waits for the other at the cluster barrier.
+  constexpr u32 kNeed =
+      1023 + PSTAGES * PSTAGE_BYTES + 2 * 128 * 4 + 4 * 2 * OUT_BLOCK + 8 * (3 * PSTAGES + 8) + 4;
+  if (dynamic_smem_bytes() < kNeed) {
+    if (threadIdx.x == 0) atomicExch(err, 2);
+    return;
+  }
   extern __shared__ unsigned char smem_raw[];
   const u32 raw = smem_u32(smem_raw);
   const u32 base = (raw + 1023u) & ~1023u;

@@ -166,7 +166,9 @@ int rmsnorm_linear_fold(const void* w, const void* gamma, void* w_out, int64_t N
                         fuse_dtype dt, void* stream);
 
 /* Synchronise the current device and return (and clear) the error word of
- * the kernels with bounded waits: 0, or nonzero if a wait ran out. */
+ * the kernels with bounded waits: 0; 1 if a wait ran out; 2 if a kernel was
+ * launched with less shared memory than its layout needs (it then returns
+ * before touching its barriers, TMA or TMEM). */
 int fuse_device_error(int* code);
 
 /* ------------------------------------------------------------------------
