@@ -46,7 +46,10 @@ constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int KT = KDIM / BK;
+// k-steps: the last one may run past K, where TMA fills zeros that add
+// nothing to the products or to the sum of squares (the persistent kernel;
+// the gamma path is only launched with K % 64 == 0)
+constexpr int KT = (KDIM + BK - 1) / BK;
 constexpr u32 TMEM_COLS = 256;
 constexpr u32 kMaxSpins = 1u << 22;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 8 * (3 * STAGES + 1) + 16;
@@ -450,7 +453,9 @@ __device__ __forceinline__ void st_shared16(u32 addr, uint4 v) {
 // With an odd number of 128-row tiles the last pair's second tile lies past
 // M: that CTA loads no x, its rows are computed from stale shared memory and
 // never stored.
-constexpr int NT_TILES = NDIM / BN;
+// column blocks: the last one may run past N; its w rows beyond N load as
+// zeros and its output columns beyond N are clipped by the TMA store
+constexpr int NT_TILES = (NDIM + BN - 1) / BN;
 constexpr int B_HALF = B_BYTES / 2;
 constexpr int PSTAGE_BYTES = A_BYTES + B_HALF;  // per CTA and stage
 constexpr int NACC = PAIR_NACC;                 // accumulator buffers in TMEM
@@ -598,10 +603,12 @@ rms_linear_persistent(const __grid_constant__ TensorMap tmap_x,
             tmem_ld32(tmem + b * TMEM_COLS + ((u32)(q * 32) << 16) + c * 32, acc);
             u32 bw[16];
             if constexpr (HAS_BIAS) {
+              // N % 8 == 0: each 8-value vector lies wholly inside or past N
               const uint4* bp = reinterpret_cast<const uint4*>(bias + n0 + c * 32);
 #pragma unroll
               for (int v = 0; v < 4; ++v) {
-                const uint4 t4 = __ldg(bp + v);
+                const uint4 t4 =
+                    n0 + c * 32 + 8 * v < NDIM ? __ldg(bp + v) : make_uint4(0u, 0u, 0u, 0u);
                 bw[4 * v] = t4.x; bw[4 * v + 1] = t4.y; bw[4 * v + 2] = t4.z; bw[4 * v + 3] = t4.w;
               }
             }

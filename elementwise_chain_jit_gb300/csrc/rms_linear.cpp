@@ -131,12 +131,22 @@ extern "C" int rmsnorm_linear(const void* x, const void* gamma, const void* w, c
   if (dt != FUSE_F16 && dt != FUSE_BF16)
     return fail(FUSE_E_DTYPE, "rmsnorm_linear runs on the tensor cores: f16 or bf16 only");
   if (M < 0 || N < 0 || K < 0) return fail(FUSE_E_SHAPE, "negative size");
-  if (M % kBM || N % kBN || K % kBK || K == 0)
-    return fail(FUSE_E_SHAPE, fmt("need M %% %d == 0, N %% %d == 0, K %% %d == 0 and K > 0 "
-                                  "(got M %lld, N %lld, K %lld)",
-                                  kBM, kBN, kBK, (long long)M, (long long)N, (long long)K));
-  if (M / kBM > 65535 || K > (int64_t(1) << 20) || (M / kBM) * (N / kBN) > INT32_MAX)
-    return fail(FUSE_E_SHAPE, "M, K or the tile count too large");
+  if (gamma == nullptr) {
+    // TMA takes the ragged edges: rows and columns past the tensors load as
+    // zeros and are clipped on store; its row strides must be multiples of 16
+    // bytes
+    if (N % 8 || K % 8 || K == 0)
+      return fail(FUSE_E_SHAPE, fmt("need N %% 8 == 0, K %% 8 == 0 and K > 0 (got N %lld, K %lld)",
+                                    (long long)N, (long long)K));
+  } else if (M % kBM || N % kBN || K % kBK || K == 0 || M / kBM > 65535) {
+    return fail(FUSE_E_SHAPE,
+                fmt("with gamma given: need M %% %d == 0 (M <= %d), N %% %d == 0, K %% %d == 0 "
+                    "and K > 0 (got M %lld, N %lld, K %lld); fold gamma into w for other shapes",
+                    kBM, 65535 * kBM, kBN, kBK, (long long)M, (long long)N, (long long)K));
+  }
+  const int64_t m_tiles64 = (M + kBM - 1) / kBM, n_tiles = (N + kBN - 1) / kBN;
+  if (K > (int64_t(1) << 20) || m_tiles64 * n_tiles > INT32_MAX)
+    return fail(FUSE_E_SHAPE, "K or the tile count too large");
   if (!(eps >= 0.f) || !std::isfinite(scale)) return fail(FUSE_E_ARG, "bad eps or scale");
   if (M == 0 || N == 0) return FUSE_OK;
   if (!x || !w || !out) return fail(FUSE_E_NULL, "NULL tensor pointer");
@@ -182,8 +192,8 @@ extern "C" int rmsnorm_linear(const void* x, const void* gamma, const void* w, c
     }
     alignas(64) CUtensorMap mo;
     if (int rc = encode_out(api, &mo, out, dt, M, N)) return rc;
-    int m_tiles = static_cast<int>(M / kBM);
-    const int64_t runs = (M / kBM + 1) / 2 * ((N / kBN + kPairRun - 1) / kPairRun);
+    int m_tiles = static_cast<int>(m_tiles64);
+    const int64_t runs = (m_tiles64 + 1) / 2 * ((n_tiles + kPairRun - 1) / kPairRun);
     const unsigned grid = 2u * static_cast<unsigned>(std::min<int64_t>(runs, clusters));
     void* args[] = {&mx, &mw, &mo, &bias, &m_tiles, &eps, &scale, &err};
     r = api->LaunchKernel(fn, grid, 1, 1, 320, 1, 1, smem, reinterpret_cast<CUstream>(stream), args,

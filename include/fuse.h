@@ -147,12 +147,14 @@ int rmsnorm_residual(const void* x, const void* residual, const void* weight, vo
  *   s_m = 1 / sqrt(sum_k x[m,k]^2 / K + eps)
  *   out[m, n] = scale * (s_m * sum_k (x[m,k] * gamma[k]) * w[n,k] + bias[n])
  * x [M, K], gamma [K], w [N, K] (K-major, the layout of a Linear weight),
- * bias [N] (may be NULL), out [M, N]; dt f16 or bf16 (accumulation fp32).
- * M % 128 == 0, N % 256 == 0, K % 64 == 0, all tensors 16-byte aligned.
+ * bias [N] (may be NULL), out [M, N]; dt f16 or bf16 (accumulation fp32);
+ * all tensors 16-byte aligned.
  * gamma NULL means gamma is already folded into w (rmsnorm_linear_fold): the
- * fast path, where the tensor cores consume the tiles as they arrive.  With
- * gamma given, x * gamma is formed (rounded to dt) on the tiles in shared
- * memory before each product.  Every wait inside the kernel is bounded: a
+ * fast path, where the tensor cores consume the tiles as they arrive; any
+ * M >= 0, N % 8 == 0, K % 8 == 0 (K > 0).  With gamma given, x * gamma is
+ * formed (rounded to dt) on the tiles in shared memory before each product,
+ * about 4x slower; that path needs M % 128 == 0 (M <= 65535 * 128),
+ * N % 256 == 0 and K % 64 == 0.  FUSE_E_SHAPE otherwise.  Every wait inside the kernel is bounded: a
  * wait that runs out records an error that fuse_device_error() reports
  * instead of hanging the device.
  */

@@ -54,9 +54,13 @@ def test_full_size_sampled_rows():
 
 
 def test_rejects_unsupported_shapes_and_dtypes():
-    with pytest.raises(F.FuseError) as e:
+    with pytest.raises(F.FuseError) as e:  # gamma given: whole tiles only
         F.rmsnorm_linear(256, 256, 256, 256, 256, 1e-6, 1.0, F.BF16, M=100, N=256, K=64)
     assert e.value.code == -2
+    for N, K in ((260, 64), (256, 60)):  # gamma folded: TMA strides of 16 bytes
+        with pytest.raises(F.FuseError) as e:
+            F.rmsnorm_linear(256, None, 256, 256, 256, 1e-6, 1.0, F.BF16, M=128, N=N, K=K)
+        assert e.value.code == -2
     with pytest.raises(F.FuseError) as e:
         F.rmsnorm_linear(256, 256, 256, 256, 256, 1e-6, 1.0, F.F32, M=128, N=256, K=64)
     assert e.value.code == -3
@@ -103,3 +107,11 @@ def test_folded_many_tiles_per_cta(bias):
     # persistent kernel takes several tiles, so both TMEM accumulator buffers
     # and both phases of their barriers are reused; every row is checked
     _folded_case(10240, 2048, 128, F.BF16, 60, bias=bias)
+
+
+@pytest.mark.parametrize("M,N,K,dt", [(1, 8, 8, F.BF16), (50, 264, 72, F.BF16),
+                                      (1000, 520, 200, F.F16), (130, 256, 4104, F.BF16)])
+def test_folded_ragged_shapes(M, N, K, dt):
+    # rows, columns and k-steps past the tensors: zeros on load, clipped on
+    # store (the output's canaries catch a store past M * N)
+    _folded_case(M, N, K, dt, 70 + M % 13)
