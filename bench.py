@@ -446,6 +446,33 @@ def time_fn(fn, reps=5, warm=2):
     return statistics.median(ts)
 
 
+def graph_per_launch(fn, k=20):
+    """Device time per launch of fn, from k launches captured into one library
+    graph and replayed once (no host cost between launches)."""
+    import torch
+
+    import elementwise_chain_jit_gb300 as F
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fn()
+    s.synchronize()
+    F.fuse_graph_begin(s)
+    with torch.cuda.stream(s):
+        for _ in range(k):
+            fn()
+    g = F.fuse_graph_end(s)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        g.launch(s)
+        s.synchronize()
+        a.record(s)
+        g.launch(s)
+        b.record(s)
+        b.synchronize()
+    g.release()
+    return a.elapsed_time(b) / k
+
+
 def graph_times(item, k=50):
     """Launch overhead of a small workload ("DeepJIT" section 6.1's per-op /
     CUDA graph / fused comparison): mean time per pass over k passes of
@@ -795,6 +822,26 @@ def run_gpu(args):
             d.update({"us_cublas_gemm_only": gms * 1e3, "fused_vs_cublas_gemm": gms / rms})
         next_rows[rl.name] = d
         del rl
+    # the chain sweep's smaller sizes (beside the step, not in it): 2^24 + 7
+    # elements (inputs larger than L2) and 2^20 + 7 (L2-resident across
+    # launches), 20 launches replayed from one graph
+    size_sweep = {}
+    if args.only is None and args.spec is None and args.flat_elems is None:
+        import workloads as W
+        for n in (W.FLAT_SIZES[3], W.FLAT_SIZES[1]):
+            for L in W.CHAIN_LENGTHS:
+                spec, dt = W.random_chain(L, 5)
+                c = F.fuse_compile(spec, (n,), dt)
+                ins = [W.device_uniform(n, -2.0, 2.0, 300 + L * 7 + j, d, dev)
+                       for j, d in enumerate(c.in_dtypes)]
+                out = torch.empty(n, dtype=_tdt(c.out_dtype), device=dev)
+                nb = sum(n * _esz(d) for d in c.in_dtypes) + n * _esz(c.out_dtype)
+                ms = graph_per_launch(lambda: F.fuse_launch(c, ins, out), k=20)
+                size_sweep[f"flat_chain_L{L}_n{n}"] = {
+                    "bytes": nb, "us_fused": ms * 1e3, "gbs": nb / (ms / 1e3) / 1e9,
+                    "frac_of_" + peak_kind + "_peak": nb / (ms / 1e3) / 1e9 / peak,
+                    "l2": "larger than L2" if nb > 129e6 else "L2-resident across reps"}
+                del ins, out
     # dominant kernel and its roofline
     dom = max(range(nitem), key=lambda i: per_item[i])
     dit = items[dom]
@@ -890,7 +937,7 @@ def run_gpu(args):
                              f"{step_bytes / 1e9:.1f} GB, evicting the small workloads' buffers",
                        "storage_dtypes": "f32/f16/bf16 per workload, arithmetic in f32"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clk, "per_chain": per_chain, "next_rows": next_rows,
+            "clocks": clk, "per_chain": per_chain, "next_rows": next_rows, "size_sweep": size_sweep,
             "partial": ({"only": args.only, "flat_elems": args.flat_elems, "spec": args.spec}
                         if args.only or args.flat_elems or args.spec else None),
             "frac_of_peak": value / world / peak, "peak_gbs": peak}
