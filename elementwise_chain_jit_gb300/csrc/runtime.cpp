@@ -263,12 +263,25 @@ std::vector<std::string> nvrtc_options() {
   if (const char* e = getenv("FUSE_LINEINFO"); e && *e == '1') o.push_back("-lineinfo");
   if (const char* e = getenv("FUSE_PTXAS_VERBOSE"); e && *e == '1')
     o.push_back("--ptxas-options=-v");
+  // extra NVRTC options, space-separated (part of the cache key like the rest)
+  if (const char* e = getenv("FUSE_NVRTC_OPTIONS"); e && *e) {
+    std::string all(e), cur;
+    for (char c : all + " ") {
+      if (c == ' ') {
+        if (!cur.empty()) o.push_back(cur);
+        cur.clear();
+      } else {
+        cur += c;
+      }
+    }
+  }
   return o;
 }
 
 // Optional on-disk cache of cubins (FUSE_CACHE_DIR): file name is the hash
 // of the full key; the file holds the key length and a second hash so that
-// a collision is detected rather than loaded.
+// a collision is detected rather than loaded, and a hash of the cubin so that
+// a damaged file is recompiled rather than handed to the driver.
 std::string disk_path(const std::string& key) {
   const char* dir = getenv("FUSE_CACHE_DIR");
   if (!dir || !*dir) return {};
@@ -277,8 +290,17 @@ std::string disk_path(const std::string& key) {
 
 struct DiskHeader {
   char magic[8];
-  uint64_t key_len, key_hash2, cubin_len;
+  uint64_t key_len, key_hash2, cubin_len, cubin_hash;
 };
+
+uint64_t bytes_hash(const std::vector<char>& v) {
+  uint64_t h = 1469598103934665603ull;
+  for (char c : v) {
+    h ^= static_cast<unsigned char>(c);
+    h *= 1099511628211ull;
+  }
+  return h;
+}
 
 uint64_t hash2(const std::string& key) { return fnv1a("salt:" + key + ":salt"); }
 
@@ -289,10 +311,16 @@ bool disk_load(const std::string& key, std::vector<char>* cubin) {
   if (!f) return false;
   DiskHeader h;
   if (!f.read(reinterpret_cast<char*>(&h), sizeof h)) return false;
-  if (memcmp(h.magic, "FUSECUB1", 8) != 0 || h.key_len != key.size() || h.key_hash2 != hash2(key))
+  if (memcmp(h.magic, "FUSECUB2", 8) != 0 || h.key_len != key.size() || h.key_hash2 != hash2(key) ||
+      h.cubin_len == 0 || h.cubin_len > (uint64_t(1) << 30))
     return false;
   cubin->resize(h.cubin_len);
-  return static_cast<bool>(f.read(cubin->data(), static_cast<std::streamsize>(h.cubin_len)));
+  if (!f.read(cubin->data(), static_cast<std::streamsize>(h.cubin_len)) ||
+      bytes_hash(*cubin) != h.cubin_hash) {
+    cubin->clear();
+    return false;
+  }
+  return true;
 }
 
 void disk_store(const std::string& key, const std::vector<char>& cubin) {
@@ -302,10 +330,11 @@ void disk_store(const std::string& key, const std::vector<char>& cubin) {
   std::ofstream f(tmp, std::ios::binary);
   if (!f) return;  // unwritable cache directory: keep going without it
   DiskHeader h;
-  memcpy(h.magic, "FUSECUB1", 8);
+  memcpy(h.magic, "FUSECUB2", 8);
   h.key_len = key.size();
   h.key_hash2 = hash2(key);
   h.cubin_len = cubin.size();
+  h.cubin_hash = bytes_hash(cubin);
   f.write(reinterpret_cast<const char*>(&h), sizeof h);
   f.write(cubin.data(), static_cast<std::streamsize>(cubin.size()));
   f.close();
@@ -330,7 +359,8 @@ int jit_compile(const std::string& source, const std::string& name, std::shared_
   auto m = std::make_shared<Module>();
   m->name = name;
   auto t0 = std::chrono::steady_clock::now();
-  if (!disk_load(key, &m->cubin)) {
+  const bool from_disk = disk_load(key, &m->cubin);
+  if (!from_disk) {
     if (const char* e = getenv("FUSE_VERBOSE"); e && *e == '1')
       fprintf(stderr, "[fuse] compiling %s:\n%s\n", name.c_str(), source.c_str());
     std::vector<const char*> hdr_text, hdr_name;
@@ -366,7 +396,8 @@ int jit_compile(const std::string& source, const std::string& name, std::shared_
       fprintf(stderr, "[fuse] %s:\n%s\n", name.c_str(), m->log.c_str());
   }
   double ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
-  stat_compile(ms);
+  if (from_disk) stat_hit();  // a disk load counts as a cache hit, not a compile
+  else stat_compile(ms);
   g_cache.emplace(key, m);
   *out = m;
   return FUSE_OK;

@@ -288,7 +288,14 @@ int fuse_graph_release(fuse_graph_handle g);
  * FUSE_E_COMPILE it holds the NVRTC log. */
 const char* fuse_last_error(void);
 
-/* Process-wide counters since load (any pointer may be NULL). */
+/* Process-wide counters since load (any pointer may be NULL): NVRTC
+ * compiles and their total time, cache hits (in memory, or a CUBIN loaded
+ * from FUSE_CACHE_DIR), kernel launches.
+ * Environment: FUSE_CACHE_DIR (on-disk CUBIN cache; each file carries hashes
+ * of its key and of the CUBIN, a damaged or foreign file is recompiled;
+ * an unwritable directory is ignored), FUSE_NVRTC_OPTIONS (extra NVRTC
+ * options, space-separated, part of the cache key), FUSE_VERBOSE=1 (print
+ * generated sources), FUSE_PTXAS_VERBOSE=1 (register use per kernel). */
 int fuse_stats(int64_t* compiles, int64_t* cache_hits, int64_t* launches, double* compile_ms);
 
 /* Number of SMs the library sizes persistent grids for on the current
