@@ -133,6 +133,7 @@ struct ChainPlan {
   bool vec_ok = false;
   int64_t C = 1, HW = 1;
   bool dynamic = false;  // shape bucket: the leading dimension comes with the launch
+  bool debug = false;    // FUSE_DEBUG_BOUNDS: every index checked against its tensor
   int64_t inner = 1;     // elements per unit of the leading dimension
   std::string source;
 };
@@ -209,6 +210,7 @@ int plan_chain(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_d
     else break;
   }
   p->vec_ok = !ch.groups || (p->HW % p->vec == 0);
+  p->debug = env_int("FUSE_DEBUG_BOUNDS", 0) == 1;
   return FUSE_OK;
 }
 
@@ -266,7 +268,18 @@ static std::string gen_chain_source(const ChainPlan& p, const char* spec) {
   }
   s << "constexpr int DTO = " << ch.out_dt << ";  // " << dtype_name(ch.out_dt) << "\n";
   s << "constexpr int NWO = VEC * Dt<DTO>::bytes / 4;\n";
-  if (p.dynamic) {
+  if (p.debug) {
+    // debug bounds checks: the launch always passes the element count and
+    // the device error word; an index outside its tensor records code 3
+    // there and the access is skipped
+    s << "struct Args { const void* in[NIN]; void* out; long long n; int* err; };\n";
+    s << (p.dynamic ? "#define SIZE_N(a) ((a).n)\n" : "#define SIZE_N(a) N\n");
+    s << "__device__ __forceinline__ bool in_bounds(const Args& a, long long i, long long lim) {\n"
+         "  if (i >= 0 && i < lim) return true;\n"
+         "  atomicExch(a.err, 3);\n"
+         "  return false;\n"
+         "}\n\n";
+  } else if (p.dynamic) {
     // shape bucket: N above is the largest element count; the launch passes
     // the actual one
     s << "struct Args { const void* in[NIN]; void* out; long long n; };\n";
@@ -318,6 +331,8 @@ static std::string gen_chain_source(const ChainPlan& p, const char* spec) {
 
   // scalar chain for one element (tail and fallback kernel)
   s << "\n__device__ __forceinline__ void apply_elem(const Args& a, idx_t e) {\n";
+  if (p.debug)  // every access below is at e (inputs 1.., output) or src_elem(e) (input 0)
+    s << "  if (!in_bounds(a, e, SIZE_N(a)) || !in_bounds(a, src_elem(e), SIZE_N(a))) return;\n";
   if (p.copy) {
     s << "  static_cast<typename Dt<DTO>::storage*>(a.out)[e] =\n"
          "      static_cast<const typename Dt<DT0>::storage*>(a.in[0])[src_elem(e)];\n}\n";
@@ -333,16 +348,20 @@ static std::string gen_chain_source(const ChainPlan& p, const char* spec) {
     s << "template <bool CHECK>\n__device__ __forceinline__ void do_chunk(const Args& a, idx_t v0, "
          "idx_t nvec) {\n";
     for (int j = 0; j < nin; ++j) s << "  u32 r" << j << "[UNROLL][NW" << j << "];\n";
+    // debug: a vector whose index or source index falls outside the
+    // tensors is neither loaded nor stored
+    const char* dbg = p.debug ? "    if (!in_bounds(a, v, nvec) || !in_bounds(a, src_vec(v), nvec)) continue;\n"
+                              : "";
     s << "#pragma unroll\n  for (int u = 0; u < UNROLL; ++u) {\n"
          "    const idx_t v = v0 + (idx_t)u * BLOCK;\n"
-         "    if (CHECK && v >= nvec) break;\n";
+         "    if (CHECK && v >= nvec) break;\n" << dbg;
     for (int j = 0; j < nin; ++j) {
       s << "    load_words(static_cast<const u32*>(a.in[" << j << "]) + (idx_t)"
         << (j == 0 ? "src_vec(v)" : "v") << " * NW" << j << ", r" << j << "[u]);\n";
     }
     s << "  }\n#pragma unroll\n  for (int u = 0; u < UNROLL; ++u) {\n"
          "    const idx_t v = v0 + (idx_t)u * BLOCK;\n"
-         "    if (CHECK && v >= nvec) break;\n"
+         "    if (CHECK && v >= nvec) break;\n" << dbg <<
          "    u32 wo[NWO];\n    apply(";
     for (int j = 0; j < nin; ++j) s << "r" << j << "[u], ";
     s << "wo);\n    store_words(static_cast<u32*>(a.out) + v * NWO, wo);\n  }\n}\n";
@@ -487,11 +506,17 @@ int chain_launch(fuse_chain* h, const void* const* inputs, int n_in, void* outpu
   if (int rc = current_device(&d)) return rc;
   fuse_chain::PerDevice* pd;
   if (int rc = chain_device_state(h, d, &pd)) return rc;
-  // kernel parameter: the Args struct {in[NIN], out[, n]} as 8-byte words
-  std::vector<uint64_t> args(static_cast<size_t>(nin) + 2);
+  // kernel parameter: the Args struct {in[NIN], out[, n][, err]} as 8-byte
+  // words (the debug build always has n, then the device error word)
+  std::vector<uint64_t> args(static_cast<size_t>(nin) + 3);
   for (int j = 0; j < nin; ++j) args[j] = reinterpret_cast<uintptr_t>(inputs[j]);
   args[nin] = reinterpret_cast<uintptr_t>(output);
   args[nin + 1] = static_cast<uint64_t>(n);
+  if (p.debug) {
+    CUdeviceptr err;
+    if (int rc = device_error_word(d.ordinal, &err)) return rc;
+    args[nin + 2] = static_cast<uint64_t>(err);
+  }
   void* kargs[] = {args.data()};
   unsigned vec_grid, scalar_grid;
   chain_grids(p, *pd, n, &vec_grid, &scalar_grid);

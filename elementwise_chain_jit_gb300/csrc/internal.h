@@ -117,6 +117,13 @@ int jit_function(Module& m, const char* fn_name, const DeviceInfo& dev, CUfuncti
 // Launch on `stream` and count it.
 int launch(CUfunction fn, unsigned grid, unsigned block, unsigned smem, void* stream, void** args);
 
+// The device's error word (allocated on first use): kernels with bounded
+// waits or debug bounds checks write a nonzero code there instead of
+// trapping; fuse_device_error() reads and clears it.
+//   1 a bounded wait ran out, 2 too little shared memory for the layout,
+//   3 an index outside its tensor (FUSE_DEBUG_BOUNDS)
+int device_error_word(int device, CUdeviceptr* out);
+
 // ------------------------------------------------------------------ helpers
 int dtype_bytes(fuse_dtype dt);
 const char* dtype_name(fuse_dtype dt);

@@ -31,7 +31,6 @@ struct RlKernel {
 
 std::mutex g_mu;
 std::map<std::tuple<int64_t, int64_t, int, int, int>, RlKernel> g_kernels;
-CUdeviceptr g_err[64];  // per-device error word of the kernels' bounded waits
 
 int rl_kernel(int64_t K, int64_t N, fuse_dtype dt, bool has_bias, bool apply_gamma, RlKernel* out) {
   auto key = std::make_tuple(K, N, static_cast<int>(dt), has_bias ? 1 : 0, apply_gamma ? 1 : 0);
@@ -83,18 +82,6 @@ int encode_out(const DriverApi* api, CUtensorMap* map, void* ptr, fuse_dtype dt,
       ptr, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
       CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail(r, "cuTensorMapEncodeTiled(out)");
-  return FUSE_OK;
-}
-
-int error_word(const DriverApi* api, int device, CUdeviceptr* out) {
-  if (!g_err[device]) {
-    CUdeviceptr p;
-    CUresult r = api->MemAlloc(&p, 16);
-    if (r != CUDA_SUCCESS) return cuda_fail(r, "cuMemAlloc(error word)");
-    if ((r = api->MemsetD32(p, 0, 4)) != CUDA_SUCCESS) return cuda_fail(r, "cuMemsetD32");
-    g_err[device] = p;
-  }
-  *out = g_err[device];
   return FUSE_OK;
 }
 
@@ -171,10 +158,7 @@ extern "C" int rmsnorm_linear(const void* x, const void* gamma, const void* w, c
                             &fn))
     return rc;
   CUdeviceptr err;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (int rc = error_word(api, d.ordinal, &err)) return rc;
-  }
+  if (int rc = device_error_word(d.ordinal, &err)) return rc;
   const int smem = persistent ? 1024 + kPairStages * (kBM + kBN / 2) * kBK * 2 + 2 * 128 * 4 +
                                     4 * 2 * kOutBox * kOutBox * 2 + 8 * (3 * kPairStages + 8) + 16
                               : k.smem;
@@ -230,23 +214,4 @@ extern "C" int rmsnorm_linear_fold(const void* w, const void* gamma, void* w_out
   void* args[] = {&w, &gamma, &w_out, &total};
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(d.sms * 8LL, (total + 255) / 256));
   return launch(fn, grid, 256, 0, stream, args);
-}
-
-extern "C" int fuse_device_error(int* code) {
-  using namespace fuse;
-  if (!code) return fail(FUSE_E_NULL, "code is NULL");
-  *code = 0;
-  DeviceInfo d;
-  if (int rc = current_device(&d)) return rc;
-  const DriverApi* api;
-  if (int rc = driver(&api)) return rc;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_err[d.ordinal]) return FUSE_OK;
-  CUresult r = api->CtxSynchronize();
-  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuCtxSynchronize");
-  if ((r = api->MemcpyDtoH(code, g_err[d.ordinal], 4)) != CUDA_SUCCESS)
-    return cuda_fail(r, "cuMemcpyDtoH(error word)");
-  if ((r = api->MemsetD32(g_err[d.ordinal], 0, 4)) != CUDA_SUCCESS)
-    return cuda_fail(r, "cuMemsetD32(error word)");
-  return FUSE_OK;
 }

@@ -442,3 +442,47 @@ int launch(CUfunction fn, unsigned grid, unsigned block, unsigned smem, void* st
 }
 
 }  // namespace fuse
+
+// ------------------------------------------------------------------ device error word
+
+namespace fuse {
+namespace {
+std::mutex g_err_mu;
+CUdeviceptr g_err_words[64];  // per device; set by kernels, read by fuse_device_error
+}  // namespace
+
+int device_error_word(int device, CUdeviceptr* out) {
+  if (device < 0 || device >= 64) return fail(FUSE_E_ARG, "device ordinal out of range");
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_words[device]) {
+    const DriverApi* api;
+    if (int rc = driver(&api)) return rc;
+    CUdeviceptr p;
+    CUresult r = api->MemAlloc(&p, 16);
+    if (r != CUDA_SUCCESS) return cuda_fail(r, "cuMemAlloc(error word)");
+    if ((r = api->MemsetD32(p, 0, 4)) != CUDA_SUCCESS) return cuda_fail(r, "cuMemsetD32");
+    g_err_words[device] = p;
+  }
+  *out = g_err_words[device];
+  return FUSE_OK;
+}
+}  // namespace fuse
+
+extern "C" int fuse_device_error(int* code) {
+  using namespace fuse;
+  if (!code) return fail(FUSE_E_NULL, "code is NULL");
+  *code = 0;
+  DeviceInfo d;
+  if (int rc = current_device(&d)) return rc;
+  const DriverApi* api;
+  if (int rc = driver(&api)) return rc;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_words[d.ordinal]) return FUSE_OK;
+  CUresult r = api->CtxSynchronize();
+  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuCtxSynchronize");
+  if ((r = api->MemcpyDtoH(code, g_err_words[d.ordinal], 4)) != CUDA_SUCCESS)
+    return cuda_fail(r, "cuMemcpyDtoH(error word)");
+  if ((r = api->MemsetD32(g_err_words[d.ordinal], 0, 4)) != CUDA_SUCCESS)
+    return cuda_fail(r, "cuMemsetD32(error word)");
+  return FUSE_OK;
+}

@@ -167,10 +167,11 @@ int rmsnorm_linear(const void* x, const void* gamma, const void* w, const void* 
 int rmsnorm_linear_fold(const void* w, const void* gamma, void* w_out, int64_t N, int64_t K,
                         fuse_dtype dt, void* stream);
 
-/* Synchronise the current device and return (and clear) the error word of
- * the kernels with bounded waits: 0; 1 if a wait ran out; 2 if a kernel was
- * launched with less shared memory than its layout needs (it then returns
- * before touching its barriers, TMA or TMEM). */
+/* Synchronise the current device and return (and clear) its error word: 0;
+ * 1 if a bounded wait ran out; 2 if a kernel was launched with less shared
+ * memory than its layout needs (it then returns before touching its barriers,
+ * TMA or TMEM); 3 if a chain built with FUSE_DEBUG_BOUNDS met an index
+ * outside its tensor. */
 int fuse_device_error(int* code);
 
 /* ------------------------------------------------------------------------
@@ -295,7 +296,10 @@ const char* fuse_last_error(void);
  * of its key and of the CUBIN, a damaged or foreign file is recompiled;
  * an unwritable directory is ignored), FUSE_NVRTC_OPTIONS (extra NVRTC
  * options, space-separated, part of the cache key), FUSE_VERBOSE=1 (print
- * generated sources), FUSE_PTXAS_VERBOSE=1 (register use per kernel). */
+ * generated sources), FUSE_PTXAS_VERBOSE=1 (register use per kernel),
+ * FUSE_DEBUG_BOUNDS=1 (chains compiled from then on check every index against
+ * its tensor before the access and record code 3 in the device error word,
+ * skipping the access, instead of touching memory outside the tensors). */
 int fuse_stats(int64_t* compiles, int64_t* cache_hits, int64_t* launches, double* compile_ms);
 
 /* Number of SMs the library sizes persistent grids for on the current

@@ -248,3 +248,42 @@ def test_launch_count_is_one_per_chain():
     after = F.fuse_stats()
     assert after["launches"] - before["launches"] == 5
     assert after["compiles"] == before["compiles"]
+
+
+# ------------------------------------------------------------ debug bounds checks
+
+@pytest.mark.parametrize("spec,dt,shape,offset", [
+    ("add;relu;scale:0.5", F.F32, ((1 << 20) + 7,), 0),   # vector chunks, remainder, tail
+    ("mul;exp;cast:f16", F.F32, (4099,), 1),              # scalar kernel (misaligned)
+    ("shuffle:4;sigmoid;add", F.F16, (2, 16, 8, 8), 0),   # shuffled vectors
+    ("shuffle:3;relu", F.F16, (1, 12, 3, 5), 0),          # shuffled, scalar (HW % VEC != 0)
+])
+def test_debug_bounds_build_matches_and_reports_nothing(monkeypatch, spec, dt, shape, offset):
+    # FUSE_DEBUG_BOUNDS=1 compiles an index check before every load and
+    # store; on correct launches the results are unchanged and the device
+    # error word stays 0
+    monkeypatch.setenv("FUSE_DEBUG_BOUNDS", "1")
+    assert "in_bounds(" in F.fuse_source(spec, shape, dt)
+    n = int(np.prod(shape))
+    inputs, _ = workloads.chain_inputs(spec, dt, n, 41)
+    F.fuse_device_error()  # clear
+    got, _ = _run_chain(spec, dt, inputs, shape, offset=offset)
+    assert F.fuse_device_error() == 0
+    _check(spec, dt, inputs, shape, got)
+
+
+def test_debug_bounds_bucket_launch(monkeypatch):
+    monkeypatch.setenv("FUSE_DEBUG_BOUNDS", "1")
+    spec, dt, shape = "shuffle:4;add;sigmoid", F.F16, (8, 16, 7, 7)
+    c = F.fuse_compile_bucket(spec, shape, dt)
+    inner, full = int(np.prod(shape[1:])), int(np.prod(shape))
+    inputs, _ = workloads.chain_inputs(spec, dt, full, 43)
+    dev = [to_dev(a, d) for a, d in zip(inputs, c.in_dtypes)]
+    F.fuse_device_error()
+    for rows in (1, 3, 8):
+        n = rows * inner
+        out = Guarded(n, c.out_dtype)
+        F.fuse_launch_rows(c, dev, out.t, rows)
+        torch.cuda.synchronize()
+        assert out.canary_ok() and F.fuse_device_error() == 0
+        _check(spec, dt, [a[:n] for a in inputs], (rows,) + shape[1:], to_host(out.t, c.out_dtype))

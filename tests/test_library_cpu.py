@@ -186,3 +186,14 @@ def test_chain_kernels_compile_without_spills(spec, shape, dt):
     assert "fuse_chain_vec" in r.stderr or "shuffle" in spec
     spills = re.findall(r"(\d+) bytes spill stores", r.stderr)
     assert spills and all(s == "0" for s in spills), r.stderr
+
+
+def test_debug_bounds_source(monkeypatch):
+    spec, shape = "shuffle:4;add;sigmoid", (2, 16, 8, 8)
+    assert "in_bounds(" not in F.fuse_source(spec, shape, F.F16)
+    monkeypatch.setenv("FUSE_DEBUG_BOUNDS", "1")
+    src = F.fuse_source(spec, shape, F.F16)
+    assert "struct Args { const void* in[NIN]; void* out; long long n; int* err; };" in src
+    assert src.count("in_bounds(a, v, nvec) || !in_bounds(a, src_vec(v), nvec)") == 2
+    assert "in_bounds(a, e, SIZE_N(a)) || !in_bounds(a, src_elem(e), SIZE_N(a))" in src
+    F.fuse_compile(spec, shape, F.F16)  # and it compiles
