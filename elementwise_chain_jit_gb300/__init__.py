@@ -31,7 +31,7 @@ EXPORTS = ["fuse_compile", "fuse_num_inputs", "fuse_input_dtypes", "fuse_launch"
            "fuse_bucket", "rmsnorm_linear", "rmsnorm_linear_fold", "fuse_device_error", "rmsnorm_residual", "layernorm_residual", "rope_qkv_split", "rope_qkv_split_noalloc",
            "detect_decode", "channel_shuffle", "fuse_graph_begin", "fuse_graph_end",
            "fuse_graph_launch", "fuse_graph_nodes", "fuse_graph_release", "fuse_last_error",
-           "fuse_stats", "fuse_device_sms"]
+           "fuse_stats", "fuse_device_sms", "fuse_selftest_bounded_wait"]
 
 
 class FuseError(RuntimeError):
@@ -78,6 +78,7 @@ _lib.fuse_last_error.restype = ctypes.c_char_p
 _lib.fuse_stats.argtypes = [ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64),
                             ctypes.POINTER(ctypes.c_double)]
 _lib.fuse_device_sms.argtypes = [ctypes.POINTER(_I)]
+_lib.fuse_selftest_bounded_wait.argtypes = [_I64, _P]
 
 
 def _check(rc: int) -> None:
@@ -382,3 +383,9 @@ def fuse_device_sms() -> int:
     s = _I()
     _check(_lib.fuse_device_sms(ctypes.byref(s)))
     return s.value
+
+
+def fuse_selftest_bounded_wait(spins: int, stream=None) -> None:
+    """Launch the bounded-wait self test (see include/fuse.h); afterwards
+    fuse_device_error() returns 1."""
+    _check(_lib.fuse_selftest_bounded_wait(int(spins), _stream(stream)))

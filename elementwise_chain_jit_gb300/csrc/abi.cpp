@@ -71,3 +71,43 @@ int channel_shuffle(const void* in, void* out, int64_t n, int64_t c, int64_t h, 
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ self test
+
+namespace {
+// one warp waits on an mbarrier that nothing arrives at, through the same
+// bounded wait as every wait in the library's kernels, and records code 1
+const char* kSelftestSource =
+    "#include \"fuse/sync.cuh\"\n"
+    "extern \"C\" __global__ void bounded_wait_selftest(unsigned spins, int* err) {\n"
+    "  __shared__ unsigned long long bar;\n"
+    "  const u32 b = smem_u32(&bar);\n"
+    "  if (threadIdx.x == 0) mbar_init(b, 1);\n"
+    "  __syncthreads();\n"
+    "  const bool ok = __all_sync(0xffffffffu, mbar_wait(b, 0, spins));\n"
+    "  if (!ok && threadIdx.x == 0) atomicExch(err, 1);\n"
+    "}\n";
+std::mutex g_selftest_mu;
+std::shared_ptr<fuse::Module> g_selftest;
+}  // namespace
+
+extern "C" int fuse_selftest_bounded_wait(int64_t spins, void* stream) {
+  using namespace fuse;
+  if (spins < 1 || spins > (int64_t(1) << 30)) return fail(FUSE_E_ARG, "spins outside 1..2^30");
+  std::shared_ptr<Module> mod;
+  {
+    std::lock_guard<std::mutex> lk(g_selftest_mu);
+    if (!g_selftest)
+      if (int rc = jit_compile(kSelftestSource, "bounded_wait_selftest", &g_selftest)) return rc;
+    mod = g_selftest;
+  }
+  DeviceInfo d;
+  if (int rc = current_device(&d)) return rc;
+  CUfunction fn;
+  if (int rc = jit_function(*mod, "bounded_wait_selftest", d, &fn)) return rc;
+  CUdeviceptr err;
+  if (int rc = device_error_word(d.ordinal, &err)) return rc;
+  unsigned sp = static_cast<unsigned>(spins);
+  void* args[] = {&sp, &err};
+  return launch(fn, 1, 32, 0, stream, args);
+}

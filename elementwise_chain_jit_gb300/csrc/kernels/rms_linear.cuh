@@ -32,6 +32,7 @@
 // for the sum of squares, and the MMA consumes the TMA tiles as they land.
 #pragma once
 #include "fuse/common.cuh"
+#include "fuse/sync.cuh"
 
 // w'[n, k] = dt(w[n, k] * gamma[k]): gamma folded into the weight once, so
 // that the tile loop needs no transform of the A operand.
@@ -51,57 +52,11 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 // the gamma path is only launched with K % 64 == 0)
 constexpr int KT = (KDIM + BK - 1) / BK;
 constexpr u32 TMEM_COLS = 256;
-constexpr u32 kMaxSpins = 1u << 22;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 8 * (3 * STAGES + 1) + 16;
 
 struct __align__(64) TensorMap {
   unsigned long long v[16];
 };
-
-__device__ __forceinline__ u32 dynamic_smem_bytes() {
-  u32 r;
-  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ u32 smem_u32(const void* p) {
-  u32 r;
-  asm("{ .reg .u64 t; cvta.to.shared.u64 t, %1; cvt.u32.u64 %0, t; }" : "=r"(r) : "l"(p));
-  return r;
-}
-
-// ---------------------------------------------------------------- mbarrier
-__device__ __forceinline__ void mbar_init(u32 bar, u32 count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(u32 bar, u32 bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(u32 bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(u32 bar, u32 parity) {
-  u32 ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// bounded: false when the phase did not complete within kMaxSpins tries
-__device__ __forceinline__ bool mbar_wait(u32 bar, u32 parity) {
-  for (u32 i = 0; i < kMaxSpins; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-// the same wait in all 32 lanes with one outcome for the warp: a lane that
-// gave up makes the whole warp give up, so the .aligned tcgen05 loads after
-// it are always executed by the full warp
-__device__ __forceinline__ bool mbar_wait_warp(u32 bar, u32 parity) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
-}
 
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(u32 dst, const TensorMap* map, u32 bar, int c0,

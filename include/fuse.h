@@ -174,6 +174,14 @@ int rmsnorm_linear_fold(const void* w, const void* gamma, void* w_out, int64_t N
  * outside its tensor. */
 int fuse_device_error(int* code);
 
+/* Exercise the failure path of the kernels' bounded waits: one warp waits
+ * on an mbarrier that nothing arrives at, gives up after `spins` tries
+ * (1..2^30; each kernel wait in the library uses 2^18, about a second) and
+ * records code 1 in
+ * the device error word, which fuse_device_error() then returns.  No fault,
+ * trap or hang: the kernel ends and the context stays usable. */
+int fuse_selftest_bounded_wait(int64_t spins, void* stream);
+
 /* ------------------------------------------------------------------------
  * Residual add + LayerNorm + cast ("DeepJIT", section 4.3: one block per
  * row, mean and variance reduced in the block, then normalised in the same
