@@ -287,3 +287,57 @@ def test_debug_bounds_bucket_launch(monkeypatch):
         torch.cuda.synchronize()
         assert out.canary_ok() and F.fuse_device_error() == 0
         _check(spec, dt, [a[:n] for a in inputs], (rows,) + shape[1:], to_host(out.t, c.out_dtype))
+
+
+# ------------------------------------------------------------ past 2^31 elements
+
+def _big_sample(n, seed):
+    # first and last elements, both sides of element 2^31, random positions;
+    # every index checked on the host to lie inside the tensor
+    g = np.random.default_rng(seed)
+    edge = 1 << 31
+    idx = np.unique(np.concatenate([np.arange(4096), np.arange(edge - 2048, min(edge + 2048, n)),
+                                    np.arange(n - 4096, n), g.integers(0, n, 100_000)]))
+    assert idx[0] >= 0 and idx[-1] < n
+    return idx
+
+
+def test_chain_past_2_to_the_31_elements():
+    # 64-bit index arithmetic (2^31 + 13 fp16 elements, 3 tensors of 4.3 GB)
+    if torch.cuda.mem_get_info()[0] < (40 << 30):
+        pytest.skip("needs 40 GB of free device memory")
+    n = (1 << 31) + 13
+    spec, dt = "add;relu;scale:0.5", F.F16
+    c = F.fuse_compile(spec, (n,), dt)
+    assert "typedef long long idx_t;" in F.fuse_source(spec, (n,), dt)
+    dev = [workloads.device_uniform(n, -2.0, 2.0, 77 + j, dt) for j in range(2)]
+    out = Guarded(n, dt)
+    F.fuse_launch(c, dev, out.t)
+    torch.cuda.synchronize()
+    assert out.canary_ok()
+    idx = _big_sample(n, 78)
+    it = torch.from_numpy(idx).cuda()
+    ins = [to_host(t[it], dt) for t in dev]
+    _check(spec, dt, ins, (len(idx),), to_host(out.t[it], dt))
+    del dev, out
+
+
+def test_shuffled_chain_past_2_to_the_31_elements():
+    # the shuffle's plane index in 64-bit arithmetic: [2676, 256, 56, 56] fp16
+    if torch.cuda.mem_get_info()[0] < (40 << 30):
+        pytest.skip("needs 40 GB of free device memory")
+    shape = (2676, 256, 56, 56)
+    n = int(np.prod(shape))
+    assert n > (1 << 31)
+    spec, dt = "shuffle:4;sigmoid", F.F16
+    c = F.fuse_compile(spec, shape, dt)
+    x = workloads.device_uniform(n, -2.0, 2.0, 79, dt)
+    out = Guarded(n, dt)
+    F.fuse_launch(c, [x], out.t)
+    torch.cuda.synchronize()
+    assert out.canary_ok()
+    idx = _big_sample(n, 80)
+    got = to_host(out.t[torch.from_numpy(idx).cuda()], dt)
+    host_x = to_host(x, dt)  # the oracle evaluates the sampled outputs from the whole input
+    del x
+    _check(spec, dt, [host_x], shape, got, idx=idx)
