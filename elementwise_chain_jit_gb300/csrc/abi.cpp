@@ -43,6 +43,7 @@ int fuse_device_sms(int* sms) {
 
 int channel_shuffle(const void* in, void* out, int64_t n, int64_t c, int64_t h, int64_t w,
                     int groups, fuse_dtype dt, void* stream) {
+  fuse::NvtxRange nvtx_range("channel_shuffle");
   using namespace fuse;
   if (!valid_dtype(dt)) return fail(FUSE_E_DTYPE, fmt("invalid dtype %d", dt));
   if (n < 0 || c < 0 || h < 0 || w < 0) return fail(FUSE_E_SHAPE, "negative dimension");

@@ -553,6 +553,7 @@ extern "C" {
 
 int fuse_compile(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dtype,
                  fuse_handle* out) {
+  fuse::NvtxRange nvtx_range("fuse_compile");
   if (!out) return fuse::fail(FUSE_E_NULL, "out is NULL");
   *out = nullptr;
   return fuse::chain_compile(spec, shape, ndim, in_dtype, out, false);
@@ -560,6 +561,7 @@ int fuse_compile(const char* spec, const int64_t* shape, int ndim, fuse_dtype in
 
 int fuse_compile_bucket(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dtype,
                         fuse_handle* out) {
+  fuse::NvtxRange nvtx_range("fuse_compile_bucket");
   if (!out) return fuse::fail(FUSE_E_NULL, "out is NULL");
   *out = nullptr;
   return fuse::chain_compile(spec, shape, ndim, in_dtype, out, true);
@@ -591,12 +593,14 @@ int fuse_input_dtypes(fuse_handle h, fuse_dtype* dts, int cap) {
 }
 
 int fuse_launch(fuse_handle h, const void* const* inputs, int n_in, void* output, void* stream) {
+  fuse::NvtxRange nvtx_range("fuse_launch");
   if (!h) return fuse::fail(FUSE_E_ARG, "NULL handle");
   return fuse::chain_launch(h, inputs, n_in, output, stream, -1);
 }
 
 int fuse_launch_rows(fuse_handle h, const void* const* inputs, int n_in, void* output,
                      int64_t rows, void* stream) {
+  fuse::NvtxRange nvtx_range("fuse_launch_rows");
   if (!h) return fuse::fail(FUSE_E_ARG, "NULL handle");
   if (rows < 0) return fuse::fail(FUSE_E_SHAPE, "rows < 0");
   return fuse::chain_launch(h, inputs, n_in, output, stream, rows);

@@ -105,6 +105,7 @@ int detect_kernel(const int* hw, const float* strides, const float* anchors, int
 extern "C" int detect_decode(const void* const* feats, const int* hw, const float* strides,
                              const float* anchors, int nscales, int na, int no, fuse_dtype in_dt,
                              void* out, void* stream) {
+  fuse::NvtxRange nvtx_range("detect_decode");
   using namespace fuse;
   if (!valid_dtype(in_dt)) return fail(FUSE_E_DTYPE, fmt("invalid dtype %d", in_dt));
   if (nscales < 1 || nscales > 8) return fail(FUSE_E_SHAPE, "nscales outside 1..8");

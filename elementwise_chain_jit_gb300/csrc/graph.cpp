@@ -56,6 +56,7 @@ int fuse_graph_end(void* stream, fuse_graph** out) {
 }
 
 int fuse_graph_launch(fuse_graph* g, void* stream) {
+  fuse::NvtxRange nvtx_range("fuse_graph_launch");
   using namespace fuse;
   if (!g || !g->exec) return fail(FUSE_E_ARG, "NULL graph");
   const DriverApi* api;

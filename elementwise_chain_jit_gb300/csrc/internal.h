@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdint>
 #include <memory>
@@ -123,6 +124,15 @@ int launch(CUfunction fn, unsigned grid, unsigned block, unsigned smem, void* st
 //   1 a bounded wait ran out, 2 too little shared memory for the layout,
 //   3 an index outside its tensor (FUSE_DEBUG_BOUNDS)
 int device_error_word(int device, CUdeviceptr* out);
+
+// A named range around an ABI call, for timeline profilers (NVTX v3,
+// header-only; a few nanoseconds when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // ------------------------------------------------------------------ helpers
 int dtype_bytes(fuse_dtype dt);

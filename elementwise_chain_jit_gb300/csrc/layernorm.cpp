@@ -77,6 +77,7 @@ int ln_kernel(int64_t hidden, fuse_dtype dt, int flags, LnKernel* out) {
 extern "C" int layernorm_residual(const void* x, const void* residual, const void* gamma,
                                   const void* beta, void* out, void* residual_out, int64_t rows,
                                   int64_t hidden, float eps, fuse_dtype dt, void* stream) {
+  fuse::NvtxRange nvtx_range("layernorm_residual");
   using namespace fuse;
   if (!valid_dtype(dt)) return fail(FUSE_E_DTYPE, fmt("invalid dtype %d", dt));
   if (rows < 0) return fail(FUSE_E_SHAPE, "rows < 0");

@@ -114,6 +114,7 @@ int max_clusters(const DriverApi* api, CUfunction fn, int smem, int* out) {
 extern "C" int rmsnorm_linear(const void* x, const void* gamma, const void* w, const void* bias,
                               void* out, int64_t M, int64_t N, int64_t K, float eps, float scale,
                               fuse_dtype dt, void* stream) {
+  fuse::NvtxRange nvtx_range("rmsnorm_linear");
   using namespace fuse;
   if (dt != FUSE_F16 && dt != FUSE_BF16)
     return fail(FUSE_E_DTYPE, "rmsnorm_linear runs on the tensor cores: f16 or bf16 only");
@@ -196,6 +197,7 @@ extern "C" int rmsnorm_linear(const void* x, const void* gamma, const void* w, c
 
 extern "C" int rmsnorm_linear_fold(const void* w, const void* gamma, void* w_out, int64_t N,
                                    int64_t K, fuse_dtype dt, void* stream) {
+  fuse::NvtxRange nvtx_range("rmsnorm_linear_fold");
   using namespace fuse;
   if (dt != FUSE_F16 && dt != FUSE_BF16) return fail(FUSE_E_DTYPE, "f16 or bf16 only");
   if (N < 0 || K < 1 || K > (int64_t(1) << 20)) return fail(FUSE_E_SHAPE, "bad N or K");

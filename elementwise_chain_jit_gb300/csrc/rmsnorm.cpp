@@ -60,6 +60,7 @@ int rms_kernel(int64_t hidden, fuse_dtype dt, RmsKernel* out) {
 extern "C" int rmsnorm_residual(const void* x, const void* residual, const void* weight, void* out,
                                 void* residual_out, int64_t rows, int64_t hidden, float eps,
                                 fuse_dtype dt, void* stream) {
+  fuse::NvtxRange nvtx_range("rmsnorm_residual");
   using namespace fuse;
   if (!valid_dtype(dt)) return fail(FUSE_E_DTYPE, fmt("invalid dtype %d", dt));
   if (rows < 0) return fail(FUSE_E_SHAPE, "rows < 0");

@@ -127,6 +127,7 @@ int rope_table(const DeviceInfo& d, float base, int hd, int64_t need, CUdevicept
 extern "C" int rope_qkv_split(const void* qkv, void* q, void* k, void* v, int64_t tokens,
                               int heads, int head_dim, int64_t pos0, float base, fuse_dtype dt,
                               void* stream) {
+  fuse::NvtxRange nvtx_range("rope_qkv_split");
   using namespace fuse;
   if (!valid_dtype(dt)) return fail(FUSE_E_DTYPE, fmt("invalid dtype %d", dt));
   if (tokens < 0 || heads < 1 || head_dim < 2 || head_dim > 1024 || head_dim % 2)
