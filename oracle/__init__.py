@@ -139,22 +139,31 @@ def parse_spec(spec: str, in_dtype: int) -> Chain:
     groups, cur = 0, in_dtype
     items = [s.strip() for s in spec.split(";") if s.strip()]
     for pos, item in enumerate(items):
-        name, _, arg = item.partition(":")
+        name, colon, arg = item.partition(":")
+        name, arg = name.strip(), arg.strip()
         if name == "shuffle":
             if pos != 0:
                 raise ValueError("shuffle must come first")
             groups = int(arg)
-            if groups <= 0:
-                raise ValueError("shuffle groups must be positive")
+            if not 0 < groups <= 1 << 20:
+                raise ValueError("shuffle groups outside 1..2^20")
             continue
+        if colon and name not in ("scale", "cast"):
+            raise ValueError(f"{name!r} takes no argument")
         if name in ("add", "mul"):
             ops.append(OP_ADD if name == "add" else OP_MUL)
             args.append(0.0)
             in_idx.append(len(in_dtypes))
             in_dtypes.append(cur)
         elif name == "scale":
+            try:
+                c = _f32(float(arg))
+            except OverflowError:  # beyond the fp32 range: rounds to infinity
+                c = float("inf")
+            if not np.isfinite(c):
+                raise ValueError("the scale constant must be finite in fp32")
             ops.append(OP_SCALE)
-            args.append(_f32(float(arg)))
+            args.append(c)
             in_idx.append(0)
         elif name in _UNARY:
             ops.append(_UNARY[name])
