@@ -18,6 +18,7 @@ has the chain's current dtype; ``scale`` multiplies by an fp32 constant.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import struct
 import subprocess
@@ -133,6 +134,31 @@ def _f32(x: float) -> float:
     return struct.unpack("<f", struct.pack("<f", x))[0]
 
 
+def _f32_of_literal(text: str) -> float:
+    """The fp32 value nearest the decimal literal's exact value, ties to even
+    (a literal rounded to binary64 first can land on an fp32 midpoint and
+    then round the wrong way).  Infinity beyond the fp32 range."""
+    from fractions import Fraction
+    exact = Fraction(text)
+    try:
+        c = _f32(float(exact))
+    except OverflowError:
+        return math.copysign(math.inf, exact)
+    best = c
+    with np.errstate(over="ignore"):
+        neighbours = (np.nextafter(np.float32(c), np.float32(-np.inf)),
+                      np.nextafter(np.float32(c), np.float32(np.inf)))
+    for cand in neighbours:
+        cand = float(cand)
+        if not math.isfinite(cand):
+            continue
+        d_best, d_cand = abs(Fraction(best) - exact), abs(Fraction(cand) - exact)
+        if d_cand < d_best or (d_cand == d_best and
+                               struct.unpack("<I", struct.pack("<f", cand))[0] % 2 == 0):
+            best = cand
+    return best
+
+
 def parse_spec(spec: str, in_dtype: int) -> Chain:
     """Read a spec into op codes, following the dtype through the casts."""
     ops, args, in_idx, in_dtypes = [], [], [], [in_dtype]
@@ -156,10 +182,7 @@ def parse_spec(spec: str, in_dtype: int) -> Chain:
             in_idx.append(len(in_dtypes))
             in_dtypes.append(cur)
         elif name == "scale":
-            try:
-                c = _f32(float(arg))
-            except OverflowError:  # beyond the fp32 range: rounds to infinity
-                c = float("inf")
+            c = _f32_of_literal(arg)
             if not np.isfinite(c):
                 raise ValueError("the scale constant must be finite in fp32")
             ops.append(OP_SCALE)

@@ -11,6 +11,7 @@
 import random
 import re
 
+import numpy as np
 import pytest
 
 import elementwise_chain_jit_gb300 as F
@@ -90,3 +91,22 @@ def test_random_valid_chains_compile(seed):
         dt = rng.choice(DTS)
         c = F.fuse_compile(spec, (rng.randint(1, 5000),), dt)
         assert c.n_in == 1 + sum(s in ("add", "mul") for s in spec.split(";"))
+
+
+def test_scale_literal_is_the_nearest_fp32_on_both_sides():
+    # just above the midpoint of 1 and 1 + 2^-23: a literal rounded to
+    # binary64 first lands on the midpoint and then ties down to 1; the
+    # nearest fp32 is 1 + 2^-23
+    lit = "1.000000059604644775390625000000000000001"
+    assert oracle.parse_spec(f"scale:{lit}", F.F32).args[0] == 1 + 2 ** -23
+    assert "x * 0x1.000002p+0f;" in F.fuse_source(f"scale:{lit}", (7,), F.F32)
+    # the exact midpoint ties to the even neighbour, 1
+    mid = "1.000000059604644775390625"
+    assert oracle.parse_spec(f"scale:{mid}", F.F32).args[0] == 1.0
+    assert "x * 0x1p+0f;" in F.fuse_source(f"scale:{mid}", (7,), F.F32)
+    # the largest fp32 and just past its rounding range
+    assert oracle.parse_spec("scale:3.4028235e38", F.F32).args[0] == float(np.finfo(np.float32).max)
+    with pytest.raises(ValueError):
+        oracle.parse_spec("scale:3.5e38", F.F32)
+    with pytest.raises(F.FuseError):
+        F.fuse_source("scale:3.5e38", (7,), F.F32)
