@@ -197,3 +197,17 @@ def test_debug_bounds_source(monkeypatch):
     assert src.count("in_bounds(a, v, nvec) || !in_bounds(a, src_vec(v), nvec)") == 2
     assert "in_bounds(a, e, SIZE_N(a)) || !in_bounds(a, src_elem(e), SIZE_N(a))" in src
     F.fuse_compile(spec, shape, F.F16)  # and it compiles
+
+
+def test_empty_inputs_succeed_without_a_launch():
+    # nothing to do is FUSE_OK before any device work: these pass on a box
+    # with no GPU, and launch nothing
+    before = F.fuse_stats()["launches"]
+    F.rmsnorm_residual(256, 256, 256, 256, 256, 1e-6, F.BF16, rows=0, hidden=4096)
+    F.layernorm_residual(256, 256, 256, 256, 256, 256, 1e-5, F.BF16, rows=0, hidden=4096)
+    F.rope_qkv_split(256, 256, 256, 256, 32, 128, 0, 10000.0, F.BF16, tokens=0)
+    F.rmsnorm_linear(256, None, 256, 256, 256, 1e-6, 1.0, F.BF16, M=0, N=256, K=64)
+    c = F.fuse_compile("add;relu;scale:0.5", (0,), F.F32)
+    F.fuse_launch(c, [256, 256], 256)
+    F.channel_shuffle(256, 512, 4, F.F16, shape=(0, 8, 4, 4))
+    assert F.fuse_stats()["launches"] == before
