@@ -135,7 +135,9 @@ class ClockSampler:
 
 # Special-function unit (MUFU) work of a chain: exp is one ex2, sigmoid one
 # ex2 and one rcp (the generated code's exp and sigmoid); the unit retires 16
-# of these per SM and clock.
+# of these per SM and clock (NVIDIA's documented arithmetic throughput).  With
+# the HBM bytes this gives two lower bounds on a chain's time; exp-heavy chains
+# can be bound by instruction issue instead, which is not modelled here.
 MUFU_PER_SM_CLK = 16
 
 
