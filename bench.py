@@ -310,6 +310,8 @@ def _rms_linear_item(dev, with_unfused, M=16384):
         # bias, no scale: what the fused kernel's contraction is held against
         gemm_out = torch.empty_like(out)
         it.library_gemm = lambda: torch.matmul(x, wf.t(), out=gemm_out)
+    # gamma passed per call: folded into stream-ordered scratch, then the product
+    it.gamma_path = lambda: F.rmsnorm_linear(x, g, w, b, out, eps, scale, W.BF16)
     return it
 
 
@@ -815,7 +817,8 @@ def run_gpu(args):
         rms = time_fn(rl.fused, reps=10, warm=3)
         d = {"flops": rl.flops, "us_fused": rms * 1e3, "tflops": rl.flops / (rms / 1e3) / 1e12,
              "frac_of_bf16_peak": rl.flops / (rms / 1e3) / 1e12 / tf_peak[0],
-             "bf16_peak_tflops": tf_peak[0], "peak_source": tf_peak[1]}
+             "bf16_peak_tflops": tf_peak[0], "peak_source": tf_peak[1],
+             "us_gamma_per_call": time_fn(rl.gamma_path, reps=10, warm=3) * 1e3}
         if rl.unfused is not None:
             ums = time_fn(rl.unfused, reps=5, warm=2)
             d.update({"us_unfused": ums * 1e3, "unfused_kernels": rl.n_unfused,

@@ -67,6 +67,8 @@ struct DriverApi {
   decltype(&::cuMemcpyDtoH) MemcpyDtoH;
   decltype(&::cuMemsetD32) MemsetD32;
   decltype(&::cuOccupancyMaxActiveClusters) OccupancyMaxActiveClusters;
+  decltype(&::cuMemAllocAsync) MemAllocAsync;
+  decltype(&::cuMemFreeAsync) MemFreeAsync;
 };
 
 // Returns FUSE_OK and the API table, or FUSE_E_CUDA (driver missing).

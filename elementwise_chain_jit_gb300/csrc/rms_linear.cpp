@@ -2,10 +2,12 @@
 //
 // "TeleTron" section 4.2 ("RMSNorm + Linear + scale" fused): the RMSNorm
 // factor of each row is computed inside the GEMM's tile loop and applied in
-// the epilogue, gamma is applied to the A operand in shared memory, and the
-// contraction runs on the tensor cores (tcgen05.mma with a TMEM accumulator,
-// operands staged by TMA).  The kernel is generated per (K, N, dtype, bias)
-// and compiled by NVRTC for sm_103a like every other kernel of the library.
+// the epilogue, and the contraction runs on the tensor cores (tcgen05.mma with
+// TMEM accumulators, operands staged by TMA).  gamma is folded into the
+// weight (w' = dt(w * gamma)): once by the caller through rmsnorm_linear_fold,
+// or, when gamma is passed, into a stream-ordered scratch copy for the call.
+// The kernel is generated per (K, N, dtype, bias) and compiled by NVRTC for
+// sm_103a like every other kernel of the library.
 #include <algorithm>
 #include <cmath>
 #include <map>
@@ -16,42 +18,39 @@
 namespace fuse {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kBM = 128, kBN = 256, kBK = 64;
 // the persistent CTA-pair kernel: stages of x (128 x 64) and half a w tile
 // (128 x 64) per CTA, accumulator buffers of 256 TMEM columns, runs of
 // column blocks that share one computation of the row statistics, and a
 // 32 x 32 output block per epilogue warp staged for the TMA store
 constexpr int kPairStages = 6, kPairAcc = 2, kPairRun = 2, kOutBox = 32;
-
-struct RlKernel {
-  std::shared_ptr<Module> mod;
-  int smem = 0;
-};
+// its dynamic shared memory: 1 KB alignment slack, the stages, rstd[2][128],
+// the epilogue's staging blocks, the mbarriers and the TMEM address slot
+constexpr int kPairSmem = 1024 + kPairStages * (kBM + kBN / 2) * kBK * 2 + 2 * 128 * 4 +
+                          4 * 2 * kOutBox * kOutBox * 2 + 8 * (3 * kPairStages + 8) + 16;
 
 std::mutex g_mu;
-std::map<std::tuple<int64_t, int64_t, int, int, int>, RlKernel> g_kernels;
+std::map<std::tuple<int64_t, int64_t, int, int>, std::shared_ptr<Module>> g_kernels;
 
-int rl_kernel(int64_t K, int64_t N, fuse_dtype dt, bool has_bias, bool apply_gamma, RlKernel* out) {
-  auto key = std::make_tuple(K, N, static_cast<int>(dt), has_bias ? 1 : 0, apply_gamma ? 1 : 0);
+int rl_module(int64_t K, int64_t N, fuse_dtype dt, bool has_bias, std::shared_ptr<Module>* out) {
+  auto key = std::make_tuple(K, N, static_cast<int>(dt), has_bias ? 1 : 0);
   if (auto it = g_kernels.find(key); it != g_kernels.end()) {
     stat_hit();
     *out = it->second;
     return FUSE_OK;
   }
-  RlKernel k;
-  k.smem = 1024 + kStages * (kBM + kBN) * kBK * 2 + 8 * (3 * kStages + 1) + 16;
   std::string src = fmt(
       "// RMSNorm -> Linear -> scale, K %lld, N %lld, %s, tcgen05\n"
       "constexpr int DT = %d;\nconstexpr long long KDIM = %lldLL;\nconstexpr long long NDIM = %lldLL;\n"
-      "constexpr int STAGES = %d, PSTAGES = %d, PAIR_NACC = %d, PAIR_RUN = %d;\n"
-      "constexpr bool HAS_BIAS = %s, APPLY_GAMMA = %s;\n"
+      "constexpr int PSTAGES = %d, PAIR_NACC = %d, PAIR_RUN = %d;\n"
+      "constexpr bool HAS_BIAS = %s;\n"
       "#include \"fuse/rms_linear.cuh\"\n",
       (long long)K, (long long)N, dtype_name(dt), static_cast<int>(dt), (long long)K, (long long)N,
-      kStages, kPairStages, kPairAcc, kPairRun, has_bias ? "true" : "false", apply_gamma ? "true" : "false");
-  if (int rc = jit_compile(src, "rmsnorm_linear", &k.mod)) return rc;
-  g_kernels.emplace(key, k);
-  *out = k;
+      kPairStages, kPairAcc, kPairRun, has_bias ? "true" : "false");
+  std::shared_ptr<Module> mod;
+  if (int rc = jit_compile(src, "rmsnorm_linear", &mod)) return rc;
+  g_kernels.emplace(key, mod);
+  *out = mod;
   return FUSE_OK;
 }
 
@@ -108,6 +107,46 @@ int max_clusters(const DriverApi* api, CUfunction fn, int smem, int* out) {
   return FUSE_OK;
 }
 
+// The persistent CTA-pair kernel on a weight with gamma already folded in.
+int launch_folded(const void* x, const void* w, const void* bias, void* out, int64_t M, int64_t N,
+                  int64_t K, float eps, float scale, fuse_dtype dt, void* stream) {
+  std::shared_ptr<Module> mod;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (int rc = rl_module(K, N, dt, bias != nullptr, &mod)) return rc;
+  }
+  DeviceInfo d;
+  if (int rc = current_device(&d)) return rc;
+  const DriverApi* api;
+  if (int rc = driver(&api)) return rc;
+  CUfunction fn;
+  if (int rc = jit_function(*mod, "rms_linear_persistent", d, &fn)) return rc;
+  CUdeviceptr err;
+  if (int rc = device_error_word(d.ordinal, &err)) return rc;
+  CUresult r = api->FuncSetAttribute(fn, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, kPairSmem);
+  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuFuncSetAttribute(shared memory)");
+  int clusters = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (int rc = max_clusters(api, fn, kPairSmem, &clusters)) return rc;
+  }
+  // x in 128-row tiles; each CTA of a pair loads one 128-row half of a w tile
+  alignas(64) CUtensorMap mx, mw, mo;
+  if (int rc = encode_kmajor(api, &mx, x, dt, M, K, kBM)) return rc;
+  if (int rc = encode_kmajor(api, &mw, w, dt, N, K, kBN / 2)) return rc;
+  if (int rc = encode_out(api, &mo, out, dt, M, N)) return rc;
+  const int64_t m_tiles64 = (M + kBM - 1) / kBM, n_tiles = (N + kBN - 1) / kBN;
+  int m_tiles = static_cast<int>(m_tiles64);
+  const int64_t runs = (m_tiles64 + 1) / 2 * ((n_tiles + kPairRun - 1) / kPairRun);
+  const unsigned grid = 2u * static_cast<unsigned>(std::min<int64_t>(runs, clusters));
+  void* args[] = {&mx, &mw, &mo, &bias, &m_tiles, &eps, &scale, &err};
+  r = api->LaunchKernel(fn, grid, 1, 1, 320, 1, 1, kPairSmem, reinterpret_cast<CUstream>(stream),
+                        args, nullptr);
+  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuLaunchKernel(rmsnorm_linear)");
+  stat_launch();
+  return FUSE_OK;
+}
+
 }  // namespace
 }  // namespace fuse
 
@@ -119,21 +158,14 @@ extern "C" int rmsnorm_linear(const void* x, const void* gamma, const void* w, c
   if (dt != FUSE_F16 && dt != FUSE_BF16)
     return fail(FUSE_E_DTYPE, "rmsnorm_linear runs on the tensor cores: f16 or bf16 only");
   if (M < 0 || N < 0 || K < 0) return fail(FUSE_E_SHAPE, "negative size");
-  if (gamma == nullptr) {
-    // TMA takes the ragged edges: rows and columns past the tensors load as
-    // zeros and are clipped on store; its row strides must be multiples of 16
-    // bytes
-    if (N % 8 || K % 8 || K == 0)
-      return fail(FUSE_E_SHAPE, fmt("need N %% 8 == 0, K %% 8 == 0 and K > 0 (got N %lld, K %lld)",
-                                    (long long)N, (long long)K));
-  } else if (M % kBM || N % kBN || K % kBK || K == 0 || M / kBM > 65535) {
-    return fail(FUSE_E_SHAPE,
-                fmt("with gamma given: need M %% %d == 0 (M <= %d), N %% %d == 0, K %% %d == 0 "
-                    "and K > 0 (got M %lld, N %lld, K %lld); fold gamma into w for other shapes",
-                    kBM, 65535 * kBM, kBN, kBK, (long long)M, (long long)N, (long long)K));
-  }
-  const int64_t m_tiles64 = (M + kBM - 1) / kBM, n_tiles = (N + kBN - 1) / kBN;
-  if (K > (int64_t(1) << 20) || m_tiles64 * n_tiles > INT32_MAX)
+  // TMA takes the ragged edges: rows and columns past the tensors load as
+  // zeros and are clipped on store; its row strides must be multiples of 16
+  // bytes
+  if (N % 8 || K % 8 || K == 0)
+    return fail(FUSE_E_SHAPE, fmt("need N %% 8 == 0, K %% 8 == 0 and K > 0 (got N %lld, K %lld)",
+                                  (long long)N, (long long)K));
+  const int64_t m_tiles = (M + kBM - 1) / kBM, n_tiles = (N + kBN - 1) / kBN;
+  if (K > (int64_t(1) << 20) || m_tiles * n_tiles > INT32_MAX)
     return fail(FUSE_E_SHAPE, "K or the tile count too large");
   if (!(eps >= 0.f) || !std::isfinite(scale)) return fail(FUSE_E_ARG, "bad eps or scale");
   if (M == 0 || N == 0) return FUSE_OK;
@@ -141,57 +173,24 @@ extern "C" int rmsnorm_linear(const void* x, const void* gamma, const void* w, c
   for (const void* p : {x, gamma, w, bias, static_cast<const void*>(out)})
     if (reinterpret_cast<uintptr_t>(p) % 16)
       return fail(FUSE_E_ARG, "rmsnorm_linear needs 16-byte aligned tensors (TMA)");
-  RlKernel k;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (int rc = rl_kernel(K, N, dt, bias != nullptr, gamma != nullptr, &k)) return rc;
-  }
-  DeviceInfo d;
-  if (int rc = current_device(&d)) return rc;
+  if (gamma == nullptr) return launch_folded(x, w, bias, out, M, N, K, eps, scale, dt, stream);
+  // gamma given: fold it into a scratch copy of w taken from the stream's
+  // memory pool and released on the stream after the product, so that calls
+  // on different streams never share it
   const DriverApi* api;
   if (int rc = driver(&api)) return rc;
-  // gamma folded into w: the persistent kernel (CTA pairs sharing the w
-  // tiles, double-buffered accumulator); gamma given: one CTA per tile,
-  // gamma applied to the x tiles in shared memory
-  const bool persistent = gamma == nullptr;
-  CUfunction fn;
-  if (int rc = jit_function(*k.mod, persistent ? "rms_linear_persistent" : "rms_linear_kernel", d,
-                            &fn))
-    return rc;
-  CUdeviceptr err;
-  if (int rc = device_error_word(d.ordinal, &err)) return rc;
-  const int smem = persistent ? 1024 + kPairStages * (kBM + kBN / 2) * kBK * 2 + 2 * 128 * 4 +
-                                    4 * 2 * kOutBox * kOutBox * 2 + 8 * (3 * kPairStages + 8) + 16
-                              : k.smem;
-  CUresult r = api->FuncSetAttribute(fn, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, smem);
-  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuFuncSetAttribute(shared memory)");
-  alignas(64) CUtensorMap mx, mw;
-  if (int rc = encode_kmajor(api, &mx, x, dt, M, K, kBM)) return rc;
-  // the CTA pairs of the persistent kernel each load one 128-row half of a w tile
-  if (int rc = encode_kmajor(api, &mw, w, dt, N, K, persistent ? kBN / 2 : kBN)) return rc;
-  if (persistent) {
-    int clusters = 0;
-    {
-      std::lock_guard<std::mutex> lk(g_mu);
-      if (int rc = max_clusters(api, fn, smem, &clusters)) return rc;
-    }
-    alignas(64) CUtensorMap mo;
-    if (int rc = encode_out(api, &mo, out, dt, M, N)) return rc;
-    int m_tiles = static_cast<int>(m_tiles64);
-    const int64_t runs = (m_tiles64 + 1) / 2 * ((n_tiles + kPairRun - 1) / kPairRun);
-    const unsigned grid = 2u * static_cast<unsigned>(std::min<int64_t>(runs, clusters));
-    void* args[] = {&mx, &mw, &mo, &bias, &m_tiles, &eps, &scale, &err};
-    r = api->LaunchKernel(fn, grid, 1, 1, 320, 1, 1, smem, reinterpret_cast<CUstream>(stream), args,
-                          nullptr);
-    if (r != CUDA_SUCCESS) return cuda_fail(r, "cuLaunchKernel(rmsnorm_linear)");
-    stat_launch();
-    return FUSE_OK;
-  }
-  void* args[] = {&mx, &mw, &gamma, &bias, &out, &eps, &scale, &err};
-  r = api->LaunchKernel(fn, static_cast<unsigned>(N / kBN), static_cast<unsigned>(M / kBM), 1, 192,
-                        1, 1, k.smem, reinterpret_cast<CUstream>(stream), args, nullptr);
-  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuLaunchKernel(rmsnorm_linear)");
-  stat_launch();
+  DeviceInfo d;
+  if (int rc = current_device(&d)) return rc;
+  CUdeviceptr wf = 0;
+  CUresult r = api->MemAllocAsync(&wf, static_cast<size_t>(N) * static_cast<size_t>(K) * 2,
+                                  reinterpret_cast<CUstream>(stream));
+  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuMemAllocAsync(folded weight)");
+  void* wfp = reinterpret_cast<void*>(wf);
+  int rc = rmsnorm_linear_fold(w, gamma, wfp, N, K, dt, stream);
+  if (rc == FUSE_OK) rc = launch_folded(x, wfp, bias, out, M, N, K, eps, scale, dt, stream);
+  r = api->MemFreeAsync(wf, reinterpret_cast<CUstream>(stream));
+  if (rc != FUSE_OK) return rc;
+  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuMemFreeAsync(folded weight)");
   return FUSE_OK;
 }
 
@@ -203,15 +202,15 @@ extern "C" int rmsnorm_linear_fold(const void* w, const void* gamma, void* w_out
   if (N < 0 || K < 1 || K > (int64_t(1) << 20)) return fail(FUSE_E_SHAPE, "bad N or K");
   if (N == 0) return FUSE_OK;
   if (!w || !gamma || !w_out) return fail(FUSE_E_NULL, "NULL tensor pointer");
-  RlKernel k;
+  std::shared_ptr<Module> mod;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (int rc = rl_kernel(K, kBN, dt, false, false, &k)) return rc;
+    if (int rc = rl_module(K, kBN, dt, false, &mod)) return rc;
   }
   DeviceInfo d;
   if (int rc = current_device(&d)) return rc;
   CUfunction fn;
-  if (int rc = jit_function(*k.mod, "rms_linear_fold", d, &fn)) return rc;
+  if (int rc = jit_function(*mod, "rms_linear_fold", d, &fn)) return rc;
   long long total = N * K;
   void* args[] = {&w, &gamma, &w_out, &total};
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(d.sms * 8LL, (total + 255) / 256));

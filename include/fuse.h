@@ -145,18 +145,21 @@ int rmsnorm_residual(const void* x, const void* residual, const void* weight, vo
  * the RMSNorm factor computed in the block and used directly in the linear
  * layer's accumulation, followed by an elementwise scale):
  *   s_m = 1 / sqrt(sum_k x[m,k]^2 / K + eps)
- *   out[m, n] = scale * (s_m * sum_k (x[m,k] * gamma[k]) * w[n,k] + bias[n])
+ *   out[m, n] = scale * (s_m * sum_k x[m,k] * (gamma[k] * w[n,k]) + bias[n])
  * x [M, K], gamma [K], w [N, K] (K-major, the layout of a Linear weight),
  * bias [N] (may be NULL), out [M, N]; dt f16 or bf16 (accumulation fp32);
  * all tensors 16-byte aligned.
- * gamma NULL means gamma is already folded into w (rmsnorm_linear_fold): the
- * fast path, where the tensor cores consume the tiles as they arrive; any
- * M >= 0, N % 8 == 0, K % 8 == 0 (K > 0).  With gamma given, x * gamma is
- * formed (rounded to dt) on the tiles in shared memory before each product,
- * about 4x slower; that path needs M % 128 == 0 (M <= 65535 * 128),
- * N % 256 == 0 and K % 64 == 0.  FUSE_E_SHAPE otherwise.  Every wait inside the kernel is bounded: a
- * wait that runs out records an error that fuse_device_error() reports
- * instead of hanging the device.
+ * Any M >= 0, N % 8 == 0, K % 8 == 0 (K > 0); FUSE_E_SHAPE otherwise.
+ * The product runs on a weight with gamma folded in, w' = dt(w * gamma), so
+ * the rounding of x * gamma falls on w * gamma instead (the same value in
+ * exact arithmetic).  gamma NULL means gamma is already folded into w
+ * (rmsnorm_linear_fold, once): one launch.  With gamma given, the call folds
+ * it into a scratch copy of w taken from the stream's memory pool
+ * (cuMemAllocAsync) and returned to it after the product: two launches and
+ * N * K elements of stream-ordered scratch, safe for concurrent calls on
+ * different streams.  Every wait inside the kernel is bounded: a wait that
+ * runs out records an error that fuse_device_error() reports instead of
+ * hanging the device.
  */
 int rmsnorm_linear(const void* x, const void* gamma, const void* w, const void* bias, void* out,
                    int64_t M, int64_t N, int64_t K, float eps, float scale, fuse_dtype dt,

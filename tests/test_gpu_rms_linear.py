@@ -54,13 +54,11 @@ def test_full_size_sampled_rows():
 
 
 def test_rejects_unsupported_shapes_and_dtypes():
-    with pytest.raises(F.FuseError) as e:  # gamma given: whole tiles only
-        F.rmsnorm_linear(256, 256, 256, 256, 256, 1e-6, 1.0, F.BF16, M=100, N=256, K=64)
-    assert e.value.code == -2
-    for N, K in ((260, 64), (256, 60)):  # gamma folded: TMA strides of 16 bytes
-        with pytest.raises(F.FuseError) as e:
-            F.rmsnorm_linear(256, None, 256, 256, 256, 1e-6, 1.0, F.BF16, M=128, N=N, K=K)
-        assert e.value.code == -2
+    for g in (256, None):  # both paths: TMA row strides of 16 bytes
+        for N, K in ((260, 64), (256, 60), (256, 0)):
+            with pytest.raises(F.FuseError) as e:
+                F.rmsnorm_linear(256, g, 256, 256, 256, 1e-6, 1.0, F.BF16, M=128, N=N, K=K)
+            assert e.value.code == -2
     with pytest.raises(F.FuseError) as e:
         F.rmsnorm_linear(256, 256, 256, 256, 256, 1e-6, 1.0, F.F32, M=128, N=256, K=64)
     assert e.value.code == -3
@@ -115,3 +113,34 @@ def test_folded_ragged_shapes(M, N, K, dt):
     # rows, columns and k-steps past the tensors: zeros on load, clipped on
     # store (the output's canaries catch a store past M * N)
     _folded_case(M, N, K, dt, 70 + M % 13)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (100, 264, 72), (300, 520, 200)])
+def test_gamma_path_ragged_shapes(M, N, K):
+    # gamma given: folded into a stream-ordered scratch copy of w for the call,
+    # so the gamma path takes the same shapes as the folded one
+    _case(M, N, K, F.BF16, 90 + M % 11)
+
+
+def test_gamma_path_on_two_streams_at_once():
+    # two calls with different gamma on two streams: each folds into its own
+    # scratch copy of w, taken from and returned to its stream's pool
+    M, N, K, dt = 512, 512, 256, F.BF16
+    x = workloads.normal((M, K), 0, 1, 95, dt)
+    w = workloads.normal((N, K), 0, 1 / np.sqrt(K), 96, dt)
+    gs = [workloads.normal(K, 1, 0.1, 97 + i, dt) for i in range(2)]
+    xd, wd = to_dev(x.reshape(-1), dt), to_dev(w.reshape(-1), dt)
+    gd = [to_dev(g, dt) for g in gs]
+    outs = [torch.empty(M * N, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for i in range(2):
+            F.rmsnorm_linear(xd, gd[i], wd, None, outs[i], 1e-6, 1.0, dt, M=M, N=N, K=K,
+                             stream=streams[i])
+    torch.cuda.synchronize()
+    assert F.fuse_device_error() == 0
+    for i in range(2):
+        want, mag = oracle.rmsnorm_linear(x, gs[i], w, None, dt, 1e-6, 1.0)
+        got = oracle.to_double(to_host(outs[i], dt), dt).reshape(M, N)
+        assert not (np.abs(got - want) > 8e-3 * mag).any()
