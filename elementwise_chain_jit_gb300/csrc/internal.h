@@ -67,8 +67,10 @@ struct DriverApi {
   decltype(&::cuMemcpyDtoH) MemcpyDtoH;
   decltype(&::cuMemsetD32) MemsetD32;
   decltype(&::cuOccupancyMaxActiveClusters) OccupancyMaxActiveClusters;
-  decltype(&::cuMemAllocAsync) MemAllocAsync;
   decltype(&::cuMemFreeAsync) MemFreeAsync;
+  decltype(&::cuMemPoolCreate) MemPoolCreate;
+  decltype(&::cuMemPoolSetAttribute) MemPoolSetAttribute;
+  decltype(&::cuMemAllocFromPoolAsync) MemAllocFromPoolAsync;
 };
 
 // Returns FUSE_OK and the API table, or FUSE_E_CUDA (driver missing).

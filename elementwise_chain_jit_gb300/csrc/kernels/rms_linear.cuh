@@ -27,6 +27,27 @@ extern "C" __global__ void rms_linear_fold(const u16* __restrict__ w, const u16*
     store_elem<DT>(wout, i, load_elem<DT>(w, i) * load_elem<DT>(gamma, i % KDIM));
 }
 
+// The same fold, 8 elements (16 bytes) per access: K % 8 == 0 and 16-byte
+// aligned pointers, so the 8 values of a vector share one row of w and gamma's
+// 8 values are one aligned vector too.
+extern "C" __global__ void rms_linear_fold_vec(const u16* __restrict__ w,
+                                               const u16* __restrict__ gamma,
+                                               u16* __restrict__ wout, long long total) {
+  const long long nvec = total / 8;
+  for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < nvec;
+       v += (long long)gridDim.x * blockDim.x) {
+    const uint4 w4 = __ldg(reinterpret_cast<const uint4*>(w) + v);
+    const uint4 g4 = __ldg(reinterpret_cast<const uint4*>(gamma) + (v * 8 % KDIM) / 8);
+    const u32 ww[4] = {w4.x, w4.y, w4.z, w4.w}, gw[4] = {g4.x, g4.y, g4.z, g4.w};
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = get_elem<DT>(ww, e) * get_elem<DT>(gw, e);
+    u32 o[4];
+    pack_vec<DT>(y, o);
+    reinterpret_cast<uint4*>(wout)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;

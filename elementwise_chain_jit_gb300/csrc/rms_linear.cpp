@@ -107,6 +107,34 @@ int max_clusters(const DriverApi* api, CUfunction fn, int smem, int* out) {
   return FUSE_OK;
 }
 
+// A device's pool for the folded-weight scratch of calls that pass gamma:
+// the library's own (the process's default pool keeps its settings), with no
+// release threshold, so a scratch block stays mapped for the next call
+// instead of being unmapped at every synchronisation.  It holds at most what
+// the calls that overlap on the GPU needed at once.
+int scratch_pool(const DriverApi* api, int device, CUmemoryPool* out) {
+  static std::mutex mu;
+  static CUmemoryPool pools[64] = {};
+  if (device < 0 || device >= 64) return fail(FUSE_E_ARG, "device ordinal out of range");
+  std::lock_guard<std::mutex> lk(mu);
+  if (!pools[device]) {
+    CUmemPoolProps props = {};
+    props.allocType = CU_MEM_ALLOCATION_TYPE_PINNED;
+    props.handleTypes = CU_MEM_HANDLE_TYPE_NONE;
+    props.location.type = CU_MEM_LOCATION_TYPE_DEVICE;
+    props.location.id = device;
+    CUmemoryPool pool;
+    CUresult r = api->MemPoolCreate(&pool, &props);
+    if (r != CUDA_SUCCESS) return cuda_fail(r, "cuMemPoolCreate");
+    cuuint64_t keep = ~cuuint64_t(0);
+    r = api->MemPoolSetAttribute(pool, CU_MEMPOOL_ATTR_RELEASE_THRESHOLD, &keep);
+    if (r != CUDA_SUCCESS) return cuda_fail(r, "cuMemPoolSetAttribute");
+    pools[device] = pool;
+  }
+  *out = pools[device];
+  return FUSE_OK;
+}
+
 // The persistent CTA-pair kernel on a weight with gamma already folded in.
 int launch_folded(const void* x, const void* w, const void* bias, void* out, int64_t M, int64_t N,
                   int64_t K, float eps, float scale, fuse_dtype dt, void* stream) {
@@ -174,17 +202,19 @@ extern "C" int rmsnorm_linear(const void* x, const void* gamma, const void* w, c
     if (reinterpret_cast<uintptr_t>(p) % 16)
       return fail(FUSE_E_ARG, "rmsnorm_linear needs 16-byte aligned tensors (TMA)");
   if (gamma == nullptr) return launch_folded(x, w, bias, out, M, N, K, eps, scale, dt, stream);
-  // gamma given: fold it into a scratch copy of w taken from the stream's
-  // memory pool and released on the stream after the product, so that calls
-  // on different streams never share it
+  // gamma given: fold it into a scratch copy of w allocated on the stream
+  // and released on the stream after the product, so that calls on
+  // different streams never share it
   const DriverApi* api;
   if (int rc = driver(&api)) return rc;
   DeviceInfo d;
   if (int rc = current_device(&d)) return rc;
+  CUmemoryPool pool = nullptr;
+  if (int rc = scratch_pool(api, d.ordinal, &pool)) return rc;
   CUdeviceptr wf = 0;
-  CUresult r = api->MemAllocAsync(&wf, static_cast<size_t>(N) * static_cast<size_t>(K) * 2,
-                                  reinterpret_cast<CUstream>(stream));
-  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuMemAllocAsync(folded weight)");
+  CUresult r = api->MemAllocFromPoolAsync(&wf, static_cast<size_t>(N) * static_cast<size_t>(K) * 2,
+                                          pool, reinterpret_cast<CUstream>(stream));
+  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuMemAllocFromPoolAsync(folded weight)");
   void* wfp = reinterpret_cast<void*>(wf);
   int rc = rmsnorm_linear_fold(w, gamma, wfp, N, K, dt, stream);
   if (rc == FUSE_OK) rc = launch_folded(x, wfp, bias, out, M, N, K, eps, scale, dt, stream);
@@ -213,6 +243,14 @@ extern "C" int rmsnorm_linear_fold(const void* w, const void* gamma, void* w_out
   if (int rc = jit_function(*mod, "rms_linear_fold", d, &fn)) return rc;
   long long total = N * K;
   void* args[] = {&w, &gamma, &w_out, &total};
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(d.sms * 8LL, (total + 255) / 256));
+  // 8 elements (16 bytes) per access when the rows and pointers allow it
+  const bool vec = K % 8 == 0 && aligned16(w) && aligned16(gamma) && aligned16(w_out);
+  const int64_t items = vec ? total / 8 : total;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(d.sms * 8LL, (items + 255) / 256));
+  if (vec) {
+    CUfunction fv;
+    if (int rc = jit_function(*mod, "rms_linear_fold_vec", d, &fv)) return rc;
+    return launch(fv, grid, 256, 0, stream, args);
+  }
   return launch(fn, grid, 256, 0, stream, args);
 }

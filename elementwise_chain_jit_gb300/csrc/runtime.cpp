@@ -146,8 +146,10 @@ void load_driver() {
   FUSE_GET(MemcpyDtoH, "cuMemcpyDtoH");
   FUSE_GET(MemsetD32, "cuMemsetD32");
   FUSE_GET(OccupancyMaxActiveClusters, "cuOccupancyMaxActiveClusters");
-  FUSE_GET(MemAllocAsync, "cuMemAllocAsync");
   FUSE_GET(MemFreeAsync, "cuMemFreeAsync");
+  FUSE_GET(MemPoolCreate, "cuMemPoolCreate");
+  FUSE_GET(MemPoolSetAttribute, "cuMemPoolSetAttribute");
+  FUSE_GET(MemAllocFromPoolAsync, "cuMemAllocFromPoolAsync");
 #undef FUSE_GET
   if (!ok) return;
   CUresult r = g_api.Init(0);

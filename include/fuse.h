@@ -154,10 +154,11 @@ int rmsnorm_residual(const void* x, const void* residual, const void* weight, vo
  * the rounding of x * gamma falls on w * gamma instead (the same value in
  * exact arithmetic).  gamma NULL means gamma is already folded into w
  * (rmsnorm_linear_fold, once): one launch.  With gamma given, the call folds
- * it into a scratch copy of w taken from the stream's memory pool
- * (cuMemAllocAsync) and returned to it after the product: two launches and
- * N * K elements of stream-ordered scratch, safe for concurrent calls on
- * different streams.  Every wait inside the kernel is bounded: a wait that
+ * it into a scratch copy of w allocated on the stream (from a per-device
+ * pool the library keeps mapped; it holds what overlapping calls needed at
+ * once) and freed on the stream after the product: two launches and N * K
+ * elements of stream-ordered scratch, safe for concurrent calls on different
+ * streams.  Every wait inside the kernel is bounded: a wait that
  * runs out records an error that fuse_device_error() reports instead of
  * hanging the device.
  */
