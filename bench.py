@@ -477,6 +477,27 @@ def graph_per_launch(fn, k=20):
     return a.elapsed_time(b) / k
 
 
+def cold_time(item, reps=10):
+    """Median time of one launch with its inputs cold in HBM and no dirty
+    lines left in L2: before each launch a read-only pass over 512 MB (four
+    times L2) evicts L2 with clean lines."""
+    import torch
+    flush = getattr(cold_time, "buf", None)
+    if flush is None:
+        flush = cold_time.buf = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream()
+    ts = []
+    for _ in range(reps + 2):
+        flush.sum()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        item.fused()
+        b.record(s)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts[2:]) * 1e3
+
+
 def graph_times(item, k=50):
     """Launch overhead of a small workload ("DeepJIT" section 6.1's per-op /
     CUDA graph / fused comparison): mean time per pass over k passes of
@@ -786,6 +807,7 @@ def run_gpu(args):
                       "speedup": ums / ms, "extra_cost_per_unfused_op_us": L * 1e3})
         if it.bytes < 64e6 and not args.no_unfused:
             d.update(graph_times(it))
+            d["us_fused_cold_clean_l2"] = cold_time(it)
         if it.mufu_ops:
             # two rooflines: HBM bytes and special-function unit operations
             # at the clock sampled during the timed region
