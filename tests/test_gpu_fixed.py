@@ -18,6 +18,12 @@ from gpu_util import Guarded, misaligned_copy, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
+# Half the spacing of each format's subnormals (IEEE 754 binary16: 2^-24;
+# bfloat16 and binary32: 2^-133 and 2^-149): below the smallest normal a
+# correct rounding is off by up to this much in absolute terms, whatever the
+# relative tolerance above it.
+SUB_HALF = {F.F16: 2.0 ** -25, F.BF16: 2.0 ** -134, F.F32: 2.0 ** -150}
+
 
 # ------------------------------------------------------------ RMSNorm
 
@@ -43,7 +49,7 @@ def _rms_case(rows, hidden, dt, seed, offset=0, inplace=False, eps=1e-6):
     got_r = to_host(res_out_t, dt).reshape(rows, hidden)
     assert np.array_equal(got_r, oracle.store(h, dt))  # one rounding of an exact sum
     rel = 8e-3 if dt == F.BF16 else (2e-3 if dt == F.F16 else 1e-5)
-    np.testing.assert_allclose(got_y, y, rtol=rel, atol=0)
+    np.testing.assert_allclose(got_y, y, rtol=rel, atol=SUB_HALF[dt])
     return got_y
 
 
@@ -117,7 +123,7 @@ def _ln_case(rows, hidden, dt, seed, flags=7, offset=0, inplace=False, eps=1e-5)
         assert np.array_equal(to_host(ro, dt).reshape(rows, hidden), oracle.store(h, dt))
     rel = 8e-3 if dt == F.BF16 else (2e-3 if dt == F.F16 else 2e-5)
     got = oracle.to_double(to_host(out.t, dt), dt).reshape(rows, hidden)
-    bad = np.abs(got - y) > rel * mag
+    bad = np.abs(got - y) > rel * mag + SUB_HALF[dt]
     assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], y[bad][:5])
 
 
@@ -154,6 +160,30 @@ def test_layernorm_full_config_sampled_rows():
     assert np.array_equal(to_host(ro[st], F.BF16), oracle.store(h, F.BF16))
     got = oracle.to_double(to_host(out[st], F.BF16), F.BF16)
     assert np.all(np.abs(got - y) <= 8e-3 * mag)
+
+
+# ------------------------------------------------------------ many rows
+# Thousands of rows: every SM runs many CTAs; tiny rows (24 elements) leave
+# most lanes of a CTA idle; 480,000 f16 outputs reach below the smallest
+# normal, where only the absolute tolerance holds.
+
+MANY_ROWS = [(F.BF16, 4096, 3000), (F.F32, 1000, 6000), (F.F16, 24, 20000)]
+
+
+@pytest.mark.parametrize("dt,hidden,rows", MANY_ROWS)
+def test_rmsnorm_many_rows(dt, hidden, rows):
+    _rms_case(rows, hidden, dt, 70)
+
+
+@pytest.mark.parametrize("dt,hidden,rows", MANY_ROWS)
+@pytest.mark.parametrize("flags", [7, 0])
+def test_layernorm_many_rows(dt, hidden, rows, flags):
+    _ln_case(rows, hidden, dt, 80, flags=flags)
+
+
+def test_norms_in_place_many_rows():
+    _rms_case(2000, 4096, F.BF16, 90, inplace=True)
+    _ln_case(2000, 4096, F.BF16, 91, inplace=True)
 
 
 # ------------------------------------------------------------ QKV split + RoPE

@@ -124,6 +124,10 @@ def test_fixed_entry_points_compile_then_report_no_device():
     for call in (
         lambda: F.rmsnorm_residual(ptr, ptr, ptr, ptr, ptr, 1e-6, F.BF16, rows=16, hidden=4096,
                                    stream=0),
+        lambda: F.layernorm_residual(ptr, ptr, ptr, ptr, ptr, ptr, 1e-5, F.BF16, rows=16,
+                                     hidden=4096, stream=0),
+        lambda: F.layernorm_residual(ptr, None, None, None, ptr, None, 1e-5, F.F32, rows=16,
+                                     hidden=1000, stream=0),
         lambda: F.rope_qkv_split(ptr, ptr, ptr, ptr, 32, 128, 0, 10000.0, F.BF16, tokens=64,
                                  stream=0),
         lambda: F.detect_decode([ptr, ptr, ptr], [(8, 8), (4, 4), (2, 2)], [8, 16, 32],
@@ -133,7 +137,7 @@ def test_fixed_entry_points_compile_then_report_no_device():
         with pytest.raises(F.FuseError) as e:
             call()
         assert e.value.code == -7 and "driver" in str(e.value)
-    assert F.fuse_stats()["compiles"] >= before + 4  # codegen + NVRTC ran before the device step
+    assert F.fuse_stats()["compiles"] >= before + 6  # codegen + NVRTC ran before the device step
 
 
 def test_argument_validation():
