@@ -193,8 +193,9 @@ extern "C" int rmsnorm_linear(const void* x, const void* gamma, const void* w, c
     return fail(FUSE_E_SHAPE, fmt("need N %% 8 == 0, K %% 8 == 0 and K > 0 (got N %lld, K %lld)",
                                   (long long)N, (long long)K));
   const int64_t m_tiles = (M + kBM - 1) / kBM, n_tiles = (N + kBN - 1) / kBN;
-  if (K > (int64_t(1) << 20) || m_tiles * n_tiles > INT32_MAX)
-    return fail(FUSE_E_SHAPE, "K or the tile count too large");
+  // TMA tile coordinates are 32-bit
+  if (K > (int64_t(1) << 20) || M > INT32_MAX - kBM || m_tiles * n_tiles > INT32_MAX)
+    return fail(FUSE_E_SHAPE, "M, K or the tile count too large");
   if (!(eps >= 0.f) || !std::isfinite(scale)) return fail(FUSE_E_ARG, "bad eps or scale");
   if (M == 0 || N == 0) return FUSE_OK;
   if (!x || !w || !out) return fail(FUSE_E_NULL, "NULL tensor pointer");

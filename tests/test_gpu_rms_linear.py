@@ -59,6 +59,10 @@ def test_rejects_unsupported_shapes_and_dtypes():
             with pytest.raises(F.FuseError) as e:
                 F.rmsnorm_linear(256, g, 256, 256, 256, 1e-6, 1.0, F.BF16, M=128, N=N, K=K)
             assert e.value.code == -2
+        # TMA row coordinates are 32-bit
+        with pytest.raises(F.FuseError) as e:
+            F.rmsnorm_linear(256, g, 256, 256, 256, 1e-6, 1.0, F.BF16, M=2 ** 31, N=256, K=64)
+        assert e.value.code == -2
     with pytest.raises(F.FuseError) as e:
         F.rmsnorm_linear(256, 256, 256, 256, 256, 1e-6, 1.0, F.F32, M=128, N=256, K=64)
     assert e.value.code == -3

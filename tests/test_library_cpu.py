@@ -160,6 +160,10 @@ def test_argument_validation():
     with pytest.raises(F.FuseError) as e:
         F.channel_shuffle(256, 256, 3, F.F16, shape=(2, 16, 8, 8), stream=0)
     assert e.value.code == -2  # 16 % 3
+    with pytest.raises(F.FuseError) as e:  # row coordinates past 32 bits
+        F.rmsnorm_linear(256, None, 256, 256, 256, 1e-6, 1.0, F.BF16, M=2 ** 31, N=256, K=64,
+                         stream=0)
+    assert e.value.code == -2
     # empty work is a no-op, even without a device
     F.rmsnorm_residual(0, 0, 0, 0, 0, 1e-6, F.BF16, rows=0, hidden=64, stream=0)
     F.rope_qkv_split(0, 0, 0, 0, 4, 128, 0, 10000.0, F.BF16, tokens=0, stream=0)
