@@ -807,7 +807,11 @@ def run_gpu(args):
                       "speedup": ums / ms, "extra_cost_per_unfused_op_us": L * 1e3})
         if it.bytes < 64e6 and not args.no_unfused:
             d.update(graph_times(it))
-            d["us_fused_cold_clean_l2"] = cold_time(it)
+        # the same launch alone, inputs cold and no predecessor's dirty lines
+        # left in L2 to write back (in the step each item pays for those)
+        cold_us = cold_time(it, reps=10 if it.bytes < 64e6 else 5)
+        d.update({"us_fused_cold_clean_l2": cold_us,
+                  "frac_cold_clean_l2": it.bytes / (cold_us * 1e-6) / 1e9 / peak})
         if it.mufu_ops:
             # two rooflines: HBM bytes and special-function unit operations
             # at the clock sampled during the timed region
@@ -825,8 +829,11 @@ def run_gpu(args):
     if args.only is None or re.search(args.only, "layernorm_residual_16384x4096_bf16"):
         ln = _ln_item(dev, with_unfused=not args.no_unfused)
         lms = time_fn(ln.fused, reps=20, warm=3)
+        cold_us = cold_time(ln, reps=5)
         d = {"bytes": ln.bytes, "us_fused": lms * 1e3, "gbs": ln.bytes / (lms / 1e3) / 1e9,
-             "frac_of_" + peak_kind + "_peak": ln.bytes / (lms / 1e3) / 1e9 / peak}
+             "frac_of_" + peak_kind + "_peak": ln.bytes / (lms / 1e3) / 1e9 / peak,
+             "us_fused_cold_clean_l2": cold_us,
+             "frac_cold_clean_l2": ln.bytes / (cold_us * 1e-6) / 1e9 / peak}
         if ln.unfused is not None:
             ums = time_fn(ln.unfused, reps=3, warm=1)
             d.update({"us_unfused": ums * 1e3, "unfused_kernels": ln.n_unfused,
