@@ -28,6 +28,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -275,7 +276,7 @@ def _ln_item(dev, with_unfused):
             d = hf - mean
             var = (d * d).mean(-1, keepdim=True)
             return (d * torch.rsqrt(var + eps) * g.float() + b.float()).to(torch.bfloat16), h
-        it.unfused, it.n_unfused = ln_unfused, 12
+        it.unfused, it.n_unfused = ln_unfused, 14  # kernels, as --launch-trace counts them
     return it
 
 
@@ -305,7 +306,7 @@ def _rms_linear_item(dev, with_unfused, M=16384):
             xf = x.float()
             y = (xf * torch.rsqrt(xf.pow(2).mean(-1, keepdim=True) + eps) * g.float()).to(torch.bfloat16)
             return torch.nn.functional.linear(y, w, b) * scale
-        it.unfused, it.n_unfused = unfused, 9
+        it.unfused, it.n_unfused = unfused, 11  # kernels, as --launch-trace counts them
         # the bare GEMM of the same shape in the vendor library, no norm, no
         # bias, no scale: what the fused kernel's contraction is held against
         gemm_out = torch.empty_like(out)
@@ -343,7 +344,7 @@ def _rope_item(dev, with_unfused):
                 rh = torch.cat([-xf[..., D // 2:], xf[..., :D // 2]], -1)
                 outs[i] = (xf * cos + rh * sin).to(torch.bfloat16)
             return outs
-        it.unfused, it.n_unfused = rope_unfused, 15
+        it.unfused, it.n_unfused = rope_unfused, 17  # kernels, as --launch-trace counts them
     return it
 
 
@@ -380,7 +381,7 @@ def _detect_item(dev, with_unfused):
                 wh = (p[..., 2:4] * 2) ** 2 * an[s].view(1, dc["na"], 1, 1, 2)
                 outs.append(torch.cat([xy, wh, p[..., 4:]], -1).view(1, -1, dc["no"]))
             return torch.cat(outs, 1)
-        it.unfused, it.n_unfused = detect_unfused, 34
+        it.unfused, it.n_unfused = detect_unfused, 40  # kernels, as --launch-trace counts them
     return it
 
 
@@ -753,6 +754,8 @@ def run_gpu(args):
                         spec_dtype={"f32": 0, "f16": 1, "bf16": 2}[args.spec_dtype])
     if not items:
         raise SystemExit(f"--only {args.only!r} matches no workload")
+    if args.launch_trace:
+        return run_launch_trace(args, items, dev)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     step_bytes = sum(it.bytes for it in items)
@@ -983,6 +986,70 @@ def run_gpu(args):
     return 0
 
 
+def device_ops(fn):
+    """The device activities (kernels, copies, memsets) of one call of fn, from
+    CUPTI's records through torch.profiler: a list of (start_us, end_us, name)
+    in start order."""
+    import torch
+    from torch.profiler import ProfilerActivity, profile
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    ops = []
+    for e in prof.profiler.kineto_results.events():
+        if e.device_type() == torch.autograd.DeviceType.CUDA:
+            t0 = e.start_ns() / 1e3
+            ops.append((t0, t0 + e.duration_ns() / 1e3, e.name()))
+    return sorted(ops)
+
+
+def launch_trace(items):
+    """Per workload, the fused launch against the unfused per-op sequence, as
+    a timeline profiler shows them: device activities, their summed busy time,
+    the span from the first start to the last end, and the idle gaps inside
+    that span (span - busy), plus the time of the whole call measured with
+    CUDA events outside the profiler."""
+    import torch
+    device_ops(lambda: None)  # the process's first session can miss records
+    out = {}
+    for it in items:
+        rec = {}
+        for mode, fn in (("fused", it.fused), ("unfused", it.unfused)):
+            if fn is None:
+                continue
+            fn()  # warm: compiled, allocated, cached
+            ops = device_ops(fn)
+            if not ops:
+                rec[mode] = {"device_ops": 0}
+                continue
+            busy = sum(b - a for a, b, _ in ops)
+            span = ops[-1][1] - ops[0][0]
+            names = {}
+            for _, _, n in ops:
+                k = n.split("<")[0].split("(")[0][:60]
+                names[k] = names.get(k, 0) + 1
+            rec[mode] = {"device_ops": len(ops), "busy_us": busy, "span_us": span,
+                         "gaps_us": max(0.0, span - busy),
+                         "us_events": time_fn(fn, reps=5, warm=1) * 1e3,
+                         "ops_by_name": names}
+        if "unfused" in rec:
+            rec["declared_unfused_kernels"] = it.n_unfused
+        out[it.name] = rec
+    torch.cuda.synchronize()
+    return out
+
+
+def run_launch_trace(args, items, dev):
+    extra = []
+    if args.only is None or re.search(args.only, "layernorm_residual_16384x4096_bf16"):
+        extra.append(_ln_item(dev, with_unfused=True))
+    if args.only is None or re.search(args.only, "rmsnorm_linear"):
+        extra.append(_rms_linear_item(dev, with_unfused=True, M=args.rl_m))
+    print(json.dumps({"launch_trace": launch_trace(items + extra)}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -997,6 +1064,8 @@ def main():
     ap.add_argument("--spec", default=None, help="time this one chain (flat) instead")
     ap.add_argument("--rl-m", type=int, default=16384, help="M of the RMSNorm -> Linear row")
     ap.add_argument("--spec-dtype", default="f32", choices=["f32", "f16", "bf16"])
+    ap.add_argument("--launch-trace", action="store_true",
+                    help="print device-op counts and gaps of fused vs unfused sequences instead")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
