@@ -205,7 +205,7 @@ __device__ __forceinline__ void st_shared16(u32 addr, uint4 v) {
 //              issues the MMAs of every block
 //   warps 2-5  epilogue of this CTA's tile, 32 rows each (TMEM lane quarter
 //              warp % 4): TMEM -> registers -> s_m * acc + bias, * scale ->
-//              a 32 x 32 block in shared memory -> TMA bulk store
+//              a 32 x 64 block in shared memory -> TMA bulk store
 //   warps 6-9  row statistics of this CTA's x rows, handed to the epilogue in
 //              shared memory (rstd[buffer][row])
 // Signals: CTA 0's "full" completes when both CTAs' copies of a stage have
@@ -227,7 +227,10 @@ constexpr int PSTAGE_BYTES = A_BYTES + B_HALF;  // per CTA and stage
 constexpr int NACC = PAIR_NACC;                 // accumulator buffers in TMEM
 constexpr int RUN = PAIR_RUN;                   // column blocks per run
 constexpr int RUNS_PER_MP = (NT_TILES + RUN - 1) / RUN;
-constexpr int OUT_BLOCK = 32 * 32 * 2;  // one epilogue warp's staged 32 x 32 block
+// one epilogue warp's staged block: 32 rows x 64 columns, 128-byte rows in
+// the output tensor map's 128-byte swizzle (so 1024-byte aligned)
+constexpr int OUT_COLS = 64;
+constexpr int OUT_BLOCK = 32 * OUT_COLS * 2;
 // Instruction descriptor of the pair's MMA, kind::f16: D fp32 (bits 4-5 = 1),
 // A and B f16 (0) or bf16 (1) in bits 7-9 / 10-12, both K-major (bits 15, 16
 // = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28 (M 256 across the pair,
@@ -254,7 +257,10 @@ rms_linear_persistent(const __grid_constant__ TensorMap tmap_x,
   const u32 base = (raw + 1023u) & ~1023u;
   unsigned char* const base_ptr = smem_raw + (base - raw);
   float* const rstd_buf = reinterpret_cast<float*>(base_ptr + PSTAGES * PSTAGE_BYTES);  // [2][128]
-  const u32 staging = base + PSTAGES * PSTAGE_BYTES + 2 * 128 * 4;  // [4 warps][2][32 x 32]
+  // [4 warps][2][32 x 64], each block 1024-byte aligned for the swizzle
+  static_assert((PSTAGES * PSTAGE_BYTES + 2 * 128 * 4) % 1024 == 0 && OUT_BLOCK % 1024 == 0,
+                "staging blocks must stay 1024-byte aligned");
+  const u32 staging = base + PSTAGES * PSTAGE_BYTES + 2 * 128 * 4;
   const u32 bars = staging + 4 * 2 * OUT_BLOCK;
   auto stage_a = [&](int s) { return base + s * PSTAGE_BYTES; };
   auto stage_b = [&](int s) { return base + s * PSTAGE_BYTES + A_BYTES; };
@@ -352,7 +358,7 @@ rms_linear_persistent(const __grid_constant__ TensorMap tmap_x,
     const int r = q * 32 + lane;
     const u32 acc_empty0 = peer_addr(acc_empty(0), 0);
     const u32 stg = staging + q * 2 * OUT_BLOCK;
-    int i = 0, j = 0, sc = 0;  // blocks, runs, staged 32 x 32 blocks so far
+    int i = 0, j = 0, sc = 0;  // blocks, runs, staged 32 x 64 blocks so far
     for (int run = cluster; run < runs && ok; run += nclusters, ++j) {
       const int mp = run_mp(run), nb = run_n(run), len = run_len(run);
       const int mt = 2 * mp + static_cast<int>(rank);
@@ -367,49 +373,54 @@ rms_linear_persistent(const __grid_constant__ TensorMap tmap_x,
         tc_fence_after();
         if (store) {
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c, ++sc) {
-            u32 acc[32];
-            tmem_ld32(tmem + b * TMEM_COLS + ((u32)(q * 32) << 16) + c * 32, acc);
-            u32 bw[16];
-            if constexpr (HAS_BIAS) {
-              // N % 8 == 0: each 8-value vector lies wholly inside or past N
-              const uint4* bp = reinterpret_cast<const uint4*>(bias + n0 + c * 32);
+          for (int c = 0; c < BN / OUT_COLS; ++c, ++sc) {
+            // 64 columns of row r: two 32-column TMEM loads, each converted
+            // and packed before the next to keep registers down
+            u32 o[OUT_COLS / 2];
 #pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                const uint4 t4 =
-                    n0 + c * 32 + 8 * v < NDIM ? __ldg(bp + v) : make_uint4(0u, 0u, 0u, 0u);
-                bw[4 * v] = t4.x; bw[4 * v + 1] = t4.y; bw[4 * v + 2] = t4.z; bw[4 * v + 3] = t4.w;
+            for (int hf = 0; hf < 2; ++hf) {
+              const int c0 = c * OUT_COLS + hf * 32;
+              u32 acc[32];
+              tmem_ld32(tmem + b * TMEM_COLS + ((u32)(q * 32) << 16) + c0, acc);
+              u32 bw[16];
+              if constexpr (HAS_BIAS) {
+                // N % 8 == 0: each 8-value vector lies wholly inside or past N
+                const uint4* bp = reinterpret_cast<const uint4*>(bias + n0 + c0);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  const uint4 t4 =
+                      n0 + c0 + 8 * v < NDIM ? __ldg(bp + v) : make_uint4(0u, 0u, 0u, 0u);
+                  bw[4 * v] = t4.x; bw[4 * v + 1] = t4.y; bw[4 * v + 2] = t4.z; bw[4 * v + 3] = t4.w;
+                }
               }
-            }
-            float y[32];
+              float y[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              float v = __uint_as_float(acc[e]) * rs;
-              if constexpr (HAS_BIAS) v += get_elem<DT>(bw, e);
-              y[e] = v * scale;
+              for (int e = 0; e < 32; ++e) {
+                float v = __uint_as_float(acc[e]) * rs;
+                if constexpr (HAS_BIAS) v += get_elem<DT>(bw, e);
+                y[e] = v * scale;
+              }
+              u32 oh[16];
+              pack_vec<DT>(y, oh);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) o[hf * 16 + e] = oh[e];
             }
-            u32 o[16];
-            pack_vec<DT>(y, o);
             // this buffer's store from two blocks ago must have read it
             const u32 buf = stg + (sc & 1) * OUT_BLOCK;
             if (sc >= 2 && lane == 0) bulk_wait_read1();
             __syncwarp();
-            // row `lane` of the 32 x 32 block, 4 chunks of 16 bytes; lanes
-            // 2l and 2l+1 start at chunk l, so 8 lanes cover all 32 banks
-            const uint4 v0 = make_uint4(o[0], o[1], o[2], o[3]);
-            const uint4 v1 = make_uint4(o[4], o[5], o[6], o[7]);
-            const uint4 v2 = make_uint4(o[8], o[9], o[10], o[11]);
-            const uint4 v3 = make_uint4(o[12], o[13], o[14], o[15]);
+            // row `lane` of the 32 x 64 block in the 128-byte swizzle of the
+            // output tensor map: its 16-byte chunk k sits at position
+            // k ^ (lane % 8) of the row, so the 8 lanes of each store phase
+            // write 8 different positions (all 32 banks)
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const int cc = (h + (lane >> 1)) & 3;
-              const uint4 v = cc == 0 ? v0 : cc == 1 ? v1 : cc == 2 ? v2 : v3;
-              st_shared16(buf + lane * 64 + cc * 16, v);
-            }
+            for (int k = 0; k < 8; ++k)
+              st_shared16(buf + lane * 128 + ((k ^ (lane & 7)) << 4),
+                          make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]));
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmap_out, buf, n0 + c * 32, mt * BM + q * 32);
+              tma_store_2d(&tmap_out, buf, n0 + c * OUT_COLS, mt * BM + q * 32);
               bulk_commit();
             }
           }

@@ -19,15 +19,18 @@ namespace fuse {
 namespace {
 
 constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr int kSmemOptinSm103 = 227 * 1024;  // shared memory a CTA may opt in to
 // the persistent CTA-pair kernel: stages of x (128 x 64) and half a w tile
 // (128 x 64) per CTA, accumulator buffers of 256 TMEM columns, runs of
 // column blocks that share one computation of the row statistics, and a
-// 32 x 32 output block per epilogue warp staged for the TMA store
-constexpr int kPairStages = 6, kPairAcc = 2, kPairRun = 2, kOutBox = 32;
+// 32 x 64 output block (128-byte rows, 128-byte swizzle) per epilogue warp
+// staged for the TMA store
+constexpr int kPairStages = 6, kPairAcc = 2, kPairRun = 2, kOutRows = 32, kOutCols = 64;
 // its dynamic shared memory: 1 KB alignment slack, the stages, rstd[2][128],
 // the epilogue's staging blocks, the mbarriers and the TMEM address slot
 constexpr int kPairSmem = 1024 + kPairStages * (kBM + kBN / 2) * kBK * 2 + 2 * 128 * 4 +
-                          4 * 2 * kOutBox * kOutBox * 2 + 8 * (3 * kPairStages + 8) + 16;
+                          4 * 2 * kOutRows * kOutCols * 2 + 8 * (3 * kPairStages + 8) + 16;
+static_assert(kPairSmem <= kSmemOptinSm103, "the persistent kernel's layout must fit a CTA");
 
 std::mutex g_mu;
 std::map<std::tuple<int64_t, int64_t, int, int>, std::shared_ptr<Module>> g_kernels;
@@ -69,16 +72,17 @@ int encode_kmajor(const DriverApi* api, CUtensorMap* map, const void* ptr, fuse_
   return FUSE_OK;
 }
 
-// The output [M, N] as the destination of 32 x 32 TMA stores (no swizzle).
+// The output [M, N] as the destination of 32-row x 64-column TMA stores from
+// 128-byte swizzled staging blocks.
 int encode_out(const DriverApi* api, CUtensorMap* map, void* ptr, fuse_dtype dt, int64_t M,
                int64_t N) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2};
-  cuuint32_t box[2] = {kOutBox, kOutBox};
+  cuuint32_t box[2] = {kOutCols, kOutRows};
   cuuint32_t elem[2] = {1, 1};
   CUresult r = api->TensorMapEncodeTiled(
       map, dt == FUSE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-      ptr, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+      ptr, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
       CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail(r, "cuTensorMapEncodeTiled(out)");
   return FUSE_OK;
