@@ -193,11 +193,14 @@ __device__ __forceinline__ void st_shared16(u32 addr, uint4 v) {
 // its own TMEM.  Per k-step an SM writes and reads 32 KB of shared memory
 // where a 128 x 256 tile on one SM moves 48 KB each way.
 //
-// Work: runs of PAIR_RUN consecutive 256-column blocks of one pair of row
-// tiles; cluster c takes runs c, c + nclusters, ...  The row statistics of a
+// Work: runs of consecutive 256-column blocks of one pair of row tiles,
+// 2 * PAIR_RUN blocks long for the first mp_long pairs and PAIR_RUN for the
+// rest; cluster c takes runs c, c + nclusters, ...  The row statistics of a
 // run are computed once, on its first block, and kept by the epilogue for
-// the others; runs taken at the same time cover few row tiles, so x stays in
-// L2 for all the blocks that read it.
+// the others, so longer runs read x through shared memory less often; the
+// shorter runs at the end even out the clusters' loads.  Runs taken at the
+// same time cover few row tiles, so x stays in L2 for all the blocks that
+// read it.
 //
 // 10 warps per CTA:
 //   warp 0     TMA producer; both CTAs' copies complete on CTA 0's "full"
@@ -227,6 +230,8 @@ constexpr int PSTAGE_BYTES = A_BYTES + B_HALF;  // per CTA and stage
 constexpr int NACC = PAIR_NACC;                 // accumulator buffers in TMEM
 constexpr int RUN = PAIR_RUN;                   // column blocks per run
 constexpr int RUNS_PER_MP = (NT_TILES + RUN - 1) / RUN;
+constexpr int RUN_LONG = 2 * RUN;                // column blocks per long run
+constexpr int RUNS_PER_MP_LONG = (NT_TILES + RUN_LONG - 1) / RUN_LONG;
 // one epilogue warp's staged block: 32 rows x 64 columns, 128-byte rows in
 // the output tensor map's 128-byte swizzle (so 1024-byte aligned)
 constexpr int OUT_COLS = 64;
@@ -242,7 +247,7 @@ extern "C" __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
 rms_linear_persistent(const __grid_constant__ TensorMap tmap_x,
                       const __grid_constant__ TensorMap tmap_w,
                       const __grid_constant__ TensorMap tmap_out, const u16* __restrict__ bias,
-                      int m_tiles, float eps, float scale, int* err) {
+                      int m_tiles, float eps, float scale, int* err, int mp_long_in) {
   // the layout below, from a base rounded up to 1024 bytes: refuse a launch
   // that gave less.  Launch constants only, so both CTAs of a pair return
   // together and neither waits for the other at the cluster barrier.
@@ -276,12 +281,22 @@ rms_linear_persistent(const __grid_constant__ TensorMap tmap_x,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const u32 rank = cluster_rank();
   const int m_pairs = (m_tiles + 1) / 2;
-  const int runs = m_pairs * RUNS_PER_MP;
+  // the first mp_long row pairs in runs of RUN_LONG blocks, the rest in runs of
+  // RUN (the host picks mp_long so that the long runs leave the clusters'
+  // loads as even as short runs alone would)
+  const int mp_long = max(0, min(mp_long_in, m_pairs));
+  const int runs_long = mp_long * RUNS_PER_MP_LONG;
+  const int runs = runs_long + (m_pairs - mp_long) * RUNS_PER_MP;
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
   // run -> its pair of row tiles, first column block and number of blocks
-  auto run_mp = [&](int run) { return run / RUNS_PER_MP; };
-  auto run_n = [&](int run) { return (run % RUNS_PER_MP) * RUN; };
-  auto run_len = [&](int run) { return min(RUN, NT_TILES - run_n(run)); };
+  auto run_mp = [&](int run) {
+    return run < runs_long ? run / RUNS_PER_MP_LONG : mp_long + (run - runs_long) / RUNS_PER_MP;
+  };
+  auto run_n = [&](int run) {
+    return run < runs_long ? (run % RUNS_PER_MP_LONG) * RUN_LONG
+                           : ((run - runs_long) % RUNS_PER_MP) * RUN;
+  };
+  auto run_len = [&](int run) { return min(run < runs_long ? RUN_LONG : RUN, NT_TILES - run_n(run)); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < PSTAGES; ++s) {

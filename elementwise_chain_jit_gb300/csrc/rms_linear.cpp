@@ -12,6 +12,7 @@
 #include <cmath>
 #include <map>
 #include <tuple>
+#include <vector>
 
 #include "internal.h"
 
@@ -86,6 +87,51 @@ int encode_out(const DriverApi* api, CUtensorMap* map, void* ptr, fuse_dtype dt,
       CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail(r, "cuTensorMapEncodeTiled(out)");
   return FUSE_OK;
+}
+
+// The kernel deals runs of column blocks to its clusters round-robin: the
+// first mp_long row pairs in runs of 2 * kPairRun blocks, the rest in runs of
+// kPairRun.  A long run computes the row statistics once for twice the
+// blocks, but coarse runs can leave the last clusters' loads uneven.  Picks
+// the largest mp_long whose most loaded cluster has no more blocks than with
+// short runs only (every value up to 512 row pairs, 64 evenly spaced ones
+// beyond), cached per shape; also returns the number of runs.
+int64_t pick_mp_long(int64_t m_pairs, int64_t nt, int64_t clusters, int64_t* runs_out) {
+  static std::mutex mu;
+  static std::map<std::tuple<int64_t, int64_t, int64_t>, std::pair<int64_t, int64_t>> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_tuple(m_pairs, nt, clusters);
+  if (auto it = cache.find(key); it != cache.end()) {
+    *runs_out = it->second.second;
+    return it->second.first;
+  }
+  const int64_t c = std::max<int64_t>(1, clusters), run_s = kPairRun, run_l = 2 * kPairRun;
+  std::vector<int64_t> load(static_cast<size_t>(c));
+  auto simulate = [&](int64_t mp_long, int64_t* nruns) {
+    std::fill(load.begin(), load.end(), 0);
+    int64_t idx = 0;
+    for (int64_t mp = 0; mp < m_pairs; ++mp) {
+      const int64_t run = mp < mp_long ? run_l : run_s;
+      for (int64_t n = 0; n < nt; n += run) load[static_cast<size_t>(idx++ % c)] += std::min(run, nt - n);
+    }
+    *nruns = idx;
+    return *std::max_element(load.begin(), load.end());
+  };
+  int64_t runs0;
+  const int64_t bound = simulate(0, &runs0);
+  int64_t best = 0, best_runs = runs0;
+  const int64_t step = m_pairs <= 512 ? 1 : (m_pairs + 63) / 64;
+  for (int64_t mp = m_pairs; mp > 0; mp = mp > step ? mp - step : 0) {
+    int64_t nruns;
+    if (simulate(mp, &nruns) <= bound) {
+      best = mp;
+      best_runs = nruns;
+      break;
+    }
+  }
+  cache.emplace(key, std::make_pair(best, best_runs));
+  *runs_out = best_runs;
+  return best;
 }
 
 // How many 2-CTA clusters of the persistent kernel fit on the device at
@@ -169,9 +215,10 @@ int launch_folded(const void* x, const void* w, const void* bias, void* out, int
   if (int rc = encode_out(api, &mo, out, dt, M, N)) return rc;
   const int64_t m_tiles64 = (M + kBM - 1) / kBM, n_tiles = (N + kBN - 1) / kBN;
   int m_tiles = static_cast<int>(m_tiles64);
-  const int64_t runs = (m_tiles64 + 1) / 2 * ((n_tiles + kPairRun - 1) / kPairRun);
+  int64_t runs;
+  int mp_long = static_cast<int>(pick_mp_long((m_tiles64 + 1) / 2, n_tiles, clusters, &runs));
   const unsigned grid = 2u * static_cast<unsigned>(std::min<int64_t>(runs, clusters));
-  void* args[] = {&mx, &mw, &mo, &bias, &m_tiles, &eps, &scale, &err};
+  void* args[] = {&mx, &mw, &mo, &bias, &m_tiles, &eps, &scale, &err, &mp_long};
   r = api->LaunchKernel(fn, grid, 1, 1, 320, 1, 1, kPairSmem, reinterpret_cast<CUstream>(stream),
                         args, nullptr);
   if (r != CUDA_SUCCESS) return cuda_fail(r, "cuLaunchKernel(rmsnorm_linear)");
