@@ -956,6 +956,14 @@ def run_gpu(args):
         e2e = {"value": job_gbs(step_bytes, world, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                "steps": e2e_steps}
+        # the host link bounds it: the step's copies cannot take less than
+        # max(in / h2d rate, out / d2h rate, (in + out) / both-ways rate)
+        link = link_rates(h_in, h_out, dev)
+        t_min = max(h2d / (link["h2d"] * 1e9), d2h / (link["d2h"] * 1e9),
+                    (h2d + d2h) / (link["both"] * 1e9))
+        bound = job_gbs(step_bytes, world, t_min * 1e3)
+        e2e.update({"link_gbs": link, "link_bound": bound,
+                    "frac_of_link_bound": e2e["value"] / bound})
     cpu = None
     if rank == 0 and not args.no_cpu:
         b, t, desc = cpu_sample(64)
@@ -984,6 +992,40 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def link_rates(h_in, h_out, dev, reps=4):
+    """Host-link copy rates in GB/s, measured in the same run on the e2e
+    pipeline's pinned buffers: host -> device alone, device -> host alone, and
+    both at once on two streams (all bytes over the time)."""
+    import torch
+    nb = min(h_in.numel(), h_out.numel(), 512 << 20)
+    d_in = torch.empty(nb, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(nb, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(up, down):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s1)
+        s2.wait_event(a)
+        for _ in range(reps):
+            if up:
+                with torch.cuda.stream(s1):
+                    d_in.copy_(h_in[:nb], non_blocking=True)
+            if down:
+                with torch.cuda.stream(s2):
+                    h_out[:nb].copy_(d_out, non_blocking=True)
+        s1.wait_stream(s2)
+        b.record(s1)
+        b.synchronize()
+        return reps * nb * (int(up) + int(down)) / (a.elapsed_time(b) / 1e3) / 1e9
+
+    timed(True, True)  # warm
+    rates = {"h2d": timed(True, False), "d2h": timed(False, True), "both": timed(True, True),
+             "bytes_per_copy": nb}
+    del d_in, d_out
+    return rates
 
 
 def device_ops(fn):
