@@ -42,7 +42,8 @@ sys.path.insert(0, ROOT)
 METRIC = "fused-chain HBM GB/s (% of GB300 peak) and µs/chain vs unfused per-op"
 UNIT = "GB/s"
 WORKLOAD = ("all fused chains at full size: chain sweep L=1..32 on 2^28+7 elements and after "
-            "ChannelShuffle(4) on fp16 [32,256,56,56]; RMSNorm+residual bf16 [16384,4096]; "
+            "ChannelShuffle(4) on fp16 [32,256,56,56]; ChannelShuffle(4) alone on the same "
+            "tensor; RMSNorm+residual bf16 [16384,4096]; "
             "QKV split+RoPE bf16 [32768,3x32x128]; add-relu-scale fp32 2^20; detect decode "
             "3 scales fp16 -> fp32 [1,25200,85]")
 FALLBACK_HBM_GBS = 6800.0
@@ -213,6 +214,8 @@ def build_items(dev, with_unfused=True, only=None, flat_elems=None, spec=None, s
         if want(f"shuffle_chain_L{L}"):
             items.append(chain_item(f"shuffle_chain_L{L}", f"shuffle:{cfg['groups']};{body}", dt,
                                     cfg["shape"], 200 + L))
+    if want("channel_shuffle_g4_32x256x56x56_f16"):
+        items.append(_shuffle_item(dev, with_unfused))
     if want("rmsnorm_residual_16384x4096_bf16"):
         items.append(_rms_item(dev, with_unfused))
     if want("rope_qkv_split_32768x32x128_bf16"):
@@ -224,6 +227,29 @@ def build_items(dev, with_unfused=True, only=None, flat_elems=None, spec=None, s
     if want("detect_decode_3scale"):
         items.append(_detect_item(dev, with_unfused))
     return items
+
+
+def _shuffle_item(dev, with_unfused):
+    """ChannelShuffle alone through its entry point: a bit-exact permutation
+    of whole H*W planes; unfused: PyTorch's view -> transpose -> contiguous."""
+    import torch
+
+    import elementwise_chain_jit_gb300 as F
+    import workloads as W
+    cfg = W.SHUFFLE_CHAIN
+    n, c, h, w = cfg["shape"]
+    g = cfg["groups"]
+    x = W.device_uniform(n * c * h * w, cfg["lo"], cfg["hi"], 300, W.F16, dev)
+    out = torch.empty_like(x)
+    it = Item(f"channel_shuffle_g{g}_{n}x{c}x{h}x{w}_f16", 2 * x.numel() * 2,
+              lambda: F.channel_shuffle(x, out, g, W.F16, shape=(n, c, h, w)),
+              kernel=("chain", f"shuffle:{g}", cfg["shape"], W.F16))
+    it.inputs, it.outputs = [x], [out]
+    if with_unfused:
+        def unfused():
+            return x.view(n, g, c // g, h, w).transpose(1, 2).contiguous().view(n, c, h, w)
+        it.unfused, it.n_unfused = unfused, 1  # kernels, as --launch-trace counts them
+    return it
 
 
 def _rms_item(dev, with_unfused):
@@ -644,6 +670,10 @@ def cpu_sample(frac_div: int):
         total_t += clock(lambda: oracle.store(oracle.chain_eval(spec, dt, ins, shape)[0], ch.out_dtype))
         total_b += sum(ns * _esz(d) for d in dts) + ns * _esz(ch.out_dtype)
     parts.append(f"shuffle chains L=1..32 on batch {nb} of [32,256,56,56]")
+    xs = W.uniform(ns, cfg["lo"], cfg["hi"], 300, W.F16).reshape(shape)
+    total_t += clock(lambda: oracle.channel_shuffle(xs, cfg["groups"]))
+    total_b += 2 * ns * 2
+    parts.append(f"channel shuffle on batch {nb}")
     rc = W.RMSNORM
     rows = max(1, rc["rows"] // frac_div)
     x = W.normal((rows, rc["hidden"]), 0, 1, 1, W.BF16)

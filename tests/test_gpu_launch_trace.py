@@ -9,7 +9,8 @@ import bench
 
 pytestmark = pytest.mark.gpu
 
-SMALL = r"add_relu_scale|detect_decode|shuffle_chain_L4$|flat_chain_L2_|rmsnorm_residual|rope_qkv"
+SMALL = (r"add_relu_scale|detect_decode|shuffle_chain_L4$|flat_chain_L2_|rmsnorm_residual|rope_qkv"
+         r"|channel_shuffle")
 
 
 @pytest.fixture(scope="module")
@@ -23,7 +24,7 @@ def items():
 
 
 def test_fused_is_one_launch_and_unfused_counts_match(items):
-    assert len(items) == 8
+    assert len(items) == 9
     for it in items:
         it.fused()
         ops = bench.device_ops(it.fused)
