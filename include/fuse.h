@@ -149,7 +149,8 @@ int rmsnorm_residual(const void* x, const void* residual, const void* weight, vo
  * x [M, K], gamma [K], w [N, K] (K-major, the layout of a Linear weight),
  * bias [N] (may be NULL), out [M, N]; dt f16 or bf16 (accumulation fp32);
  * all tensors 16-byte aligned.
- * Any M >= 0, N % 8 == 0, K % 8 == 0 (K > 0); FUSE_E_SHAPE otherwise.
+ * 0 <= M < 2^31 - 128 (TMA tile coordinates are 32-bit), N % 8 == 0,
+ * 0 < K <= 2^20 with K % 8 == 0; FUSE_E_SHAPE otherwise.
  * The product runs on a weight with gamma folded in, w' = dt(w * gamma), so
  * the rounding of x * gamma falls on w * gamma instead (the same value in
  * exact arithmetic).  gamma NULL means gamma is already folded into w
