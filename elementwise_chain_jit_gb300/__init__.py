@@ -28,7 +28,7 @@ STATUS = {0: "FUSE_OK", -1: "FUSE_E_SPEC", -2: "FUSE_E_SHAPE", -3: "FUSE_E_DTYPE
 # every symbol include/fuse.h declares
 EXPORTS = ["fuse_compile", "fuse_num_inputs", "fuse_input_dtypes", "fuse_launch", "fuse_release",
            "fuse_source", "fuse_compile_bucket", "fuse_launch_rows", "fuse_source_bucket",
-           "fuse_bucket", "rmsnorm_linear", "rmsnorm_linear_fold", "fuse_device_error", "rmsnorm_residual", "layernorm_residual", "rope_qkv_split", "rope_qkv_split_noalloc",
+           "fuse_bucket", "fuse_warmup", "rmsnorm_linear", "rmsnorm_linear_fold", "fuse_device_error", "rmsnorm_residual", "layernorm_residual", "rope_qkv_split", "rope_qkv_split_noalloc",
            "detect_decode", "channel_shuffle", "fuse_graph_begin", "fuse_graph_end",
            "fuse_graph_launch", "fuse_graph_nodes", "fuse_graph_release", "fuse_last_error",
            "fuse_stats", "fuse_device_sms", "fuse_selftest_bounded_wait"]
@@ -59,6 +59,7 @@ _lib.fuse_launch_rows.argtypes = [_P, ctypes.POINTER(_P), _I, _P, _I64, _P]
 _lib.fuse_source_bucket.argtypes = [ctypes.c_char_p, ctypes.POINTER(_I64), _I, _I, ctypes.c_char_p,
                                     ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
 _lib.fuse_bucket.argtypes = [_I64, ctypes.POINTER(_I64)]
+_lib.fuse_warmup.argtypes = [ctypes.c_char_p, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)]
 _lib.rmsnorm_residual.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _F, _I, _P]
 _lib.rmsnorm_linear.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _F, _I, _P]
 _lib.fuse_device_error.argtypes = [ctypes.POINTER(_I)]
@@ -210,6 +211,27 @@ def fuse_bucket(n: int) -> int:
     b = _I64()
     _check(_lib.fuse_bucket(int(n), ctypes.byref(b)))
     return b.value
+
+
+_DT_NAMES = {F32: "f32", F16: "f16", BF16: "bf16"}
+
+
+def fuse_warmup(entries, threads: int = 0) -> tuple[int, int]:
+    """Compiles a warm-up list into the library's cache (see fuse.h).  Each
+    entry is a line 'spec | d0,d1,... | dtype [| bucket]' or a tuple
+    (spec, shape, dtype[, bucket]).  Returns (compiled, already cached)."""
+    lines = []
+    for e in entries:
+        if isinstance(e, str):
+            lines.append(e)
+        else:
+            dims = ",".join(str(int(d)) for d in e[1])
+            line = f"{e[0]} | {dims} | {_DT_NAMES[_dtype(e[2])]}"
+            lines.append(line + (" | bucket" if len(e) > 3 and e[3] else ""))
+    c, h = _I(), _I()
+    _check(_lib.fuse_warmup("\n".join(lines).encode(), int(threads), ctypes.byref(c),
+                            ctypes.byref(h)))
+    return c.value, h.value
 
 
 # ---------------------------------------------------------------- fixed entry points

@@ -13,7 +13,6 @@
 #include "internal.h"
 
 namespace fuse {
-const char* last_error_cstr();
 void read_stats(int64_t* c, int64_t* h, int64_t* l, double* ms);
 int chain_compile(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_dt,
                   fuse_chain** out, bool bucket);

@@ -13,10 +13,13 @@
 // thread, several vectors in flight per thread, a grid of (SMs x resident
 // CTAs) looping over whole chunks, and one CTA finishing the ragged remainder
 // and the scalar tail after its share of the main loop.
+#include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <sstream>
+#include <thread>
 
 #include "internal.h"
 
@@ -565,6 +568,97 @@ int fuse_compile_bucket(const char* spec, const int64_t* shape, int ndim, fuse_d
   if (!out) return fuse::fail(FUSE_E_NULL, "out is NULL");
   *out = nullptr;
   return fuse::chain_compile(spec, shape, ndim, in_dtype, out, true);
+}
+
+int fuse_warmup(const char* list, int threads, int* compiled, int* cached) {
+  fuse::NvtxRange nvtx_range("fuse_warmup");
+  using namespace fuse;
+  if (compiled) *compiled = 0;
+  if (cached) *cached = 0;
+  if (!list) return fail(FUSE_E_NULL, "list is NULL");
+  auto trim = [](std::string t) {
+    const size_t a = t.find_first_not_of(" \t\r"), b = t.find_last_not_of(" \t\r");
+    return a == std::string::npos ? std::string() : t.substr(a, b - a + 1);
+  };
+  // every line: spec | d0,d1,... | dtype [| bucket]; its kernel source
+  struct Entry {
+    int line;
+    std::string source;
+  };
+  std::vector<Entry> entries;
+  std::istringstream in(list);
+  std::string text;
+  for (int ln = 1; std::getline(in, text); ++ln) {
+    text = trim(text);
+    if (text.empty() || text[0] == '#') continue;
+    std::vector<std::string> f;
+    for (size_t a = 0;;) {
+      const size_t b = text.find('|', a);
+      f.push_back(trim(text.substr(a, b == std::string::npos ? std::string::npos : b - a)));
+      if (b == std::string::npos) break;
+      a = b + 1;
+    }
+    if (f.size() < 3 || f.size() > 4 || (f.size() == 4 && f[3] != "bucket"))
+      return fail(FUSE_E_SPEC,
+                  fmt("warm-up list line %d: want 'spec | d0,d1,... | f32|f16|bf16 [| bucket]'", ln));
+    std::vector<int64_t> shape;
+    for (size_t a = 0;;) {
+      const size_t b = f[1].find(',', a);
+      const std::string d = trim(f[1].substr(a, b == std::string::npos ? std::string::npos : b - a));
+      char* end = nullptr;
+      const long long v = strtoll(d.c_str(), &end, 10);
+      if (d.empty() || *end || v < 0)
+        return fail(FUSE_E_SHAPE, fmt("warm-up list line %d: bad dimension '%s'", ln, d.c_str()));
+      shape.push_back(v);
+      if (b == std::string::npos) break;
+      a = b + 1;
+    }
+    const fuse_dtype dt = f[2] == "f32" ? FUSE_F32 : f[2] == "f16" ? FUSE_F16 : FUSE_BF16;
+    if (f[2] != "f32" && f[2] != "f16" && f[2] != "bf16")
+      return fail(FUSE_E_DTYPE, fmt("warm-up list line %d: dtype '%s'", ln, f[2].c_str()));
+    ChainPlan p;
+    if (int rc = plan_chain(f[0].c_str(), shape.data(), static_cast<int>(shape.size()), dt, &p))
+      return fail(rc, fmt("warm-up list line %d: %s", ln, last_error_cstr()));
+    p.dynamic = f.size() == 4;
+    entries.push_back({ln, gen_chain_source(p, f[0].c_str())});
+  }
+  // compile on worker threads (distinct sources compile in parallel); the
+  // first error, with its line, is reported on the calling thread
+  const int n = static_cast<int>(entries.size());
+  int nt = threads > 0 ? threads : static_cast<int>(std::thread::hardware_concurrency());
+  nt = std::max(1, std::min({nt, 16, n}));
+  std::atomic<int> next{0}, n_compiled{0}, n_cached{0};
+  std::mutex err_mu;
+  int err_rc = FUSE_OK;
+  std::string err_msg;
+  auto work = [&] {
+    for (int i; (i = next.fetch_add(1)) < n;) {
+      {
+        std::lock_guard<std::mutex> lk(err_mu);
+        if (err_rc != FUSE_OK) return;
+      }
+      std::shared_ptr<Module> m;
+      bool fresh = false;
+      if (int rc = jit_compile(entries[i].source, "fuse_chain", &m, &fresh)) {
+        std::lock_guard<std::mutex> lk(err_mu);
+        if (err_rc == FUSE_OK) {
+          err_rc = rc;
+          err_msg = fmt("warm-up list line %d: ", entries[i].line) + last_error_cstr();
+        }
+        return;
+      }
+      (fresh ? n_compiled : n_cached).fetch_add(1);
+    }
+  };
+  std::vector<std::thread> pool;
+  for (int t = 1; t < nt; ++t) pool.emplace_back(work);
+  work();
+  for (auto& t : pool) t.join();
+  if (err_rc != FUSE_OK) return fail(err_rc, err_msg);
+  if (compiled) *compiled = n_compiled.load();
+  if (cached) *cached = n_cached.load();
+  clear_error();
+  return FUSE_OK;
 }
 
 int fuse_bucket(int64_t n, int64_t* bucket) {

@@ -19,6 +19,7 @@ namespace fuse {
 // returns `code` (so call sites read `return fail(FUSE_E_ARG, "...")`).
 int fail(int code, const std::string& msg);
 void clear_error();
+const char* last_error_cstr();  // the calling thread's last-error message
 std::string fmt(const char* f, ...) __attribute__((format(printf, 1, 2)));
 
 struct Stats {
@@ -113,7 +114,11 @@ struct Module {
 
 // Compile `source` (cache key: source + arch + options) or fetch it from the
 // cache.  `name` is used in messages only.
-int jit_compile(const std::string& source, const std::string& name, std::shared_ptr<Module>* out);
+// Thread-safe: the same source compiles once (later callers wait for it),
+// distinct sources compile in parallel.  *compiled (if given) tells whether
+// NVRTC ran, as opposed to a memory or disk cache hit.
+int jit_compile(const std::string& source, const std::string& name, std::shared_ptr<Module>* out,
+                bool* compiled = nullptr);
 
 // The kernel `fn_name` of module m on the current device (loads the module
 // there on first use).

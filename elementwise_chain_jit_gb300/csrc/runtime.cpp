@@ -11,12 +11,14 @@
 
 #include <atomic>
 #include <chrono>
+#include <condition_variable>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <fstream>
 #include <unordered_map>
+#include <unordered_set>
 
 #include "internal.h"
 
@@ -251,7 +253,9 @@ int default_sms() {
 
 namespace {
 std::mutex g_cache_mu;
+std::condition_variable g_cache_cv;
 std::unordered_map<std::string, std::shared_ptr<Module>> g_cache;
+std::unordered_set<std::string> g_in_flight;  // keys a thread is compiling now
 
 uint64_t fnv1a(const std::string& s) {
   uint64_t h = 1469598103934665603ull;
@@ -347,62 +351,89 @@ void disk_store(const std::string& key, const std::vector<char>& cubin) {
 }
 }  // namespace
 
-int jit_compile(const std::string& source, const std::string& name, std::shared_ptr<Module>* out) {
+namespace {
+
+// NVRTC (or the disk cache) for one source, outside the cache lock.
+int compile_module(const std::string& key, const std::string& source, const std::string& name,
+                   const std::vector<std::string>& opts, Module* m, bool* from_disk) {
+  m->name = name;
+  *from_disk = disk_load(key, &m->cubin);
+  if (*from_disk) return FUSE_OK;
+  if (const char* e = getenv("FUSE_VERBOSE"); e && *e == '1')
+    fprintf(stderr, "[fuse] compiling %s:\n%s\n", name.c_str(), source.c_str());
+  std::vector<const char*> hdr_text, hdr_name;
+  for (int i = 0; i < kNumEmbeddedHeaders; ++i) {
+    hdr_text.push_back(kEmbeddedHeaders[i].text);
+    hdr_name.push_back(kEmbeddedHeaders[i].name);
+  }
+  nvrtcProgram prog;
+  nvrtcResult r = nvrtcCreateProgram(&prog, source.c_str(), (name + ".cu").c_str(),
+                                     kNumEmbeddedHeaders, hdr_text.data(), hdr_name.data());
+  if (r != NVRTC_SUCCESS)
+    return fail(FUSE_E_COMPILE, fmt("nvrtcCreateProgram: %s", nvrtcGetErrorString(r)));
+  std::vector<const char*> copt;
+  for (auto& o : opts) copt.push_back(o.c_str());
+  r = nvrtcCompileProgram(prog, static_cast<int>(copt.size()), copt.data());
+  size_t log_size = 0;
+  nvrtcGetProgramLogSize(prog, &log_size);
+  m->log.resize(log_size);
+  if (log_size) nvrtcGetProgramLog(prog, &m->log[0]);
+  while (!m->log.empty() && m->log.back() == '\0') m->log.pop_back();
+  if (r != NVRTC_SUCCESS) {
+    nvrtcDestroyProgram(&prog);
+    return fail(FUSE_E_COMPILE,
+                fmt("NVRTC failed on %s: %s\n", name.c_str(), nvrtcGetErrorString(r)) + m->log);
+  }
+  size_t n = 0;
+  nvrtcGetCUBINSize(prog, &n);
+  m->cubin.resize(n);
+  nvrtcGetCUBIN(prog, m->cubin.data());
+  nvrtcDestroyProgram(&prog);
+  disk_store(key, m->cubin);
+  if (const char* e = getenv("FUSE_PTXAS_VERBOSE"); e && *e == '1')
+    fprintf(stderr, "[fuse] %s:\n%s\n", name.c_str(), m->log.c_str());
+  return FUSE_OK;
+}
+
+}  // namespace
+
+int jit_compile(const std::string& source, const std::string& name, std::shared_ptr<Module>* out,
+                bool* compiled) {
+  if (compiled) *compiled = false;
   std::vector<std::string> opts = nvrtc_options();
   std::string key = "sm_103a\n";
   for (auto& o : opts) key += o + "\n";
   key += source;
-
-  std::lock_guard<std::mutex> lk(g_cache_mu);
-  auto it = g_cache.find(key);
-  if (it != g_cache.end()) {
-    stat_hit();
-    *out = it->second;
-    return FUSE_OK;
+  {
+    std::unique_lock<std::mutex> lk(g_cache_mu);
+    for (;;) {
+      auto it = g_cache.find(key);
+      if (it != g_cache.end()) {
+        stat_hit();
+        *out = it->second;
+        return FUSE_OK;
+      }
+      if (!g_in_flight.count(key)) break;
+      g_cache_cv.wait(lk);  // another thread compiles this source: take its module
+    }
+    g_in_flight.insert(key);
   }
+  // distinct sources compile in parallel; the same source only once
   auto m = std::make_shared<Module>();
-  m->name = name;
+  bool from_disk = false;
   auto t0 = std::chrono::steady_clock::now();
-  const bool from_disk = disk_load(key, &m->cubin);
-  if (!from_disk) {
-    if (const char* e = getenv("FUSE_VERBOSE"); e && *e == '1')
-      fprintf(stderr, "[fuse] compiling %s:\n%s\n", name.c_str(), source.c_str());
-    std::vector<const char*> hdr_text, hdr_name;
-    for (int i = 0; i < kNumEmbeddedHeaders; ++i) {
-      hdr_text.push_back(kEmbeddedHeaders[i].text);
-      hdr_name.push_back(kEmbeddedHeaders[i].name);
-    }
-    nvrtcProgram prog;
-    nvrtcResult r = nvrtcCreateProgram(&prog, source.c_str(), (name + ".cu").c_str(),
-                                       kNumEmbeddedHeaders, hdr_text.data(), hdr_name.data());
-    if (r != NVRTC_SUCCESS)
-      return fail(FUSE_E_COMPILE, fmt("nvrtcCreateProgram: %s", nvrtcGetErrorString(r)));
-    std::vector<const char*> copt;
-    for (auto& o : opts) copt.push_back(o.c_str());
-    r = nvrtcCompileProgram(prog, static_cast<int>(copt.size()), copt.data());
-    size_t log_size = 0;
-    nvrtcGetProgramLogSize(prog, &log_size);
-    m->log.resize(log_size);
-    if (log_size) nvrtcGetProgramLog(prog, &m->log[0]);
-    while (!m->log.empty() && m->log.back() == '\0') m->log.pop_back();
-    if (r != NVRTC_SUCCESS) {
-      nvrtcDestroyProgram(&prog);
-      return fail(FUSE_E_COMPILE, fmt("NVRTC failed on %s: %s\n", name.c_str(),
-                                      nvrtcGetErrorString(r)) + m->log);
-    }
-    size_t n = 0;
-    nvrtcGetCUBINSize(prog, &n);
-    m->cubin.resize(n);
-    nvrtcGetCUBIN(prog, m->cubin.data());
-    nvrtcDestroyProgram(&prog);
-    disk_store(key, m->cubin);
-    if (const char* e = getenv("FUSE_PTXAS_VERBOSE"); e && *e == '1')
-      fprintf(stderr, "[fuse] %s:\n%s\n", name.c_str(), m->log.c_str());
+  const int rc = compile_module(key, source, name, opts, m.get(), &from_disk);
+  {
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    g_in_flight.erase(key);
+    if (rc == FUSE_OK) g_cache.emplace(key, m);
   }
+  g_cache_cv.notify_all();  // waiters find the module, or compile (and fail) themselves
+  if (rc != FUSE_OK) return rc;
   double ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
   if (from_disk) stat_hit();  // a disk load counts as a cache hit, not a compile
   else stat_compile(ms);
-  g_cache.emplace(key, m);
+  if (compiled) *compiled = !from_disk;
   *out = m;
   return FUSE_OK;
 }

@@ -124,6 +124,22 @@ int fuse_source_bucket(const char* spec, const int64_t* shape, int ndim, fuse_dt
                        char* buf, size_t cap, size_t* len);
 int fuse_bucket(int64_t n, int64_t* bucket);
 
+/* Warm-up list ("DeepJIT" sections 3.3 and 6.2: compile the common shapes
+ * before serving, so that no launch ever compiles).  `list` holds one chain
+ * per line:
+ *     <spec> | <d0>,<d1>,... | f32|f16|bf16 [| bucket]
+ * (the arguments of fuse_compile, or of fuse_compile_bucket with the fourth
+ * field); blank lines and lines starting with '#' are skipped.  Every chain
+ * is compiled, or loaded from the disk cache, into the library's cache on up
+ * to `threads` host threads (0: one per core; at most 16); distinct chains
+ * compile in parallel.  A later fuse_compile of the same chain, shape and
+ * dtype then takes no compile.  *compiled and *cached (either may be NULL)
+ * receive how many entries NVRTC compiled and how many were cached already
+ * (in memory or on disk).  A line that does not parse returns FUSE_E_SPEC,
+ * FUSE_E_SHAPE or FUSE_E_DTYPE with its line number in fuse_last_error();
+ * compile errors as fuse_compile.  Needs no GPU. */
+int fuse_warmup(const char* list, int threads, int* compiled, int* cached);
+
 /* ------------------------------------------------------------------------
  * Residual add + RMSNorm + cast ("TeleTron", sections 3.3 and 4.2).
  * Per row r of [rows, hidden]:
