@@ -148,3 +148,26 @@ def test_gamma_path_on_two_streams_at_once():
         want, mag = oracle.rmsnorm_linear(x, gs[i], w, None, dt, 1e-6, 1.0)
         got = oracle.to_double(to_host(outs[i], dt), dt).reshape(M, N)
         assert not (np.abs(got - want) > 8e-3 * mag).any()
+
+
+def test_mixed_run_schedule_every_row():
+    """16384 x 4096 on the GPU's clusters deals runs of 4 column blocks for most
+    row pairs and runs of 2 for the last ones: every row is checked, on columns
+    from each of the 16 column blocks (an output column depends only on its
+    row of w, so the oracle takes just those rows of w)."""
+    M, N, K, dt = 16384, 4096, 64, F.BF16
+    x = workloads.normal((M, K), 0, 1, 90, dt)
+    g = workloads.normal(K, 1, 0.1, 91, dt)
+    w = workloads.normal((N, K), 0, 1 / np.sqrt(K), 92, dt)
+    b = workloads.normal(N, 0, 0.5, 93, dt)
+    out = torch.empty(M * N, dtype=torch.bfloat16, device="cuda")
+    F.rmsnorm_linear(to_dev(x.reshape(-1), dt), to_dev(g, dt), to_dev(w.reshape(-1), dt),
+                     to_dev(b, dt), out, 1e-6, 0.5, dt, M=M, N=N, K=K)
+    torch.cuda.synchronize()
+    assert F.fuse_device_error() == 0
+    cols = np.unique(np.concatenate([np.arange(0, N, 256), np.arange(255, N, 256),
+                                     np.random.default_rng(9).integers(0, N, 32)]))
+    want, mag = oracle.rmsnorm_linear(x, g, w[cols], b[cols], dt, 1e-6, 0.5)
+    got = oracle.to_double(to_host(out.view(M, N)[:, torch.from_numpy(cols).cuda()], dt), dt)
+    bad = np.abs(got - want) > 8e-3 * mag
+    assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], want[bad][:5])
