@@ -385,9 +385,10 @@ def _detect_item(dev, with_unfused):
              for s, (h, w_) in enumerate(dc["hw"])]
     nrows = sum(dc["na"] * h * w_ for h, w_ in dc["hw"])
     dout = torch.empty(nrows * dc["no"], dtype=torch.float32, device=dev)
+    # the fixed arguments converted once, as a caller decoding every frame would
+    dec = F.DetectDecoder(dc["hw"], dc["strides"], anchors, dc["na"], dc["no"], W.F16)
     it = Item("detect_decode_3scale", sum(f.numel() * 2 for f in feats) + dout.numel() * 4,
-              lambda: F.detect_decode(feats, dc["hw"], dc["strides"], anchors, dc["na"], dc["no"],
-                                      dout, W.F16),
+              lambda: dec(feats, dout),
               kernel=("detect",))
     it.inputs, it.outputs = feats, [dout]
     if with_unfused:

@@ -329,6 +329,28 @@ def detect_decode(feats, hw, strides, anchors, na: int, no: int, out, in_dt=None
                               _stream(stream)))
 
 
+class DetectDecoder:
+    """detect_decode with its fixed arguments -- per-scale shapes, strides,
+    anchors, anchors per cell, outputs per anchor, input dtype -- converted
+    once; a call passes only the feature maps, the output and the stream
+    (about half the host time of a detect_decode call)."""
+
+    def __init__(self, hw, strides, anchors, na: int, no: int, in_dt):
+        self.ns, self.na, self.no, self.dt = len(hw), int(na), int(no), _dtype(in_dt)
+        self._hw = (_I * (2 * self.ns))(*[int(d) for pair in hw for d in pair])
+        self._st = (_F * self.ns)(*[float(v) for v in strides])
+        flat = [float(a) for a in _flatten(anchors)]
+        self._an = (_F * len(flat))(*flat)
+        self._feats = _P * self.ns
+
+    def __call__(self, feats, out, stream=None) -> None:
+        if len(feats) != self.ns:
+            raise ValueError(f"{self.ns} feature maps expected, got {len(feats)}")
+        _check(_lib.detect_decode(self._feats(*[_ptr(f) for f in feats]), self._hw, self._st,
+                                  self._an, self.ns, self.na, self.no, self.dt, _ptr(out),
+                                  _stream(stream)))
+
+
 def channel_shuffle(x, out, groups: int, dt=None, shape=None, stream=None) -> None:
     n, c, h, w = shape if shape is not None else x.shape
     if dt is None:

@@ -276,6 +276,25 @@ def test_detect_full_config():
     _detect_case(cfg["hw"], F.F16, cfg["seed"])
 
 
+def test_detect_decoder_object_matches_the_function():
+    """DetectDecoder converts the fixed arguments once; its calls give the
+    same bits as detect_decode on the same inputs, frame after frame."""
+    cfg = workloads.DETECT
+    hw, na, no = cfg["hw"], cfg["na"], cfg["no"]
+    anchors = workloads.detect_anchors(cfg["strides"], na)
+    rows = sum(na * h * w for h, w in hw)
+    dec = F.DetectDecoder(hw, cfg["strides"], anchors, na, no, F.F16)
+    for frame in range(3):
+        feats = [workloads.device_normal((1, na * no, h, w), 0, 2.0, 70 + 3 * frame + s, F.F16,
+                                         "cuda") for s, (h, w) in enumerate(hw)]
+        a = torch.empty(rows * no, dtype=torch.float32, device="cuda")
+        b = torch.empty_like(a)
+        dec(feats, a)
+        F.detect_decode(feats, hw, cfg["strides"], anchors, na, no, b, F.F16)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("hw", [[(1, 1)], [(3, 3), (2, 1), (1, 2)], [(8, 8), (4, 4), (2, 2)],
                                 [(13, 7), (5, 9)], [(80, 80), (40, 40), (20, 20), (10, 10)]])
 @pytest.mark.parametrize("dt", [F.F16, F.F32, F.BF16])

@@ -219,3 +219,9 @@ def test_empty_inputs_succeed_without_a_launch():
     F.fuse_launch(c, [256, 256], 256)
     F.channel_shuffle(256, 512, 4, F.F16, shape=(0, 8, 4, 4))
     assert F.fuse_stats()["launches"] == before
+
+
+def test_detect_decoder_checks_the_feature_count():
+    dec = F.DetectDecoder([(8, 8), (4, 4)], [8, 16], [[[1, 2]] * 3] * 2, 3, 85, F.F16)
+    with pytest.raises(ValueError):
+        dec([256], 256, stream=0)
