@@ -992,8 +992,7 @@ def run_gpu(args):
         # each way) is reported but not used: when one direction is much
         # slower its time measures that direction, not a shared capacity
         link = link_rates(h_in, h_out, dev)
-        t_min = max(h2d / (link["h2d"] * 1e9), d2h / (link["d2h"] * 1e9))
-        bound = job_gbs(step_bytes, world, t_min * 1e3)
+        bound = link_bound(step_bytes, world, h2d, d2h, link)
         e2e.update({"link_gbs": link, "link_bound": bound,
                     "frac_of_link_bound": e2e["value"] / bound})
     cpu = None
@@ -1024,6 +1023,15 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def link_bound(step_bytes, world, h2d_bytes, d2h_bytes, link):
+    """The most an end-to-end step can reach (GB/s of its algorithmic bytes)
+    when its copies are the only limit: the inputs cannot arrive faster than
+    the host-to-device rate nor the outputs leave faster than the
+    device-to-host rate, each measured alone."""
+    t_min = max(h2d_bytes / (link["h2d"] * 1e9), d2h_bytes / (link["d2h"] * 1e9))
+    return job_gbs(step_bytes, world, t_min * 1e3)
 
 
 def link_rates(h_in, h_out, dev, reps=4):

@@ -47,3 +47,19 @@ def test_mufu_count_of_a_chain():
 def test_cpu_all_cores_sample_uses_every_core():
     b, t, threads, desc = bench.cpu_sample_all_cores(4096)
     assert b > 0 and t > 0 and threads == (os.cpu_count() or 1) and "slices" in desc
+
+
+def test_link_bound_takes_the_slower_direction():
+    step, h2d, d2h = 29.0e9, 22.7e9, 6.3e9
+    # fast both ways: the inputs bind (22.7 GB at 210 GB/s)
+    fast = bench.link_bound(step, 1, h2d, d2h, {"h2d": 210.0, "d2h": 193.0, "both": 340.0})
+    assert fast == pytest.approx(step / (h2d / 210e9) / 1e9)
+    # slow device-to-host: still the inputs (6.3 GB at 67 GB/s is 94 ms < 108 ms)
+    slow = bench.link_bound(step, 1, h2d, d2h, {"h2d": 210.0, "d2h": 67.0, "both": 122.0})
+    assert slow == pytest.approx(fast)
+    # slower still: the outputs bind
+    slower = bench.link_bound(step, 1, h2d, d2h, {"h2d": 210.0, "d2h": 20.0, "both": 100.0})
+    assert slower == pytest.approx(step / (d2h / 20e9) / 1e9)
+    # two ranks move twice the bytes in the same time
+    assert bench.link_bound(step, 2, h2d, d2h, {"h2d": 210.0, "d2h": 193.0}) == \
+        pytest.approx(2 * fast)
