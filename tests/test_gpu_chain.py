@@ -341,3 +341,27 @@ def test_shuffled_chain_past_2_to_the_31_elements():
     host_x = to_host(x, dt)  # the oracle evaluates the sampled outputs from the whole input
     del x
     _check(spec, dt, [host_x], shape, got, idx=idx)
+
+
+# ------------------------------------------------------------ output over an input
+
+@pytest.mark.parametrize("over", [0, 2])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_output_written_over_an_input(over, offset):
+    """fuse.h allows the output to be the same pointer as an input of its
+    dtype: every element is read before the thread that owns it writes it."""
+    spec, dt, n = "add;mul;relu;sigmoid;scale:0.75", F.F32, 10_007
+    inputs, _ = workloads.chain_inputs(spec, dt, n, 60 + over)
+    c = F.fuse_compile(spec, (n,), dt)
+    dev = [to_dev(a, d) for a, d in zip(inputs, c.in_dtypes)]
+    if offset:
+        dev = [misaligned_copy(t, offset) for t in dev]
+    F.fuse_launch(c, dev, dev[over])
+    torch.cuda.synchronize()
+    got = to_host(dev[over], c.out_dtype)
+    fails, counts, _ = oracle.chain_check(spec, dt, inputs, (n,), got)
+    assert fails == 0, counts
+    # the other inputs are untouched
+    for j, (t, a) in enumerate(zip(dev, inputs)):
+        if j != over:
+            assert np.array_equal(to_host(t, c.in_dtypes[j]), a)
