@@ -787,6 +787,8 @@ def run_gpu(args):
         raise SystemExit(f"--only {args.only!r} matches no workload")
     if args.launch_trace:
         return run_launch_trace(args, items, dev)
+    if args.sequences_once:
+        return run_sequences_once(args, items, dev)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     step_bytes = sum(it.bytes for it in items)
@@ -1122,6 +1124,38 @@ def launch_trace(items):
     return out
 
 
+def run_sequences_once(args, items, dev):
+    """Each workload's fused call, then its unfused sequence, once each inside
+    an NVTX range named "seq" (after an untimed warm-up of both), for a
+    profiler that counts per-kernel DRAM bytes:
+        ncu --nvtx --nvtx-include "seq/" --metrics dram__bytes_read.sum,... \
+            python bench.py --sequences-once
+    Prints the workloads in order with their unfused kernel counts, which
+    attribute the profiler's kernel list to them."""
+    import torch
+    extra = []
+    if args.only is None or re.search(args.only, "layernorm_residual_16384x4096_bf16"):
+        extra.append(_ln_item(dev, with_unfused=True))
+    if args.only is None or re.search(args.only, "rmsnorm_linear"):
+        extra.append(_rms_linear_item(dev, with_unfused=True, M=args.rl_m))
+    order = []
+    for it in items + extra:
+        it.fused()
+        if it.unfused is not None:
+            it.unfused()
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("seq")
+        it.fused()
+        if it.unfused is not None:
+            it.unfused()
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+        order.append({"name": it.name, "bytes": it.bytes,
+                      "unfused_kernels": it.n_unfused if it.unfused is not None else 0})
+    print(json.dumps({"sequences": order}))
+    return 0
+
+
 def run_launch_trace(args, items, dev):
     extra = []
     if args.only is None or re.search(args.only, "layernorm_residual_16384x4096_bf16"):
@@ -1148,6 +1182,9 @@ def main():
     ap.add_argument("--spec-dtype", default="f32", choices=["f32", "f16", "bf16"])
     ap.add_argument("--launch-trace", action="store_true",
                     help="print device-op counts and gaps of fused vs unfused sequences instead")
+    ap.add_argument("--sequences-once", action="store_true",
+                    help="run each fused call and unfused sequence once in an NVTX range "
+                         "'seq', for a profiler")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
