@@ -62,3 +62,66 @@ def test_graph_replays_a_mixed_sequence_bit_exactly():
             t.zero_()
         torch.cuda.synchronize()
     g.release()
+
+
+def test_graph_with_layernorm_detect_shuffle_and_tensor_core_kernels():
+    """A captured sequence with the LayerNorm and detect kernels, a plain
+    ChannelShuffle, and the tcgen05 RMSNorm -> Linear on both of its paths:
+    folded weight (one cluster launch) and gamma per call, whose scratch copy
+    of w is allocated and freed on the stream (memory nodes in the graph)."""
+    dev = torch.device("cuda")
+    s = torch.cuda.Stream()
+    rows, hidden = 40, 2048
+    x = workloads.device_normal((rows, hidden), 0, 1, 71, F.BF16)
+    r = workloads.device_normal((rows, hidden), 0, 1, 72, F.BF16)
+    g = workloads.device_normal((hidden,), 1, 0.1, 73, F.BF16)
+    b = workloads.device_normal((hidden,), 0, 0.1, 74, F.BF16)
+    ly, lro = torch.empty_like(x), torch.empty_like(x)
+    hw, strides, na, no = [(8, 8), (4, 4)], [8.0, 16.0], 3, 85
+    anchors = workloads.detect_anchors(strides, na)
+    feats = [workloads.device_normal((1, na * no, h, w_), 0, 2, 75 + i, F.F16)
+             for i, (h, w_) in enumerate(hw)]
+    dout = torch.empty(sum(na * h * w_ for h, w_ in hw) * no, dtype=torch.float32, device=dev)
+    dec = F.DetectDecoder(hw, strides, anchors, na, no, F.F16)
+    sx = workloads.device_uniform(2 * 16 * 8 * 8, -2, 2, 77, F.F16)
+    so = torch.empty_like(sx)
+    M, N, K = 300, 264, 136
+    xm = workloads.device_normal((M, K), 0, 1, 78, F.BF16)
+    gm = workloads.device_normal((K,), 1, 0.1, 79, F.BF16)
+    wm = workloads.device_normal((N, K), 0, K ** -0.5, 80, F.BF16)
+    bm = workloads.device_normal((N,), 0, 0.5, 81, F.BF16)
+    wf = torch.empty_like(wm)
+    F.rmsnorm_linear_fold(wm, gm, wf, F.BF16)
+    o_fold = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    o_gamma = torch.empty_like(o_fold)
+
+    def sequence():
+        F.layernorm_residual(x, r, g, b, ly, lro, 1e-5, F.BF16, stream=s)
+        dec(feats, dout, stream=s)
+        F.channel_shuffle(sx, so, 4, F.F16, shape=(2, 16, 8, 8), stream=s)
+        F.rmsnorm_linear(xm, None, wf, bm, o_fold, 1e-6, 0.5, F.BF16, stream=s)
+        F.rmsnorm_linear(xm, gm, wm, bm, o_gamma, 1e-6, 0.5, F.BF16, stream=s)
+
+    outs = [ly, lro, dout, so, o_fold, o_gamma]
+    with torch.cuda.stream(s):
+        sequence()
+    s.synchronize()
+    assert F.fuse_device_error() == 0
+    want = [t.clone() for t in outs]
+    for t in outs:
+        t.zero_()
+    torch.cuda.synchronize()
+    F.fuse_graph_begin(s)
+    sequence()
+    gr = F.fuse_graph_end(s)
+    assert gr.nodes >= 6  # six kernels, plus the gamma path's memory nodes
+    for _ in range(3):
+        gr.launch(s)
+        s.synchronize()
+        for a, w_ in zip(outs, want):
+            assert torch.equal(a.view(torch.uint8), w_.view(torch.uint8))
+        for t in outs:
+            t.zero_()
+        torch.cuda.synchronize()
+    assert F.fuse_device_error() == 0
+    gr.release()
