@@ -279,6 +279,101 @@ def _rms_item(dev, with_unfused):
     return it
 
 
+def decode_glue(dev, layers=32, tokens=8, hidden=4096, heads=32, head_dim=128, ffn=11008,
+                pos0=1000, reps=20):
+    """The elementwise glue of a decoder's decode step, the multi-launch
+    sequence "DeepJIT" section 6.1 measures per op, as a CUDA graph, and fused:
+    per layer, residual + RMSNorm, QKV split + RoPE, a SwiGLU gate
+    (sigmoid(g) * g * u as the chain sigmoid;mul;mul) and residual + RMSNorm
+    again, at `tokens` tokens; the matrix products between them are not part of
+    it.  Returns the time of one whole step (all layers), in microseconds,
+    (a) as PyTorch eager ops, (b) those replayed from one CUDA graph, (c) the
+    library's fused calls from a host loop, (d) those replayed from one
+    library graph."""
+    import torch
+
+    import elementwise_chain_jit_gb300 as F
+    import workloads as W
+    bf = torch.bfloat16
+    x = [W.device_normal((tokens, hidden), 0, 1, 900 + i, W.BF16, dev) for i in range(layers)]
+    r = [W.device_normal((tokens, hidden), 0, 1, 1000 + i, W.BF16, dev) for i in range(layers)]
+    wn = W.device_normal((hidden,), 1, 0.1, 1100, W.BF16, dev)
+    qkv = [W.device_normal((tokens, 3 * heads * head_dim), 0, 1, 1200 + i, W.BF16, dev)
+           for i in range(layers)]
+    gate = [W.device_normal((tokens, ffn), 0, 1, 1300 + i, W.BF16, dev) for i in range(layers)]
+    up = [W.device_normal((tokens, ffn), 0, 1, 1400 + i, W.BF16, dev) for i in range(layers)]
+    y, ro = torch.empty_like(x[0]), torch.empty_like(x[0])
+    y2, ro2 = torch.empty_like(x[0]), torch.empty_like(x[0])
+    q, k, v = (torch.empty(heads * tokens * head_dim, dtype=bf, device=dev) for _ in range(3))
+    act = torch.empty_like(gate[0])
+    swiglu = F.fuse_compile("sigmoid;mul;mul", (tokens, ffn), W.BF16)
+    stream = torch.cuda.Stream()
+
+    def fused():
+        for i in range(layers):
+            F.rmsnorm_residual(x[i], r[i], wn, y, ro, 1e-6, W.BF16, stream=stream)
+            F.rope_qkv_split(qkv[i], q, k, v, heads, head_dim, pos0, 10000.0, W.BF16,
+                             stream=stream)
+            F.fuse_launch(swiglu, [gate[i], gate[i], up[i]], act, stream=stream)
+            F.rmsnorm_residual(ro, x[i], wn, y2, ro2, 1e-6, W.BF16, stream=stream)
+
+    pos = torch.arange(pos0, pos0 + tokens, device=dev, dtype=torch.float64)
+    inv = 10000.0 ** (-torch.arange(0, head_dim, 2, device=dev, dtype=torch.float64) / head_dim)
+    ang = pos[:, None] * inv[None, :]
+    cos = torch.cat([ang.cos(), ang.cos()], -1).float()[None]
+    sin = torch.cat([ang.sin(), ang.sin()], -1).float()[None]
+
+    def rms(a, b):
+        h = a.float() + b.float()
+        return (h * torch.rsqrt(h.pow(2).mean(-1, keepdim=True) + 1e-6) * wn.float()).to(bf), \
+            h.to(bf)
+
+    def eager():
+        for i in range(layers):
+            yy, hh = rms(x[i], r[i])
+            t = qkv[i].view(tokens, 3, heads, head_dim)
+            outs = [t[:, j].transpose(0, 1).contiguous() for j in range(3)]
+            for j in range(2):
+                xf = outs[j].float()
+                rh = torch.cat([-xf[..., head_dim // 2:], xf[..., :head_dim // 2]], -1)
+                outs[j] = (xf * cos + rh * sin).to(bf)
+            gf = gate[i].float()
+            a_ = (torch.sigmoid(gf) * gf * up[i].float()).to(bf)
+            rms(hh, x[i])
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            fn()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record()
+            for _ in range(reps):
+                fn()
+            b.record()
+        b.synchronize()
+        return a.elapsed_time(b) / reps * 1e3
+
+    out = {"layers": layers, "tokens": tokens, "launches_fused": 4 * layers,
+           "us_eager": timed(eager), "us_fused_host_loop": timed(fused)}
+    # the same sequences replayed from one graph each
+    with torch.cuda.stream(stream):
+        eager()
+    stream.synchronize()
+    tg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(tg, stream=stream):
+        eager()
+    out["us_eager_graph"] = timed(tg.replay)
+    F.fuse_graph_begin(stream)
+    with torch.cuda.stream(stream):
+        fused()
+    g = F.fuse_graph_end(stream)
+    out["us_fused_graph"] = timed(lambda: g.launch(stream))
+    out["graph_nodes_fused"] = g.nodes
+    g.release()
+    return out
+
+
 def _ln_item(dev, with_unfused):
     """Residual add + LayerNorm (a next row, measured beside the step)."""
     import torch
@@ -892,6 +987,8 @@ def run_gpu(args):
             d.update({"us_cublas_gemm_only": gms * 1e3, "fused_vs_cublas_gemm": gms / rms})
         next_rows[rl.name] = d
         del rl
+    if (args.only is None or re.search(args.only, "decode_glue")) and not args.no_unfused:
+        next_rows["decode_glue_32_layers_8_tokens"] = decode_glue(dev)
     # the chain sweep's smaller sizes (beside the step, not in it): 2^24 + 7
     # elements (inputs larger than L2) and 2^20 + 7 (L2-resident across
     # launches), 20 launches replayed from one graph
