@@ -371,6 +371,7 @@ static std::string gen_chain_source(const ChainPlan& p, const char* spec) {
     // sizes: compile-time constants for a fixed shape (the compiler folds
     // every branch below), the launch's element count for a shape bucket
     s << "\nextern \"C\" __global__ void __launch_bounds__(BLOCK) fuse_chain_vec(const Args a) {\n"
+         "  pdl_enter();\n"
          "  const idx_t n = (idx_t)SIZE_N(a), nvec = n / VEC, nfull = nvec / (idx_t)CHUNK;\n"
          "  const idx_t nrem = nvec - nfull * (idx_t)CHUNK, tail = n - nvec * VEC;\n"
          "  for (idx_t c = blockIdx.x; c < nfull; c += gridDim.x)\n"
@@ -384,6 +385,7 @@ static std::string gen_chain_source(const ChainPlan& p, const char* spec) {
   }
   // scalar kernel: any alignment
   s << "\nextern \"C\" __global__ void __launch_bounds__(256) fuse_chain_scalar(const Args a) {\n"
+         "  pdl_enter();\n"
        "  const idx_t n = (idx_t)SIZE_N(a);\n"
        "  for (idx_t e = (idx_t)blockIdx.x * 256 + threadIdx.x; e < n;"
        " e += (idx_t)gridDim.x * 256)\n"

@@ -46,6 +46,7 @@ struct DriverApi {
   decltype(&::cuModuleLoadData) ModuleLoadData;
   decltype(&::cuModuleGetFunction) ModuleGetFunction;
   decltype(&::cuLaunchKernel) LaunchKernel;
+  decltype(&::cuLaunchKernelEx) LaunchKernelEx;
   decltype(&::cuFuncSetAttribute) FuncSetAttribute;
   decltype(&::cuFuncGetAttribute) FuncGetAttribute;
   decltype(&::cuMemAlloc) MemAlloc;

@@ -181,6 +181,19 @@ __device__ __forceinline__ void store_words(u32* p, const u32 (&w)[NW]) {
   }
 }
 
+// ---------------------------------------------------------------- launch order
+// Programmatic dependent launch (sm_90 and later).  A kernel launched with the
+// programmatic-serialization attribute may have its CTAs scheduled before the
+// previous kernel on the stream has finished; griddepcontrol.wait holds them
+// until that kernel has completed and its writes are visible, so the stream
+// order is kept.  launch_dependents then lets the next launch schedule its own
+// CTAs early.  Both are no-ops for a launch without the attribute.  Every
+// kernel of the library calls this first, before touching memory.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- reductions
 
 __device__ __forceinline__ float warp_sum(float v) {

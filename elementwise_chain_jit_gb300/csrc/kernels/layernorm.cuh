@@ -52,6 +52,7 @@ __device__ __forceinline__ void chan_merge(float& n, float& mean, float& m2, flo
 extern "C" __global__ void __maxnreg__(LN_MAX_REGS)
 layernorm_vec(const void* x, const void* res, const void* gamma, const void* beta, void* out,
               void* res_out, long long rows, float eps) {
+  pdl_enter();
   __shared__ float pn[NWARPS], pmean[NWARPS], pm2[NWARPS];
   constexpr long long ROW_W = (long long)HIDDEN * Dt<DT>::bytes / 4;
   for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
@@ -193,6 +194,7 @@ layernorm_vec(const void* x, const void* res, const void* gamma, const void* bet
 extern "C" __global__ void __launch_bounds__(BLOCK)
 layernorm_scalar(const void* x, const void* res, const void* gamma, const void* beta, void* out,
                  void* res_out, long long rows, float eps) {
+  pdl_enter();
   __shared__ float part1[NWARPS], part2[NWARPS];
   for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
     const long long base = row * HIDDEN;

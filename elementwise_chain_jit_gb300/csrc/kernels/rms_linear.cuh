@@ -22,6 +22,7 @@
 // the tile loop needs no transform of either operand.
 extern "C" __global__ void rms_linear_fold(const u16* __restrict__ w, const u16* __restrict__ gamma,
                                            u16* __restrict__ wout, long long total) {
+  pdl_enter();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x)
     store_elem<DT>(wout, i, load_elem<DT>(w, i) * load_elem<DT>(gamma, i % KDIM));
@@ -33,6 +34,7 @@ extern "C" __global__ void rms_linear_fold(const u16* __restrict__ w, const u16*
 extern "C" __global__ void rms_linear_fold_vec(const u16* __restrict__ w,
                                                const u16* __restrict__ gamma,
                                                u16* __restrict__ wout, long long total) {
+  pdl_enter();
   const long long nvec = total / 8;
   for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < nvec;
        v += (long long)gridDim.x * blockDim.x) {

@@ -36,6 +36,7 @@ __device__ __forceinline__ float block_sum(float v, float* part) {
 extern "C" __global__ void __launch_bounds__(BLOCK)
 rmsnorm_vec(const void* x, const void* res, const void* w, void* out, void* res_out,
             long long rows, float eps) {
+  pdl_enter();
   __shared__ float part[NWARPS];
   for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
     const u32* xr = static_cast<const u32*>(x) + row * (HIDDEN * Dt<DT>::bytes / 4);
@@ -91,6 +92,7 @@ rmsnorm_vec(const void* x, const void* res, const void* w, void* out, void* res_
 extern "C" __global__ void __launch_bounds__(BLOCK)
 rmsnorm_scalar(const void* x, const void* res, const void* w, void* out, void* res_out,
                long long rows, float eps) {
+  pdl_enter();
   __shared__ float part[NWARPS];
   for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
     const long long base = row * HIDDEN;

@@ -34,6 +34,7 @@ constexpr int HD_WORDS = HD * BYTES / 4;
 #if FUSE_ROPE_VEC
 extern "C" __global__ void __launch_bounds__(BLOCK)
 rope_vec(const void* qkv, void* q, void* k, void* v, const float* table, long long pos0) {
+  pdl_enter();
   const long long t = blockIdx.x;
   const u32* src = static_cast<const u32*>(qkv) + t * TOKEN_WORDS;
   const float* tab = table + (pos0 + t) * (2 * HALF);
@@ -101,6 +102,7 @@ rope_vec(const void* qkv, void* q, void* k, void* v, const float* table, long lo
 // any alignment: one element (or pair) per thread step
 extern "C" __global__ void __launch_bounds__(BLOCK)
 rope_scalar(const void* qkv, void* q, void* k, void* v, const float* table, long long pos0) {
+  pdl_enter();
   const long long t = blockIdx.x;
   const long long src = t * 3LL * HEADS * HD;
   const float* tab = table + (pos0 + t) * (2 * HALF);

@@ -126,6 +126,7 @@ void load_driver() {
   FUSE_GET(ModuleLoadData, "cuModuleLoadData");
   FUSE_GET(ModuleGetFunction, "cuModuleGetFunction");
   FUSE_GET(LaunchKernel, "cuLaunchKernel");
+  FUSE_GET(LaunchKernelEx, "cuLaunchKernelEx");
   FUSE_GET(FuncSetAttribute, "cuFuncSetAttribute");
   FUSE_GET(FuncGetAttribute, "cuFuncGetAttribute");
   FUSE_GET(MemAlloc, "cuMemAlloc");
@@ -469,9 +470,28 @@ int launch(CUfunction fn, unsigned grid, unsigned block, unsigned smem, void* st
   const DriverApi* api;
   if (int rc = driver(&api)) return rc;
   if (grid == 0) return FUSE_OK;
-  CUresult r = api->LaunchKernel(fn, grid, 1, 1, block, 1, 1, smem,
-                                 reinterpret_cast<CUstream>(stream), args, nullptr);
-  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuLaunchKernel");
+  // programmatic dependent launch: the kernel's CTAs may be scheduled while
+  // the previous kernel on the stream finishes; the kernel itself waits for
+  // that kernel (griddepcontrol.wait, its first statement) before touching
+  // memory.  FUSE_PDL=0 launches in plain stream order.
+  static const bool pdl = [] {
+    const char* e = getenv("FUSE_PDL");
+    return !(e && *e == '0');
+  }();
+  CUlaunchAttribute attr = {};
+  attr.id = CU_LAUNCH_ATTRIBUTE_PROGRAMMATIC_STREAM_SERIALIZATION;
+  attr.value.programmaticStreamSerializationAllowed = 1;
+  CUlaunchConfig cfg = {};
+  cfg.gridDimX = grid;
+  cfg.gridDimY = cfg.gridDimZ = 1;
+  cfg.blockDimX = block;
+  cfg.blockDimY = cfg.blockDimZ = 1;
+  cfg.sharedMemBytes = smem;
+  cfg.hStream = reinterpret_cast<CUstream>(stream);
+  cfg.attrs = pdl ? &attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  CUresult r = api->LaunchKernelEx(&cfg, fn, args, nullptr);
+  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuLaunchKernelEx");
   stat_launch();
   return FUSE_OK;
 }

@@ -328,7 +328,9 @@ const char* fuse_last_error(void);
  * generated sources), FUSE_PTXAS_VERBOSE=1 (register use per kernel),
  * FUSE_DEBUG_BOUNDS=1 (chains compiled from then on check every index against
  * its tensor before the access and record code 3 in the device error word,
- * skipping the access, instead of touching memory outside the tensors). */
+ * skipping the access, instead of touching memory outside the tensors),
+ * FUSE_PDL=0 (launch in plain stream order instead of with programmatic
+ * dependent launch; read once per process). */
 int fuse_stats(int64_t* compiles, int64_t* cache_hits, int64_t* launches, double* compile_ms);
 
 /* Number of SMs the library sizes persistent grids for on the current
