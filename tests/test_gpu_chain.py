@@ -365,3 +365,31 @@ def test_output_written_over_an_input(over, offset):
     for j, (t, a) in enumerate(zip(dev, inputs)):
         if j != over:
             assert np.array_equal(to_host(t, c.in_dtypes[j]), a)
+
+
+# ------------------------------------------------------------ configuration fuzz
+
+@pytest.mark.parametrize("block", range(6))
+def test_random_configurations(block):
+    """Seeded random chains over the planner's whole range: 1-32 ops, start
+    dtype f16, f32 or bf16, sizes from 1 to ~300k elements, a shuffle prefix on
+    random NCHW shapes, and unaligned pointers (the scalar kernel).  Every case
+    against the oracle."""
+    rng = np.random.default_rng(7000 + block)
+    for _ in range(25):
+        length = int(rng.integers(1, 33))
+        seed = int(rng.integers(0, 1_000_000))
+        start = (F.F16, F.F32, F.BF16)[int(rng.integers(0, 3))]
+        spec, dt = workloads.random_chain(length, seed, start_dtype=start)
+        if rng.random() < 0.3:
+            groups = int(rng.choice([1, 2, 4, 8]))
+            shape = (int(rng.integers(1, 4)), groups * int(rng.integers(1, 9)),
+                     int(rng.integers(1, 12)), int(rng.integers(1, 12)))
+            spec = f"shuffle:{groups};{spec}"
+        else:
+            shape = (int(rng.choice([1, 7, 31, 255, 4097, 65_543, int(rng.integers(1, 300_000))])),)
+        offset = int(rng.random() < 0.25)
+        n = int(np.prod(shape))
+        inputs, _ = workloads.chain_inputs(spec, dt, n, seed)
+        got, _ = _run_chain(spec, dt, inputs, shape, offset)
+        _check(spec, dt, inputs, shape, got)
