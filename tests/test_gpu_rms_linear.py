@@ -171,3 +171,21 @@ def test_mixed_run_schedule_every_row():
     got = oracle.to_double(to_host(out.view(M, N)[:, torch.from_numpy(cols).cuda()], dt), dt)
     bad = np.abs(got - want) > 8e-3 * mag
     assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], want[bad][:5])
+
+
+@pytest.mark.parametrize("block", range(3))
+def test_random_shapes(block):
+    """Seeded random shapes on both paths: any M, N and K multiples of 8 (one
+    to several row tiles, column blocks and k-steps with ragged edges), both
+    dtypes, with and without bias."""
+    rng = np.random.default_rng(500 + block)
+    for i in range(8):
+        M = int(rng.integers(1, 701))
+        N = 8 * int(rng.integers(1, 129))
+        K = 8 * int(rng.integers(1, 129))
+        dt = (F.BF16, F.F16)[int(rng.integers(0, 2))]
+        bias = bool(rng.random() < 0.7)
+        if rng.random() < 0.5:
+            _case(M, N, K, dt, 600 + 10 * block + i, bias=bias)
+        else:
+            _folded_case(M, N, K, dt, 700 + 10 * block + i, bias=bias)
