@@ -319,6 +319,10 @@ rms_linear_persistent(const __grid_constant__ TensorMap tmap_x,
   cluster_sync();  // both CTAs' barriers and TMEM exist before the first copy
   tc_fence_after();
   const u32 tmem = *reinterpret_cast<volatile u32*>(base_ptr + (tmem_slot - base));
+  // the set-up above touches no global memory, so it may overlap the previous
+  // kernel on the stream; from here on wait for it (programmatic dependent
+  // launch, a no-op for a plain launch) and let the next one be scheduled
+  pdl_enter();
 
   bool ok = true;
   if (warp == 0) {

@@ -10,6 +10,7 @@
 // sm_103a like every other kernel of the library.
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <map>
 #include <tuple>
 #include <vector>
@@ -219,9 +220,27 @@ int launch_folded(const void* x, const void* w, const void* bias, void* out, int
   int mp_long = static_cast<int>(pick_mp_long((m_tiles64 + 1) / 2, n_tiles, clusters, &runs));
   const unsigned grid = 2u * static_cast<unsigned>(std::min<int64_t>(runs, clusters));
   void* args[] = {&mx, &mw, &mo, &bias, &m_tiles, &eps, &scale, &err, &mp_long};
-  r = api->LaunchKernel(fn, grid, 1, 1, 320, 1, 1, kPairSmem, reinterpret_cast<CUstream>(stream),
-                        args, nullptr);
-  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuLaunchKernel(rmsnorm_linear)");
+  // programmatic dependent launch, as for the other kernels (FUSE_PDL=0 off):
+  // the kernel's set-up overlaps the previous kernel, which it waits for
+  // before its first global access
+  static const bool pdl = [] {
+    const char* e = getenv("FUSE_PDL");
+    return !(e && *e == '0');
+  }();
+  CUlaunchAttribute attr = {};
+  attr.id = CU_LAUNCH_ATTRIBUTE_PROGRAMMATIC_STREAM_SERIALIZATION;
+  attr.value.programmaticStreamSerializationAllowed = 1;
+  CUlaunchConfig cfg = {};
+  cfg.gridDimX = grid;
+  cfg.gridDimY = cfg.gridDimZ = 1;
+  cfg.blockDimX = 320;
+  cfg.blockDimY = cfg.blockDimZ = 1;
+  cfg.sharedMemBytes = kPairSmem;
+  cfg.hStream = reinterpret_cast<CUstream>(stream);
+  cfg.attrs = pdl ? &attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  r = api->LaunchKernelEx(&cfg, fn, args, nullptr);
+  if (r != CUDA_SUCCESS) return cuda_fail(r, "cuLaunchKernelEx(rmsnorm_linear)");
   stat_launch();
   return FUSE_OK;
 }
