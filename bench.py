@@ -735,6 +735,15 @@ def cpu_sample_all_cores(frac_div: int):
     return total_b, total_t, cores, f"flat chains L=1..32 on {n} elements, {cores} slices, one thread each"
 
 
+def sample_share(frac_div: int) -> str:
+    """What share of each workload cpu_sample(frac_div) runs: the shuffle
+    workloads shrink by whole batches only, detect by whole cells per side."""
+    nb = 32 // min(frac_div, 32)
+    return (f"1/{frac_div} of the flat chains, RMSNorm, RoPE and add-relu-scale; "
+            f"{nb}/32 of the shuffle workloads' batch; detect with each scale's sides "
+            f"divided by {int(np.sqrt(frac_div))}, at least 1 cell")
+
+
 def cpu_sample(frac_div: int):
     """The oracle on a bounded sample of every workload; returns (bytes, seconds, description)."""
     import oracle
@@ -853,7 +862,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": tt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample": f"1/{frac} of each workload per step"},
+            "config": {"workload": WORKLOAD, "sample": sample_share(frac) + " per step"},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -1105,7 +1114,7 @@ def run_gpu(args):
     if rank == 0 and not args.no_cpu:
         b, t, desc = cpu_sample(64)
         cpu = {"value": b / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": desc + " (1/64 of each workload)", "seconds": t,
+               "sample": desc + f" ({sample_share(64)})", "seconds": t,
                "host_cores": os.cpu_count(), "nproc": len(os.sched_getaffinity(0))}
         ab, at, athreads, adesc = cpu_sample_all_cores(64)
         cpu["all_cores"] = {"value": ab / at / 1e9, "unit": UNIT, "cores": athreads,
