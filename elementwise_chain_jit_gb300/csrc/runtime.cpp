@@ -287,6 +287,28 @@ std::vector<std::string> nvrtc_options() {
   return o;
 }
 
+// What else decides the cubin besides the generated source and the options:
+// the text of the embedded headers the source includes and the NVRTC
+// version.  Part of every cache key, so that a cache directory filled by
+// another build of the library (headers changed) or another NVRTC is
+// recompiled rather than loaded.
+const std::string& toolchain_tag() {
+  static const std::string tag = [] {
+    std::string all;
+    for (int i = 0; i < kNumEmbeddedHeaders; ++i) {
+      all += kEmbeddedHeaders[i].name;
+      all += '\0';
+      all += kEmbeddedHeaders[i].text;
+      all += '\0';
+    }
+    int major = 0, minor = 0;
+    nvrtcVersion(&major, &minor);
+    return fmt("headers %016llx nvrtc %d.%d\n", static_cast<unsigned long long>(fnv1a(all)),
+               major, minor);
+  }();
+  return tag;
+}
+
 // Optional on-disk cache of cubins (FUSE_CACHE_DIR): file name is the hash
 // of the full key; the file holds the key length and a second hash so that
 // a collision is detected rather than loaded, and a hash of the cubin so that
@@ -402,7 +424,7 @@ int jit_compile(const std::string& source, const std::string& name, std::shared_
                 bool* compiled) {
   if (compiled) *compiled = false;
   std::vector<std::string> opts = nvrtc_options();
-  std::string key = "sm_103a\n";
+  std::string key = "sm_103a\n" + toolchain_tag();
   for (auto& o : opts) key += o + "\n";
   key += source;
   {

@@ -321,8 +321,10 @@ const char* fuse_last_error(void);
 /* Process-wide counters since load (any pointer may be NULL): NVRTC
  * compiles and their total time, cache hits (in memory, or a CUBIN loaded
  * from FUSE_CACHE_DIR), kernel launches.
- * Environment: FUSE_CACHE_DIR (on-disk CUBIN cache; each file carries hashes
- * of its key and of the CUBIN, a damaged or foreign file is recompiled;
+ * Environment: FUSE_CACHE_DIR (on-disk CUBIN cache, keyed by the generated
+ * source, the NVRTC options, the library's kernel headers and the NVRTC
+ * version; each file carries hashes of its key and of the CUBIN, a damaged or
+ * foreign file is recompiled;
  * an unwritable directory is ignored), FUSE_NVRTC_OPTIONS (extra NVRTC
  * options, space-separated, part of the cache key), FUSE_VERBOSE=1 (print
  * generated sources), FUSE_PTXAS_VERBOSE=1 (register use per kernel),
