@@ -40,16 +40,14 @@ __device__ __forceinline__ u32 pack2_bf16(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-// 1/d for d >= 1: the hardware reciprocal approximation refined by one
-// Newton-Raphson step for f(r) = 1/r - d, r1 = r + r(1 - d r), which squares
-// the approximation's relative error (result within about 1 ulp).  From
-// d >= 2^126 on the true value is below the normal range and the unrefined
-// approximation (0, flushed) is returned; NaN stays NaN.
+// 1/d for d >= 1: the hardware reciprocal approximation, documented (PTX ISA,
+// rcp.approx.f32) to at most 1 ulp from 1/d over the whole range.  From
+// d >= 2^126 on the true value is below the normal range and is flushed to 0;
+// 1/inf = 0; NaN stays NaN.
 __device__ __forceinline__ float rcp_ge1(float d) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
-  const float r1 = fmaf(r, fmaf(-d, r, 1.0f), r);
-  return d < 0x1p126f ? r1 : r;
+  return r;
 }
 // logistic sigmoid 1 / (1 + exp(-x)), exp from CUDA's expf (no fast-math)
 __device__ __forceinline__ float sigmoid(float x) { return rcp_ge1(1.0f + expf(-x)); }
