@@ -76,6 +76,23 @@ def test_unary_op_on_every_fp16_value(op, out):
     assert counts[3] == 0, (spec, counts)
 
 
+@pytest.mark.parametrize("op", ["sigmoid", "exp", "sigmoid;sigmoid"])
+def test_transcendentals_over_the_fp32_range(op):
+    """4M fp32 values spread over [-104, 104] plus the special values: where
+    exp(-x) overflows, where 1 + exp(-x) passes 2^126 and the reciprocal
+    flushes to zero, where exp underflows and overflows.  Every element is
+    pinned (flat 1e-6 or the running bound), none unpinned."""
+    grid = np.linspace(-104.0, 104.0, 1 << 22, dtype=np.float64).astype(np.float32)
+    special = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 3.4028235e38, -3.4028235e38, 1e-45,
+                        -1e-45, 1.1754944e-38, -87.33655, -87.33654, 88.72283, 88.72284,
+                        -103.97208, -103.97209], dtype=np.float32)
+    x = np.concatenate([grid, special])
+    got, _ = _run_chain(op, F.F32, [x], x.shape)
+    fails, counts, cls = oracle.chain_check(op, F.F32, [x], x.shape, got)
+    assert fails == 0, (op, counts, x[cls == 2][:8], got[cls == 2][:8])
+    assert counts[3] == 0, (op, counts)
+
+
 # ------------------------------------------------------------ random chains
 
 def _check(spec, dt, inputs, shape, got, idx=None):
