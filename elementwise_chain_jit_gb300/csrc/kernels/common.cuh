@@ -193,11 +193,80 @@ __device__ __forceinline__ void pdl_enter() {
 }
 
 // ---------------------------------------------------------------- reductions
+// Every sum below is a balanced binary tree: a term passes through at most
+// ceil(log2(number of nonzero terms)) fp32 additions at each stage (adding an
+// exact zero does not round).  A row of n terms reduced per thread, across
+// the lanes of a warp and across warps is therefore rounded at most
+// ceil(log2 n) + 3 times on any path, which is what the error bounds of the
+// row reductions are derived from.
 
+// butterfly over the 32 lanes: every lane ends with the same bits (fp32
+// addition is commutative, so both partners of a step compute the same sum)
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
+}
+
+// a[0] + ... + a[N-1] as a balanced tree, in registers (N is a constant)
+template <int N>
+__device__ __forceinline__ float tree_sum(float (&a)[N]) {
+#pragma unroll
+  for (int w = 1; w < N; w *= 2) {
+#pragma unroll
+    for (int i = 0; i + w < N; i += 2 * w) a[i] += a[i + w];
+  }
+  return a[0];
+}
+
+__host__ __device__ constexpr int floor_log2(int n) { return n < 2 ? 0 : 1 + floor_log2(n / 2); }
+
+// Cascade (pairwise) summation of N terms that arrive one at a time, in a
+// loop the compiler unrolls: lvl[j] holds the sum of a complete tree of 2^j
+// terms, like the bits of a binary counter, so the result is a balanced tree
+// of depth ceil(log2 N) with only floor(log2 N) + 1 partial sums live.
+template <int N>
+struct Cascade {
+  static constexpr int L = floor_log2(N) + 1;
+  float lvl[L];
+  // the k-th term (k counts from 0; k must fold to a constant)
+  __device__ __forceinline__ void add(int k, float v) {
+#pragma unroll
+    for (int j = 0; j < L; ++j) {
+      if ((k >> j) & 1) {
+        v = lvl[j] + v;
+      } else {
+        lvl[j] = v;
+        return;
+      }
+    }
+  }
+  // the partial trees of N's set bits, smallest first
+  __device__ __forceinline__ float total() const {
+    float acc = 0.f;
+    bool first = true;
+#pragma unroll
+    for (int j = 0; j < L; ++j) {
+      if ((N >> j) & 1) {
+        acc = first ? lvl[j] : lvl[j] + acc;
+        first = false;
+      }
+    }
+    return acc;
+  }
+};
+
+// Sum over a CTA of NWARPS_ warps: a butterfly within each warp, the warps'
+// sums through shared memory `part`, then a second butterfly over them (lanes
+// past NWARPS_ add zeros).  Every thread gets the same bits.  One barrier;
+// the caller separates two uses of the same `part` by another barrier.
+template <int NWARPS_>
+__device__ __forceinline__ float cta_sum(float v, float* part) {
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = v;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  return warp_sum(lane < NWARPS_ ? part[lane] : 0.f);
 }
 
 // Loads of data many CTAs reuse (weights, tables): read-only path, cached.

@@ -11,39 +11,15 @@
 // mean = sum(h)/HIDDEN; var = sum((h - mean)^2)/HIDDEN -- the same quantity
 // as the page's E[h^2] - mean^2, taken in two passes over the registers so
 // that fp32 does not cancel; out = dt((h - mean) * (1/sqrt(var + eps)) *
-// gamma + beta).  Reductions: per-thread sums, a warp shuffle tree, then the
-// warps' partial sums through shared memory.
+// gamma + beta).  Both sums are balanced trees (per thread, over lanes, over
+// warps; common.cuh): each term is rounded at most ceil(log2 HIDDEN) + 3
+// times on its way into the statistic.
 #pragma once
 #include "fuse/common.cuh"
 
 constexpr int NWARPS = BLOCK / 32;
 constexpr int NVR = HIDDEN / VEC;
 constexpr int NWV = VEC * Dt<DT>::bytes / 4;
-
-__device__ __forceinline__ float ln_block_sum(float v, float* part) {
-  v = warp_sum(v);
-  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float t = 0.f;
-#pragma unroll
-  for (int i = 0; i < NWARPS; ++i) t += part[i];
-  return t;
-}
-
-// Pairwise combination of (count, mean, sum of squared deviations) of two
-// disjoint sets (Chan, Golub and LeVeque's parallel variance update):
-// mean = mean_a + d*n_b/n, M2 = M2_a + M2_b + d^2*n_a*n_b/n with
-// d = mean_b - mean_a.  Empty sets (n = 0) leave the other side unchanged.
-__device__ __forceinline__ void chan_merge(float& n, float& mean, float& m2, float nb, float meanb,
-                                           float m2b) {
-  const float nt = n + nb;
-  if (nt == 0.f) return;
-  const float d = meanb - mean;
-  const float f = nb / nt;
-  mean += d * f;
-  m2 += m2b + d * d * n * f;
-  n = nt;
-}
 
 #ifndef LN_MAX_REGS
 #define LN_MAX_REGS 255
@@ -53,7 +29,10 @@ extern "C" __global__ void __maxnreg__(LN_MAX_REGS)
 layernorm_vec(const void* x, const void* res, const void* gamma, const void* beta, void* out,
               void* res_out, long long rows, float eps) {
   pdl_enter();
-  __shared__ float pn[NWARPS], pmean[NWARPS], pm2[NWARPS];
+  // one buffer per statistic: a row's second barrier separates its reads of
+  // psum from the next row's writes, and the next row's first barrier its
+  // reads of pdev
+  __shared__ float psum[NWARPS], pdev[NWARPS];
   constexpr long long ROW_W = (long long)HIDDEN * Dt<DT>::bytes / 4;
   for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
     const u32* xr = static_cast<const u32*>(x) + row * ROW_W;
@@ -67,17 +46,20 @@ layernorm_vec(const void* x, const void* res, const void* gamma, const void* bet
       }
     }
     float h[R][VEC];
-    float s1 = 0.f;
+    float s1v[R];  // per vector: its values summed as a tree
 #pragma unroll
     for (int i = 0; i < R; ++i) {
       const int v = threadIdx.x + i * BLOCK;
+      s1v[i] = 0.f;
       if (NVR % BLOCK == 0 || v < NVR) {
+        float t[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
           h[i][e] = get_elem<DT>(wx[i], e);
           if constexpr (HAS_RES) h[i][e] += get_elem<DT>(wr[i], e);
-          s1 += h[i][e];
+          t[e] = h[i][e];
         }
+        s1v[i] = tree_sum(t);
         if constexpr (HAS_RES) {
           u32 o[NWV];
           pack_vec<DT>(h[i], o);
@@ -85,79 +67,24 @@ layernorm_vec(const void* x, const void* res, const void* gamma, const void* bet
         }
       }
     }
-    // this thread's (count, mean, M2) over its registers, then one merge tree:
-    // warp lanes into lane 0, then every thread merges the warps' partials in
-    // the same order (one barrier per row, identical statistics everywhere)
-    float cnt = 0.f;
-#pragma unroll
-    for (int i = 0; i < R; ++i)
-      if (NVR % BLOCK == 0 || static_cast<int>(threadIdx.x) + i * BLOCK < NVR) cnt += VEC;
-    float mean = cnt > 0.f ? s1 / cnt : 0.f, m2 = 0.f;
+    const float mean = cta_sum<NWARPS>(tree_sum(s1v), psum) / HIDDEN;
+    // second pass over the registers: squared deviations from the row mean
+    float s2v[R];
 #pragma unroll
     for (int i = 0; i < R; ++i) {
       const int v = threadIdx.x + i * BLOCK;
+      s2v[i] = 0.f;
       if (NVR % BLOCK == 0 || v < NVR) {
+        float t[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
           const float d = h[i][e] - mean;
-          m2 += d * d;
+          t[e] = d * d;
         }
+        s2v[i] = tree_sum(t);
       }
     }
-    if constexpr (NVR % BLOCK == 0 && (NWARPS & (NWARPS - 1)) == 0) {
-      // every thread holds R*VEC values: each merge joins two equal sets, so
-      // mean = (a + b) / 2 and M2 = M2a + M2b + d^2 * n / 2 (n per side)
-      float half_n = 0.5f * cnt;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float mb = __shfl_down_sync(0xffffffffu, mean, o);
-        const float qb = __shfl_down_sync(0xffffffffu, m2, o);
-        const float d = mb - mean;
-        mean = 0.5f * (mean + mb);
-        m2 += qb + d * d * half_n;
-        half_n *= 2.f;
-      }
-      if ((threadIdx.x & 31) == 0) {
-        pmean[threadIdx.x >> 5] = mean;
-        pm2[threadIdx.x >> 5] = m2;
-      }
-      __syncthreads();
-      // the warps' partials merged by a butterfly over lanes (lane % NWARPS
-      // holds warp lane % NWARPS); both partners of a step compute
-      // mean = (a + b) / 2 and M2 = (M2a + M2b) + d^2 * n / 2, which do not
-      // depend on the operand order, so every lane ends with the same bits
-      mean = pmean[(threadIdx.x & 31) % NWARPS];
-      m2 = pm2[(threadIdx.x & 31) % NWARPS];
-#pragma unroll
-      for (int step = 1; step < NWARPS; step *= 2) {
-        const float mb = __shfl_xor_sync(0xffffffffu, mean, step);
-        const float qb = __shfl_xor_sync(0xffffffffu, m2, step);
-        const float d = mb - mean;
-        mean = 0.5f * (mean + mb);
-        m2 = (m2 + qb) + d * d * half_n;
-        half_n *= 2.f;
-      }
-    } else {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float nb = __shfl_down_sync(0xffffffffu, cnt, o);
-        const float mb = __shfl_down_sync(0xffffffffu, mean, o);
-        const float qb = __shfl_down_sync(0xffffffffu, m2, o);
-        chan_merge(cnt, mean, m2, nb, mb, qb);
-      }
-      if ((threadIdx.x & 31) == 0) {
-        pn[threadIdx.x >> 5] = cnt;
-        pmean[threadIdx.x >> 5] = mean;
-        pm2[threadIdx.x >> 5] = m2;
-      }
-      __syncthreads();
-      cnt = pn[0];
-      mean = pmean[0];
-      m2 = pm2[0];
-#pragma unroll
-      for (int w = 1; w < NWARPS; ++w) chan_merge(cnt, mean, m2, pn[w], pmean[w], pm2[w]);
-    }
-    const float rstd = 1.0f / sqrtf(m2 / HIDDEN + eps);
+    const float rstd = 1.0f / sqrtf(cta_sum<NWARPS>(tree_sum(s2v), pdev) / HIDDEN + eps);
     // gamma and beta (the same for every row, cache-resident) are read only
     // now: the pointers pass through an empty asm that takes rstd, so the
     // compiler cannot hoist their loads above the reductions, where they would
@@ -185,44 +112,54 @@ layernorm_vec(const void* x, const void* res, const void* gamma, const void* bet
         store_words(static_cast<u32*>(out) + row * ROW_W + v * NWV, o);
       }
     }
-    __syncthreads();  // pn/pmean/pm2 are reused by the next row
   }
 }
 #endif
 
-// any alignment: three passes over the row, element by element
+// any alignment: three passes over the row, element by element; each
+// thread's sums are cascades (balanced trees built as the terms arrive)
+constexpr int SITER = (HIDDEN + BLOCK - 1) / BLOCK;  // elements per thread
+
+template <bool RES>
+__device__ __forceinline__ float ln_h(const void* x, const void* res, long long i) {
+  float hv = load_elem<DT>(x, i);
+  if constexpr (RES) hv += load_elem<DT>(res, i);
+  return hv;
+}
+
 extern "C" __global__ void __launch_bounds__(BLOCK)
 layernorm_scalar(const void* x, const void* res, const void* gamma, const void* beta, void* out,
                  void* res_out, long long rows, float eps) {
   pdl_enter();
-  __shared__ float part1[NWARPS], part2[NWARPS];
+  __shared__ float psum[NWARPS], pdev[NWARPS];
   for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
     const long long base = row * HIDDEN;
-    float s1 = 0.f;
-    for (int i = threadIdx.x; i < HIDDEN; i += BLOCK) {
-      float hv = load_elem<DT>(x, base + i);
-      if constexpr (HAS_RES) hv += load_elem<DT>(res, base + i);
-      s1 += hv;
+    Cascade<SITER> c1;
+#pragma unroll
+    for (int k = 0; k < SITER; ++k) {
+      const int i = threadIdx.x + k * BLOCK;
+      c1.add(k, (HIDDEN % BLOCK == 0 || i < HIDDEN) ? ln_h<HAS_RES>(x, res, base + i) : 0.f);
     }
-    const float mean = ln_block_sum(s1, part1) / HIDDEN;
-    float s2 = 0.f;
-    for (int i = threadIdx.x; i < HIDDEN; i += BLOCK) {
-      float hv = load_elem<DT>(x, base + i);
-      if constexpr (HAS_RES) hv += load_elem<DT>(res, base + i);
-      s2 += (hv - mean) * (hv - mean);
-    }
-    const float rstd = 1.0f / sqrtf(ln_block_sum(s2, part2) / HIDDEN + eps);
-    for (int i = threadIdx.x; i < HIDDEN; i += BLOCK) {
-      float hv = load_elem<DT>(x, base + i);
-      if constexpr (HAS_RES) {
-        hv += load_elem<DT>(res, base + i);
-        store_elem<DT>(res_out, base + i, hv);
+    const float mean = cta_sum<NWARPS>(c1.total(), psum) / HIDDEN;
+    Cascade<SITER> c2;
+#pragma unroll
+    for (int k = 0; k < SITER; ++k) {
+      const int i = threadIdx.x + k * BLOCK;
+      float sq = 0.f;
+      if (HIDDEN % BLOCK == 0 || i < HIDDEN) {
+        const float d = ln_h<HAS_RES>(x, res, base + i) - mean;
+        sq = d * d;
       }
+      c2.add(k, sq);
+    }
+    const float rstd = 1.0f / sqrtf(cta_sum<NWARPS>(c2.total(), pdev) / HIDDEN + eps);
+    for (int i = threadIdx.x; i < HIDDEN; i += BLOCK) {
+      const float hv = ln_h<HAS_RES>(x, res, base + i);
+      if constexpr (HAS_RES) store_elem<DT>(res_out, base + i, hv);
       float t = (hv - mean) * rstd;
       if constexpr (HAS_GAMMA) t *= load_elem<DT>(gamma, i);
       if constexpr (HAS_BETA) t += load_elem<DT>(beta, i);
       store_elem<DT>(out, base + i, t);
     }
-    __syncthreads();
   }
 }
