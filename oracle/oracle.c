@@ -542,20 +542,23 @@ void oracle_rmsnorm_linear(const void* x, const void* gamma, const void* w, cons
  * here with h = x + residual.  res, gamma, beta may be NULL (no residual,
  * gamma = 1, beta = 0).  res_out receives h when res is given.  mag receives,
  * per output, the sum of the magnitudes of the terms of
- * y = h*s*gamma - mean*s*gamma + beta (s = 1/sqrt(var + eps)). */
+ * y = h*s*gamma - mean*s*gamma + beta (s = 1/sqrt(var + eps)), where the
+ * mean is itself a sum of the hidden terms h_k / hidden, whose magnitudes
+ * add up to mean(|h|):  mag = (|h| + mean(|h|)) * s * |gamma| + |beta|. */
 void oracle_layernorm_residual(const void* x, const void* res, const void* gamma, const void* beta,
                                int dt, int64_t rows, int64_t hidden, float eps, double* y,
                                double* res_out, double* mag) {
   for (int64_t r = 0; r < rows; ++r) {
-    double s1 = 0.0, s2 = 0.0;
+    double s1 = 0.0, s2 = 0.0, sa = 0.0;
     for (int64_t k = 0; k < hidden; ++k) {
       double hk = load_elem(x, dt, r * hidden + k);
       if (res) hk += load_elem(res, dt, r * hidden + k);
       if (res_out) res_out[r * hidden + k] = hk;
       s1 += hk;
       s2 += hk * hk;
+      sa += fabs(hk);
     }
-    double mean = s1 / (double)hidden;
+    double mean = s1 / (double)hidden, mean_abs = sa / (double)hidden;
     double var = s2 / (double)hidden - mean * mean;
     double s = 1.0 / sqrt(var + (double)eps);
     for (int64_t k = 0; k < hidden; ++k) {
@@ -564,7 +567,7 @@ void oracle_layernorm_residual(const void* x, const void* res, const void* gamma
       double g = gamma ? load_elem(gamma, dt, k) : 1.0;
       double b = beta ? load_elem(beta, dt, k) : 0.0;
       y[r * hidden + k] = (hk - mean) * s * g + b;
-      if (mag) mag[r * hidden + k] = (fabs(hk) + fabs(mean)) * s * fabs(g) + fabs(b);
+      if (mag) mag[r * hidden + k] = (fabs(hk) + mean_abs) * s * fabs(g) + fabs(b);
     }
   }
 }
