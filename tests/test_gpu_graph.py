@@ -1,12 +1,18 @@
 """GPU tests of fuse_graph_*: a sequence of library launches recorded with
-stream capture and replayed as one graph must produce exactly what the same
-launches produce when issued one by one."""
+stream capture and replayed as one graph.  Every replay's outputs are checked
+against the oracle (the tolerances of the eager tests), and must also equal,
+bit for bit, what the same launches produce when issued one by one."""
 import numpy as np
 import pytest
 import torch
 
 import elementwise_chain_jit_gb300 as F
+import oracle
+import tolerance as tol
 import workloads
+from gpu_util import to_host
+from test_gpu_fixed import _rope_check
+from test_gpu_rms_linear import _check as _rms_linear_check
 
 pytestmark = pytest.mark.gpu
 
@@ -40,6 +46,22 @@ def test_graph_replays_a_mixed_sequence_bit_exactly():
         F.rope_qkv_split(qkv, q, k, v, H, D, 5, 10000.0, F.BF16, stream=s)
 
     outs = [o1, o2, y, ro, q, k, v]
+    h_in1 = [to_host(t, d) for t, d in zip(in1, c1.in_dtypes)]
+    h_in2 = to_host(in2, F.F16)
+    hx, hr, hw = (to_host(t, F.BF16) for t in (x, r, w))
+    y_want, h_want = oracle.rmsnorm_residual(hx, hr, hw, F.BF16, 1e-6)
+    h_qkv = to_host(qkv, F.BF16)
+
+    def check_against_oracle():
+        for spec, dt, ins, shp, out, odt in ((spec1, dt1, h_in1, (n,), o1, c1.out_dtype),
+                                             ("shuffle:4;relu;scale:0.5", F.F16, [h_in2], shape,
+                                              o2, F.F16)):
+            fails, counts, _ = oracle.chain_check(spec, dt, ins, shp, to_host(out, odt))
+            assert fails == 0 and counts[3] == 0, (spec, counts)
+        assert np.array_equal(to_host(ro, F.BF16), oracle.store(h_want, F.BF16))
+        tol.assert_accepted(to_host(y, F.BF16), F.BF16, y_want, what="rmsnorm y")
+        _rope_check(h_qkv, H, D, 5, F.BF16, *(to_host(t, F.BF16) for t in (q, k, v)))
+
     with torch.cuda.stream(s):
         sequence()  # first use: compiles, loads modules, builds the RoPE table
     s.synchronize()
@@ -56,6 +78,7 @@ def test_graph_replays_a_mixed_sequence_bit_exactly():
     for _ in range(2):
         g.launch(s)
         s.synchronize()
+        check_against_oracle()
         for a, b in zip(outs, want):
             assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
         for t in outs:
@@ -103,6 +126,24 @@ def test_graph_with_layernorm_detect_shuffle_and_tensor_core_kernels():
         F.rmsnorm_linear(xm, gm, wm, bm, o_gamma, 1e-6, 0.5, F.BF16, stream=s)
 
     outs = [ly, lro, dout, so, o_fold, o_gamma]
+    hx, hr, hg, hb = (to_host(t, F.BF16) for t in (x, r, g, b))
+    ln_want, ln_h, ln_mag = oracle.layernorm_residual(hx, hr, hg, hb, F.BF16, 1e-5)
+    d_want, d_mag = oracle.detect_decode([to_host(f, F.F16).reshape(1, na * no, h, w_)
+                                          for f, (h, w_) in zip(feats, hw)],
+                                         F.F16, strides, anchors, na, no)
+    s_want = oracle.channel_shuffle(to_host(sx, F.F16).reshape(2, 16, 8, 8), 4)
+    hxm, hgm, hwm, hbm = (to_host(t, F.BF16) for t in (xm, gm, wm, bm))
+    m_want, m_mag = oracle.rmsnorm_linear(hxm, hgm, hwm, hbm, F.BF16, 1e-6, 0.5)
+
+    def check_against_oracle():
+        assert np.array_equal(to_host(lro, F.BF16), oracle.store(ln_h, F.BF16))
+        tol.assert_accepted(to_host(ly, F.BF16), F.BF16, ln_want, ln_mag, what="layernorm")
+        tol.assert_accepted(to_host(dout, F.F32), F.F32, d_want.reshape(-1), d_mag.reshape(-1),
+                            what="detect")
+        assert np.array_equal(to_host(so, F.F16), s_want.reshape(-1))
+        for o in (o_fold, o_gamma):
+            _rms_linear_check(to_host(o, F.BF16), F.BF16, hxm, m_want, m_mag, 0.5, K)
+
     with torch.cuda.stream(s):
         sequence()
     s.synchronize()
@@ -118,6 +159,7 @@ def test_graph_with_layernorm_detect_shuffle_and_tensor_core_kernels():
     for _ in range(3):
         gr.launch(s)
         s.synchronize()
+        check_against_oracle()
         for a, w_ in zip(outs, want):
             assert torch.equal(a.view(torch.uint8), w_.view(torch.uint8))
         for t in outs:

@@ -200,7 +200,7 @@ def test_check_accepts_an_fp32_device(length, seed):
     dev = _simulate_fp32_device(spec, dt, inputs, (4099,))
     fails, counts, _ = oracle.chain_check(spec, dt, inputs, (4099,), dev)
     assert fails == 0, (spec, counts)
-    assert counts[3] <= 4099 // 100, (spec, counts)  # few unpinned
+    assert counts[3] == 0, (spec, counts)  # none unpinned
 
 
 def test_check_rejects_perturbed_results():

@@ -68,3 +68,17 @@ def test_two_valued_row_closed_form():
         y, _, _ = oracle.layernorm_residual(_bf16(row[None, :]), None, None, None, BF, eps)
         want = np.tile([ab, -ab], 32) / np.sqrt(ab * ab + np.float32(eps))
         np.testing.assert_allclose(y[0], want, rtol=1e-12)
+
+
+def test_term_magnitudes_by_hand():
+    # row h = (-1, 3): mean 1, mean(|h|) 2, var 4; eps 0 gives s = 1/2.
+    # y = (h - mean) s gamma + beta has the terms h s gamma, -mean s gamma
+    # and beta, and the mean is the sum of the terms h_k / 2, whose
+    # magnitudes add up to mean(|h|) = 2 (not |mean| = 1):
+    #   mag_k = (|h_k| + 2) * s * |gamma_k| + |beta_k|
+    x = _bf16([[-1.0, 3.0]])
+    g = _bf16([2.0, -1.0])
+    b = _bf16([0.5, -0.25])
+    y, _, mag = oracle.layernorm_residual(x, None, g, b, BF, 0.0)
+    assert y.tolist() == [[(-1 - 1) * 0.5 * 2 + 0.5, (3 - 1) * 0.5 * -1 - 0.25]]
+    assert mag.tolist() == [[(1 + 2) * 0.5 * 2 + 0.5, (3 + 2) * 0.5 * 1 + 0.25]]
