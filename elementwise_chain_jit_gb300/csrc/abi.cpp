@@ -3,7 +3,10 @@
 // ChannelShuffle ("算子与运行时", section 2) on contiguous NCHW is a
 // permutation of whole H*W planes.  It runs through the chain engine as the
 // spec "shuffle:G" with no ops: a bit copy whose input index is the shuffle's
-// gather, with 16/32-byte coalesced accesses on both sides.  The pages' own
+// gather, with 16/32-byte coalesced accesses on both sides.  The handle is a
+// shape bucket over the batch dimension N (one compile per (C, H, W, G,
+// dtype), N passed with the launch), so a batch that changes from call to
+// call compiles nothing after the first.  The pages' own
 // remedy for the slow reshape/transpose (shared-memory reordering before
 // coalesced writes, section 2.1) is not needed on NCHW, where each plane is
 // already contiguous in both layouts.
@@ -21,7 +24,9 @@ int chain_launch(fuse_chain* h, const void* const* inputs, int n_in, void* outpu
 
 namespace {
 std::mutex g_shuffle_mu;
-std::map<std::tuple<int64_t, int64_t, int64_t, int64_t, int, int>, fuse_chain*> g_shuffle;
+// (c, h, w, groups, dtype, 64-bit indices) -> bucket handle
+std::map<std::tuple<int64_t, int64_t, int64_t, int, int, bool>, fuse_chain*> g_shuffle;
+constexpr int64_t kMaxShuffleElems = int64_t(1) << 40;  // the chain engine's limit
 }  // namespace
 }  // namespace fuse
 
@@ -48,26 +53,37 @@ int channel_shuffle(const void* in, void* out, int64_t n, int64_t c, int64_t h, 
   if (n < 0 || c < 0 || h < 0 || w < 0) return fail(FUSE_E_SHAPE, "negative dimension");
   if (groups <= 0) return fail(FUSE_E_ARG, "groups must be positive");
   if (c % groups) return fail(FUSE_E_SHAPE, "channels not divisible by groups");
-  if (n * c * h * w == 0) return FUSE_OK;
+  if (n == 0 || c == 0 || h == 0 || w == 0) return FUSE_OK;
+  // (no product is formed before it is known to stay below 2^40)
+  if (c > kMaxShuffleElems / h || c * h > kMaxShuffleElems / w ||
+      n > kMaxShuffleElems / (c * h * w))
+    return fail(FUSE_E_SHAPE, "more than 2^40 elements");
   if (!in || !out) return fail(FUSE_E_NULL, "NULL tensor pointer");
   if (in == out) return fail(FUSE_E_ARG, "channel_shuffle cannot run in place");
+  // the batch bucket: every N whose elements stay below 2^31 shares one
+  // kernel with 32-bit indices; larger N take a second one with 64-bit
+  // indices, up to the engine's 2^40 elements
+  const int64_t plane = c * h * w;
+  const int64_t n32 = ((int64_t(1) << 31) - 1) / plane;
+  const bool wide = n > n32;
+  const int64_t cap = wide ? kMaxShuffleElems / plane : n32;
   fuse_chain* hnd = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_shuffle_mu);
-    auto key = std::make_tuple(n, c, h, w, groups, static_cast<int>(dt));
+    auto key = std::make_tuple(c, h, w, groups, static_cast<int>(dt), wide);
     auto it = g_shuffle.find(key);
     if (it != g_shuffle.end()) {
       hnd = it->second;
       stat_hit();
     } else {
-      int64_t shape[4] = {n, c, h, w};
+      int64_t shape[4] = {cap, c, h, w};
       std::string spec = fmt("shuffle:%d", groups);
-      if (int rc = chain_compile(spec.c_str(), shape, 4, dt, &hnd, false)) return rc;
+      if (int rc = chain_compile(spec.c_str(), shape, 4, dt, &hnd, true)) return rc;
       g_shuffle.emplace(key, hnd);
     }
   }
   const void* ins[1] = {in};
-  return chain_launch(hnd, ins, 1, out, stream, -1);
+  return chain_launch(hnd, ins, 1, out, stream, n);
 }
 
 }  // extern "C"

@@ -3,14 +3,14 @@
 // The generated source defines before including this file:
 //   DT      dtype code of qkv, q, k, v
 //   HEADS   heads;  HD  head_dim (even);  HALF = HD / 2
-//   TOKENS  tokens of the call
 //   BLOCK   threads per CTA
 //   VEC     elements of each half a q/k item covers (HALF % VEC == 0)
 //   VV      elements a v item copies (HD % VV == 0)
 //   FUSE_ROPE_VEC  1 when vector widths fit (else only the scalar kernel)
 //
-// qkv is [TOKENS, 3, HEADS, HD]; q, k, v are [HEADS, TOKENS, HD].  Token t is
-// at position pos0 + t; table[pos][0][i] = cos(theta), table[pos][1][i] =
+// qkv is [tokens, 3, HEADS, HD]; q, k, v are [HEADS, tokens, HD], with the
+// token count a launch argument (one CTA per token), so one compiled kernel
+// serves every token count.  Token t is at position pos0 + t; table[pos][0][i] = cos(theta), table[pos][1][i] =
 // sin(theta), theta = pos * base^(-2i/HD), built on the device in fp64 and
 // stored as fp32.  A q/k item rotates VEC pairs (i, i + HALF):
 //   o[i] = x[i] cos - x[i + HALF] sin,  o[i + HALF] = x[i + HALF] cos + x[i] sin
@@ -33,7 +33,8 @@ constexpr int HD_WORDS = HD * BYTES / 4;
 
 #if FUSE_ROPE_VEC
 extern "C" __global__ void __launch_bounds__(BLOCK)
-rope_vec(const void* qkv, void* q, void* k, void* v, const float* table, long long pos0) {
+rope_vec(const void* qkv, void* q, void* k, void* v, const float* table, long long pos0,
+         long long tokens) {
   pdl_enter();
   const long long t = blockIdx.x;
   const u32* src = static_cast<const u32*>(qkv) + t * TOKEN_WORDS;
@@ -79,7 +80,7 @@ rope_vec(const void* qkv, void* q, void* k, void* v, const float* table, long lo
         o1[e] = x1 * c - x2 * s;
         o2[e] = x2 * c + x1 * s;
       }
-      u32* dst = static_cast<u32*>(which == 0 ? q : k) + (h * (long long)TOKENS + t) * HD_WORDS;
+      u32* dst = static_cast<u32*>(which == 0 ? q : k) + (h * tokens + t) * HD_WORDS;
       u32 p1[NW], p2[NW];
       pack_vec<DT>(o1, p1);
       pack_vec<DT>(o2, p2);
@@ -92,7 +93,7 @@ rope_vec(const void* qkv, void* q, void* k, void* v, const float* table, long lo
     const int it = threadIdx.x + n * BLOCK;
     if (V_ITEMS % BLOCK == 0 || it < V_ITEMS) {
       const int h = it / V_PER_ROW, j = it % V_PER_ROW;
-      store_words(static_cast<u32*>(v) + (h * (long long)TOKENS + t) * HD_WORDS + j * NWV, vw[n]);
+      store_words(static_cast<u32*>(v) + (h * tokens + t) * HD_WORDS + j * NWV, vw[n]);
     }
   }
 }
@@ -101,7 +102,8 @@ rope_vec(const void* qkv, void* q, void* k, void* v, const float* table, long lo
 
 // any alignment: one element (or pair) per thread step
 extern "C" __global__ void __launch_bounds__(BLOCK)
-rope_scalar(const void* qkv, void* q, void* k, void* v, const float* table, long long pos0) {
+rope_scalar(const void* qkv, void* q, void* k, void* v, const float* table, long long pos0,
+            long long tokens) {
   pdl_enter();
   const long long t = blockIdx.x;
   const long long src = t * 3LL * HEADS * HD;
@@ -113,14 +115,14 @@ rope_scalar(const void* qkv, void* q, void* k, void* v, const float* table, long
     const float x2 = load_elem<DT>(qkv, src + row * HD + HALF + i);
     const float c = tab[i], s = tab[HALF + i];
     void* dst = which == 0 ? q : k;
-    const long long o = (h * (long long)TOKENS + t) * HD;
+    const long long o = (h * tokens + t) * HD;
     store_elem<DT>(dst, o + i, x1 * c - x2 * s);
     store_elem<DT>(dst, o + HALF + i, x2 * c + x1 * s);
   }
   for (int it = threadIdx.x; it < HEADS * HD; it += BLOCK) {
     const int h = it / HD, d = it % HD;
     typedef typename Dt<DT>::storage S;
-    static_cast<S*>(v)[(h * (long long)TOKENS + t) * HD + d] =
+    static_cast<S*>(v)[(h * tokens + t) * HD + d] =
         static_cast<const S*>(qkv)[src + (2 * HEADS + h) * HD + d];
   }
 }

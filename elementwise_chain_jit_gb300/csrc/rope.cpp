@@ -33,7 +33,7 @@ struct Table {
 };
 
 std::mutex g_mu;
-std::map<std::tuple<int64_t, int, int, int>, RopeKernel> g_kernels;
+std::map<std::tuple<int, int, int>, RopeKernel> g_kernels;  // (heads, head_dim, dtype)
 std::map<std::tuple<int, uint32_t, int>, Table> g_tables;  // (device, base bits, head_dim)
 std::vector<CUdeviceptr> g_retired;  // outgrown tables, kept: in-flight kernels may read them
 std::shared_ptr<Module> g_table_mod;
@@ -44,8 +44,11 @@ int pick_vec(int n, int bytes) {
   return v * bytes >= 4 ? v : 0;
 }
 
-int rope_kernel(int64_t tokens, int heads, int hd, fuse_dtype dt, RopeKernel* out) {
-  auto key = std::make_tuple(tokens, heads, hd, static_cast<int>(dt));
+// One kernel per (heads, head_dim, dtype): the token count and the start
+// position come with the launch, so a serving loop whose batch changes every
+// step compiles nothing after its first call.
+int rope_kernel(int heads, int hd, fuse_dtype dt, RopeKernel* out) {
+  auto key = std::make_tuple(heads, hd, static_cast<int>(dt));
   if (auto it = g_kernels.find(key); it != g_kernels.end()) {
     stat_hit();
     *out = it->second;
@@ -60,13 +63,13 @@ int rope_kernel(int64_t tokens, int heads, int hd, fuse_dtype dt, RopeKernel* ou
   const int items = 2 * heads * (hd / 2 / k.vec);
   k.block = std::min(256, std::max(32, (items + 31) / 32 * 32));
   std::string src = fmt(
-      "// QKV split + transpose + RoPE: tokens %lld, heads %d, head_dim %d, %s\n"
+      "// QKV split + transpose + RoPE: heads %d, head_dim %d, %s\n"
       "constexpr int DT = %d;\nconstexpr int HEADS = %d;\nconstexpr int HD = %d;\n"
-      "constexpr int HALF = %d;\nconstexpr long long TOKENS = %lldLL;\nconstexpr int BLOCK = %d;\n"
+      "constexpr int HALF = %d;\nconstexpr int BLOCK = %d;\n"
       "constexpr int VEC = %d;\nconstexpr int VV = %d;\n#define FUSE_ROPE_VEC %d\n"
       "#include \"fuse/rope.cuh\"\n",
-      (long long)tokens, heads, hd, dtype_name(dt), static_cast<int>(dt), heads, hd, hd / 2,
-      (long long)tokens, k.block, k.vec, k.vv, k.has_vec ? 1 : 0);
+      heads, hd, dtype_name(dt), static_cast<int>(dt), heads, hd, hd / 2, k.block, k.vec, k.vv,
+      k.has_vec ? 1 : 0);
   if (int rc = jit_compile(src, "rope_qkv_split", &k.mod)) return rc;
   g_kernels.emplace(key, k);
   *out = k;
@@ -133,7 +136,7 @@ extern "C" int rope_qkv_split(const void* qkv, void* q, void* k, void* v, int64_
   if (tokens < 0 || heads < 1 || head_dim < 2 || head_dim > 1024 || head_dim % 2)
     return fail(FUSE_E_SHAPE, "need tokens >= 0, heads >= 1, head_dim even in 2..1024");
   if (tokens > 0x7fffffff) return fail(FUSE_E_SHAPE, "tokens above 2^31 - 1");
-  if (pos0 < 0 || pos0 + tokens > kMaxPositions)
+  if (pos0 < 0 || pos0 > kMaxPositions || tokens > kMaxPositions - pos0)
     return fail(FUSE_E_SHAPE, "positions must lie in [0, 2^22)");
   if (!(base > 1.f) || !std::isfinite(base)) return fail(FUSE_E_ARG, "base must be finite and > 1");
   if (tokens == 0) return FUSE_OK;
@@ -141,7 +144,7 @@ extern "C" int rope_qkv_split(const void* qkv, void* q, void* k, void* v, int64_
   RopeKernel kr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (int rc = rope_kernel(tokens, heads, head_dim, dt, &kr)) return rc;
+    if (int rc = rope_kernel(heads, head_dim, dt, &kr)) return rc;
   }
   DeviceInfo d;
   if (int rc = current_device(&d)) return rc;
@@ -159,8 +162,8 @@ extern "C" int rope_qkv_split(const void* qkv, void* q, void* k, void* v, int64_
           reinterpret_cast<uintptr_t>(p) % need_v == 0;
   CUfunction fn;
   if (int rc = jit_function(*kr.mod, vec ? "rope_vec" : "rope_scalar", d, &fn)) return rc;
-  long long p0 = pos0;
-  void* args[] = {&qkv, &q, &k, &v, &table, &p0};
+  long long p0 = pos0, nt = tokens;
+  void* args[] = {&qkv, &q, &k, &v, &table, &p0, &nt};
   return launch(fn, static_cast<unsigned>(tokens), static_cast<unsigned>(kr.block), 0, stream,
                 args);
 }
