@@ -73,6 +73,10 @@ struct DriverApi {
   decltype(&::cuMemPoolCreate) MemPoolCreate;
   decltype(&::cuMemPoolSetAttribute) MemPoolSetAttribute;
   decltype(&::cuMemAllocFromPoolAsync) MemAllocFromPoolAsync;
+  // optional (NULL on drivers before CUDA 12.4)
+  decltype(&::cuFuncIsLoaded) FuncIsLoaded;
+  decltype(&::cuFuncLoad) FuncLoad;
+  decltype(&::cuCtxGetId) CtxGetId;
 };
 
 // Returns FUSE_OK and the API table, or FUSE_E_CUDA (driver missing).

@@ -23,13 +23,22 @@
 //    calls whose work overlaps on the GPU -- on different streams, or from
 //    different threads without ordering -- race on the array and may read each
 //    other's rows.  Serialise them on one stream.
-//  * The first call on a device looks up the array's device address (with
-//    that device current) and keeps it; make that first call before any
-//    stream capture begins.
+//  * Set-up, once per CUDA context: the array's device address is looked up
+//    in the calling thread's current context (host code cannot use the
+//    symbol itself: on the host it names a stand-in, not device memory), and
+//    the file's four kernels are loaded there.  CUDA loads modules and
+//    kernels lazily by default (on first use), which allocates device memory
+//    for their code and data, so the FIRST call in a context does that work,
+//    whatever its dtype; make it before any stream capture begins and before
+//    an arena takes the remaining device memory.  The result is kept per
+//    context, under the driver's unique context id (never reused within a
+//    process, so a context made after a device reset is set up afresh);
+//    later calls allocate nothing.
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cmath>
+#include <map>
 #include <mutex>
 
 #include "internal.h"
@@ -40,12 +49,6 @@ static constexpr long long kScratchFloats = 1LL << 20;
 static __device__ __align__(256) float g_rope_rows[kScratchFloats];
 
 namespace {
-
-// Device addresses of g_rope_rows, one per device (host code may not use the
-// symbol itself: on the host it names a stand-in, not device memory).
-constexpr int kMaxDevices = 64;
-std::mutex g_addr_mu;
-float* g_addr[kMaxDevices];
 
 __global__ void rope_rows_build(float* rows, long long pos0, long long tokens, int hd,
                                 double base) {
@@ -125,22 +128,75 @@ __global__ void rope_noalloc_kernel(const void* qkv, void* q, void* k, void* v, 
   }
 }
 
-int rows_address(float** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+// The kernels of this file: loaded in the current context before the first
+// launch, so that no launch (in particular none inside a stream capture)
+// loads one lazily.
+const void* const kKernels[] = {
+    reinterpret_cast<const void*>(&rope_rows_build),
+    reinterpret_cast<const void*>(&rope_noalloc_kernel<FUSE_F32>),
+    reinterpret_cast<const void*>(&rope_noalloc_kernel<FUSE_F16>),
+    reinterpret_cast<const void*>(&rope_noalloc_kernel<FUSE_BF16>),
+};
+
+int ensure_loaded(const void* kernel) {
+  cudaFunction_t f = nullptr;
+  cudaError_t e = cudaGetFuncBySymbol(&f, kernel);
   if (e != cudaSuccess)
-    return fuse::fail(FUSE_E_CUDA, fuse::fmt("cudaGetDevice: %s", cudaGetErrorString(e)));
-  if (dev < 0 || dev >= kMaxDevices) return fuse::fail(FUSE_E_CUDA, "device ordinal out of range");
-  std::lock_guard<std::mutex> lk(g_addr_mu);
-  if (!g_addr[dev]) {
-    float* p = nullptr;
-    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_rope_rows);
-    if (e != cudaSuccess)
-      return fuse::fail(FUSE_E_CUDA,
-                        fuse::fmt("cudaGetSymbolAddress(rope rows): %s", cudaGetErrorString(e)));
-    g_addr[dev] = p;
+    return fuse::fail(FUSE_E_CUDA, fuse::fmt("cudaGetFuncBySymbol: %s", cudaGetErrorString(e)));
+  const fuse::DriverApi* api;
+  if (int rc = fuse::driver(&api)) return rc;
+  CUfunction cf = reinterpret_cast<CUfunction>(f);
+  if (api->FuncIsLoaded && api->FuncLoad) {
+    CUfunctionLoadingState st = CU_FUNCTION_LOADING_STATE_UNLOADED;
+    CUresult r = api->FuncIsLoaded(&st, cf);
+    if (r == CUDA_SUCCESS && st == CU_FUNCTION_LOADING_STATE_LOADED) return FUSE_OK;
+    r = api->FuncLoad(cf);
+    if (r != CUDA_SUCCESS) return fuse::cuda_fail(r, "cuFuncLoad (rope_qkv_split_noalloc)");
+    return FUSE_OK;
   }
-  *out = g_addr[dev];
+  // a driver without cuFuncLoad: reading the kernel's attributes loads it
+  cudaFuncAttributes attr;
+  e = cudaFuncGetAttributes(&attr, kernel);
+  if (e != cudaSuccess)
+    return fuse::fail(FUSE_E_CUDA, fuse::fmt("cudaFuncGetAttributes: %s", cudaGetErrorString(e)));
+  return FUSE_OK;
+}
+
+// The array's device address in the current context, with every kernel of
+// the file loaded there.
+int setup_context(float** out) {
+  float* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_rope_rows);
+  if (e != cudaSuccess)
+    return fuse::fail(FUSE_E_CUDA,
+                      fuse::fmt("cudaGetSymbolAddress(rope rows): %s", cudaGetErrorString(e)));
+  for (const void* k : kKernels)
+    if (int rc = ensure_loaded(k)) return rc;
+  *out = p;
+  return FUSE_OK;
+}
+
+std::mutex g_ctx_mu;
+std::map<unsigned long long, float*> g_ctx_rows;  // context id -> array address
+
+// Set up the current context once; later calls find the address here.  A
+// driver without context ids gets the set-up on every call (it allocates
+// nothing once done, but needs the runtime's symbol lookup each time).
+int rows_in_current_context(float** out) {
+  const fuse::DriverApi* api;
+  if (int rc = fuse::driver(&api)) return rc;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!api->CtxGetId || api->CtxGetCurrent(&ctx) != CUDA_SUCCESS || !ctx ||
+      api->CtxGetId(ctx, &id) != CUDA_SUCCESS)
+    return setup_context(out);
+  std::lock_guard<std::mutex> lk(g_ctx_mu);
+  if (auto it = g_ctx_rows.find(id); it != g_ctx_rows.end()) {
+    *out = it->second;
+    return FUSE_OK;
+  }
+  if (int rc = setup_context(out)) return rc;
+  g_ctx_rows.emplace(id, *out);
   return FUSE_OK;
 }
 
@@ -154,12 +210,13 @@ extern "C" int rope_qkv_split_noalloc(const void* qkv, void* q, void* k, void* v
   if (!valid_dtype(dt)) return fail(FUSE_E_DTYPE, fmt("invalid dtype %d", dt));
   if (tokens < 0 || heads < 1 || head_dim < 2 || head_dim > 1024 || head_dim % 2)
     return fail(FUSE_E_SHAPE, "need tokens >= 0, heads >= 1, head_dim even in 2..1024");
-  if (tokens * head_dim > kScratchFloats)
+  // (no product is formed before the operands are known to be small)
+  if (tokens > kScratchFloats / head_dim)
     return fail(FUSE_E_SHAPE,
-                fmt("tokens * head_dim = %lld exceeds this entry point's fixed table of %lld "
+                fmt("tokens %lld * head_dim %d exceeds this entry point's fixed table of %lld "
                     "values; split the call or use rope_qkv_split",
-                    (long long)(tokens * head_dim), kScratchFloats));
-  if (pos0 < 0 || pos0 + tokens > (int64_t(1) << 22))
+                    (long long)tokens, head_dim, kScratchFloats));
+  if (pos0 < 0 || pos0 > (int64_t(1) << 22) || tokens > (int64_t(1) << 22) - pos0)
     return fail(FUSE_E_SHAPE, "positions must lie in [0, 2^22)");
   if (!(base > 1.f) || !std::isfinite(base)) return fail(FUSE_E_ARG, "base must be finite and > 1");
   if (tokens == 0) return FUSE_OK;
@@ -167,11 +224,18 @@ extern "C" int rope_qkv_split_noalloc(const void* qkv, void* q, void* k, void* v
   DeviceInfo d;
   if (int rc = current_device(&d)) return rc;
   float* rows = nullptr;
-  if (int rc = rows_address(&rows)) return rc;
+  if (int rc = rows_in_current_context(&rows)) return rc;
+  // this library's runtime keeps its own last-error state; drop any error an
+  // earlier call left there, so that only this call's launches are checked
+  (void)cudaGetLastError();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long long total = tokens * (head_dim / 2);
   const unsigned grid = static_cast<unsigned>(std::min<long long>(d.sms * 8LL, (total + 255) / 256));
   rope_rows_build<<<grid, 256, 0, s>>>(rows, pos0, tokens, head_dim, static_cast<double>(base));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return fail(FUSE_E_CUDA, fmt("rope_qkv_split_noalloc rows launch: %s", cudaGetErrorString(e)));
+  stat_launch();
   const unsigned block = 256;
   if (dt == FUSE_F32)
     rope_noalloc_kernel<FUSE_F32><<<static_cast<unsigned>(tokens), block, 0, s>>>(
@@ -182,10 +246,9 @@ extern "C" int rope_qkv_split_noalloc(const void* qkv, void* q, void* k, void* v
   else
     rope_noalloc_kernel<FUSE_BF16><<<static_cast<unsigned>(tokens), block, 0, s>>>(
         qkv, q, k, v, rows, tokens, heads, head_dim);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess)
     return fail(FUSE_E_CUDA, fmt("rope_qkv_split_noalloc launch: %s", cudaGetErrorString(e)));
-  stat_launch();
   stat_launch();
   return FUSE_OK;
 }

@@ -155,6 +155,18 @@ void load_driver() {
   FUSE_GET(MemAllocFromPoolAsync, "cuMemAllocFromPoolAsync");
 #undef FUSE_GET
   if (!ok) return;
+  {
+    CUdriverProcAddressQueryResult q;
+    if (gpa("cuFuncIsLoaded", reinterpret_cast<void**>(&g_api.FuncIsLoaded), 12040,
+            CU_GET_PROC_ADDRESS_DEFAULT, &q) != CUDA_SUCCESS)
+      g_api.FuncIsLoaded = nullptr;
+    if (gpa("cuFuncLoad", reinterpret_cast<void**>(&g_api.FuncLoad), 12040,
+            CU_GET_PROC_ADDRESS_DEFAULT, &q) != CUDA_SUCCESS)
+      g_api.FuncLoad = nullptr;
+    if (gpa("cuCtxGetId", reinterpret_cast<void**>(&g_api.CtxGetId), 12000,
+            CU_GET_PROC_ADDRESS_DEFAULT, &q) != CUDA_SUCCESS)
+      g_api.CtxGetId = nullptr;
+  }
   CUresult r = g_api.Init(0);
   if (r != CUDA_SUCCESS) {
     const char* name = "?";

@@ -6,52 +6,93 @@ a CUDA-graph stream capture, loops that forbid allocation after start-up --
 call this entry point instead of rope_qkv_split.  Its cos/sin rows live in a
 fixed 4 MB array inside the library's module; every call shares it.
 
-This test calls it through the C ABI twice in a row, on different inputs,
-positions and token counts (so the second call runs over rows the first one
-left behind), and checks each result against rope_qkv_split on the same
-inputs: v bit for bit, q and k within the RoPE tolerance (8e-3 relative to
-the magnitude of the rotation's two terms, from the oracle).  It also checks
-that a call larger than the fixed array is refused with FUSE_E_SHAPE.  The
-file is named to be collected last; it needs nothing from earlier tests.
+The tests call it through the C ABI and check every result against the
+oracle: v bit for bit, q and k within the RoPE tolerance (tests/tolerance.py:
+8e-3 relative to the magnitude of the rotation's two terms for bf16, 2 ulp
+for fp16, 1e-6 for fp32).
+  * After one set-up call (bf16), calls of all three dtypes are recorded into
+    a CUDA graph with stream capture (thread-local mode: an allocation or a
+    synchronising call of this thread inside the capture breaks it) and
+    replayed twice; the same calls made eagerly change neither PyTorch's
+    allocated memory nor the device's free memory.
+  * Two calls in a row for each dtype, on different inputs, positions and
+    token counts, so the second call runs over rows the first one left
+    behind.
+  * A call larger than the fixed array is refused with FUSE_E_SHAPE.
+The file is named to be collected last; it needs nothing from earlier tests
+and passes alone in a fresh process.
 """
 import numpy as np
 import pytest
 import torch
 
 import elementwise_chain_jit_gb300 as F
-import oracle
 import workloads
+from gpu_util import to_dev, to_host
+from test_gpu_fixed import _rope_check
 
 pytestmark = pytest.mark.gpu
 
-
-def _up(a):
-    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
-
-
-def _down(t):
-    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+DTS = [F.F32, F.F16, F.BF16]
+TORCH_DT = {F.F32: torch.float32, F.F16: torch.float16, F.BF16: torch.bfloat16}
 
 
-def test_noalloc_matches_rope_qkv_split_on_two_calls_in_a_row():
+def _case(tokens, heads, hd, dt, seed):
+    qkv = workloads.normal((tokens, 3 * heads * hd), 0, 1, seed, dt)
+    outs = [torch.full((heads * tokens * hd,), float("nan"), dtype=TORCH_DT[dt], device="cuda")
+            for _ in range(3)]
+    return qkv, to_dev(qkv.reshape(-1), dt), outs
+
+
+def test_noalloc_calls_in_a_captured_graph_allocate_nothing():
+    heads, hd = 4, 128
+    # set-up call (first in this context, any dtype)
+    qkv0, qd0, o0 = _case(64, heads, hd, F.BF16, 880)
+    F.rope_qkv_split_noalloc(qd0, *o0, heads, hd, 100, 10000.0, F.BF16, tokens=64)
+    torch.cuda.synchronize()
+    _rope_check(qkv0, heads, hd, 100, F.BF16, *(to_host(t, F.BF16) for t in o0))
+
+    cases = [(dt, 40 + 24 * i, 1000 * (i + 1)) + _case(40 + 24 * i, heads, hd, dt, 890 + i)
+             for i, dt in enumerate(DTS)]
+    torch.cuda.synchronize()
+    alloc0 = torch.cuda.memory_allocated()
+    free0 = torch.cuda.mem_get_info()[0]
+    for dt, tokens, pos0, _, qd, outs in cases:  # eager, every dtype
+        F.rope_qkv_split_noalloc(qd, *outs, heads, hd, pos0, 10000.0, dt, tokens=tokens)
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == alloc0
+    assert torch.cuda.mem_get_info()[0] == free0
+    for dt, tokens, pos0, qkv, _, outs in cases:
+        _rope_check(qkv, heads, hd, pos0, dt, *(to_host(t, dt) for t in outs))
+        for t in outs:
+            t.fill_(float("nan"))
+
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    F.fuse_graph_begin(s)
+    for dt, tokens, pos0, _, qd, outs in cases:
+        F.rope_qkv_split_noalloc(qd, *outs, heads, hd, pos0, 10000.0, dt, tokens=tokens, stream=s)
+    g = F.fuse_graph_end(s)
+    assert g.nodes == 2 * len(cases)  # the rows build and the rotation, per call
+    for _ in range(2):
+        g.launch(s)
+        s.synchronize()
+        for dt, tokens, pos0, qkv, _, outs in cases:
+            _rope_check(qkv, heads, hd, pos0, dt, *(to_host(t, dt) for t in outs))
+            for t in outs:
+                t.fill_(float("nan"))
+        torch.cuda.synchronize()
+    g.release()
+
+
+@pytest.mark.parametrize("dt", DTS)
+def test_noalloc_matches_the_oracle_on_two_calls_in_a_row(dt):
     heads, hd = 8, 128
     for call, (tokens, pos0) in enumerate([(1024, 31000), (300, 7)]):
-        qkv = workloads.normal((tokens, 3 * heads * hd), 0, 1, 900 + call, F.BF16)
-        qd = _up(qkv.reshape(-1))
-        ref = [torch.empty(heads * tokens * hd, dtype=torch.bfloat16, device="cuda")
-               for _ in range(3)]
-        got = [torch.full_like(r, float("nan")) for r in ref]
-        F.rope_qkv_split(qd, *ref, heads, hd, pos0, 10000.0, F.BF16, tokens=tokens)
-        F.rope_qkv_split_noalloc(qd, *got, heads, hd, pos0, 10000.0, F.BF16, tokens=tokens)
+        qkv, qd, outs = _case(tokens, heads, hd, dt, 900 + call + 10 * dt)
+        F.rope_qkv_split_noalloc(qd, *outs, heads, hd, pos0, 10000.0, dt, tokens=tokens)
         torch.cuda.synchronize()
-        r_q, r_k, r_v = (_down(t) for t in ref)
-        g_q, g_k, g_v = (_down(t) for t in got)
-        assert np.array_equal(g_v, r_v)
-        _, _, _, qm, km = oracle.rope_qkv_split(qkv, F.BF16, heads, hd, pos0 + np.arange(tokens))
-        for g, r, mag in ((g_q, r_q, qm), (g_k, r_k, km)):
-            gd = oracle.to_double(g, F.BF16).reshape(mag.shape)
-            rd = oracle.to_double(r, F.BF16).reshape(mag.shape)
-            assert np.all(np.abs(gd - rd) <= 8e-3 * mag), call
+        _rope_check(qkv, heads, hd, pos0, dt, *(to_host(t, dt) for t in outs))
 
 
 def test_noalloc_refuses_calls_beyond_its_fixed_array():
