@@ -233,9 +233,9 @@ static void emit_op(std::ostringstream& s, const ChainOp& op, const std::string&
     case OP_MUL: s << "      x = x * " << operand(elem_of_input, op.input) << ";\n"; break;
     case OP_SCALE: s << "      x = x * " << hex_float(op.c) << ";\n"; break;
     case OP_RELU: s << "      x = x > 0.f ? x : 0.f;\n"; break;
-    // 1 / (1 + exp(-x)); the reciprocal of a value >= 1 by one Newton step on
-    // the hardware approximation (common.cuh), a third of the instructions of
-    // the IEEE division for the same result within an ulp
+    // 1 / (1 + exp(-x)); the reciprocal of the value >= 1 by the hardware
+    // approximation, documented to within 1 ulp (common.cuh), in place of the
+    // IEEE division
     case OP_SIGMOID: s << "      x = sigmoid(x);\n"; break;
     case OP_EXP: s << "      x = expf(x);\n"; break;
     case OP_CAST:

@@ -74,8 +74,10 @@ typedef struct fuse_chain* fuse_handle;
  * Every step runs in fp32 registers; only casts and the final store round.
  * A spec with no ops (only a shuffle, or empty) copies input 0 bit for bit.
  *
+ * At most 1024 ops and 128 input tensors; 1 <= G <= 2^20 (FUSE_E_SPEC).
  * shape/ndim: the tensor shape (1..8 dims, contiguous, row-major); with a
- *   shuffle it must be 4-D NCHW with C divisible by G.  Up to 2^40 elements.
+ *   shuffle it must be 4-D NCHW with C divisible by G.  Up to 2^40 elements
+ *   (FUSE_E_SHAPE).
  * in_dtype: dtype of input 0.
  * out: receives the handle.  Returns FUSE_E_SPEC/SHAPE/DTYPE/COMPILE on
  *   error (no handle is made).
@@ -231,8 +233,11 @@ int layernorm_residual(const void* x, const void* residual, const void* gamma, c
  * library builds on the device in fp64 and keeps (fp32, 2 * positions *
  * head_dim/2 * 4 bytes) per device, base and head_dim; it grows as larger
  * positions are asked for.  dt: f16, bf16 or f32.  head_dim even,
- * 2 <= head_dim <= 1024; heads >= 1; tokens >= 0; 0 <= pos0 and
- * pos0 + tokens <= 2^24.
+ * 2 <= head_dim <= 1024; heads >= 1; 0 <= tokens <= 2^31 - 1; 0 <= pos0 and
+ * pos0 + tokens <= 2^22 (every position below 2^22); FUSE_E_SHAPE otherwise,
+ * FUSE_E_ARG unless base is finite and > 1.  One kernel is compiled per
+ * (heads, head_dim, dt) on first use; the token count and pos0 are launch
+ * arguments, so calls with other token counts compile nothing.
  */
 int rope_qkv_split(const void* qkv, void* q, void* k, void* v, int64_t tokens, int heads,
                    int head_dim, int64_t pos0, float base, fuse_dtype dt, void* stream);
@@ -251,12 +256,18 @@ int rope_qkv_split(const void* qkv, void* q, void* k, void* v, int64_t tokens, i
  * a fixed array inside the library's module (2^20 fp32 values, 4 MB, held on
  * every device that has loaded the library until the process exits), and both
  * of its kernels are compiled ahead of time.
- *   - tokens * head_dim must be <= 2^20, else FUSE_E_SHAPE.
+ *   - tokens * head_dim must be <= 2^20, and pos0 + tokens <= 2^22, else
+ *     FUSE_E_SHAPE.
  *   - All calls on a device share the array; each call rewrites the rows it
  *     uses first, so nothing needs clearing, but calls that overlap on the GPU
  *     (other streams, unordered threads) race on it: order them on one stream.
- *   - The first call on a device looks up the array's address with that
- *     device current; make it before any stream capture begins.
+ *   - Every call looks up the array's address in the calling thread's
+ *     current context and makes sure the entry point's kernels are loaded
+ *     there.  CUDA loads modules and kernels lazily by default, and loading
+ *     allocates device memory, so the FIRST call in a context (any dtype)
+ *     does that set-up: make it before any stream capture begins and before
+ *     an arena takes the remaining device memory.  Later calls allocate
+ *     nothing, whatever their dtype.
  */
 int rope_qkv_split_noalloc(const void* qkv, void* q, void* k, void* v, int64_t tokens, int heads,
                            int head_dim, int64_t pos0, float base, fuse_dtype dt, void* stream);
@@ -273,8 +284,10 @@ int rope_qkv_split_noalloc(const void* qkv, void* q, void* k, void* v, int64_t t
  *   k = 0: (2p - 0.5 + x) * stride    k = 1: (2p - 0.5 + y) * stride
  *   k = 2: (2p)^2 * anchor_w          k = 3: (2p)^2 * anchor_h
  *   k >= 4: p
- * 1 <= nscales <= 8, 1 <= na <= 16, 5 <= no <= 1024.  The strides and
- * anchors are baked into the kernel (a new set compiles a new kernel).
+ * 1 <= nscales <= 8, 1 <= na <= 16, 5 <= no <= 1024, and per scale H_s,
+ * W_s >= 1 with H_s*W_s <= 2^24 (FUSE_E_SHAPE); non-finite strides or
+ * anchors are FUSE_E_ARG.  The strides and anchors are baked into the kernel
+ * (a new set compiles a new kernel).
  */
 int detect_decode(const void* const* feats, const int* hw, const float* strides,
                   const float* anchors, int nscales, int na, int no, fuse_dtype in_dt, void* out,
@@ -283,7 +296,12 @@ int detect_decode(const void* const* feats, const int* hw, const float* strides,
 /* ------------------------------------------------------------------------
  * ChannelShuffle ("算子与运行时", section 2): out[n, j*g + i] =
  * in[n, i*(c/g) + j] for i < g, j < c/g, on contiguous NCHW; a bit-exact
- * copy of whole H*W planes.  c % groups == 0.  in and out must not overlap.
+ * copy of whole H*W planes.  c % groups == 0 (else FUSE_E_SHAPE), groups > 0
+ * (else FUSE_E_ARG), n*c*h*w <= 2^40 (else FUSE_E_SHAPE); a zero dimension is
+ * a no-op.  in and out must not overlap (in == out is FUSE_E_ARG).  One
+ * kernel is compiled per (c, h, w, groups, dt) on first use (a second one
+ * once n*c*h*w reaches 2^31, with 64-bit indices); n is a launch argument, so
+ * calls with other batch sizes compile nothing.
  */
 int channel_shuffle(const void* in, void* out, int64_t n, int64_t c, int64_t h, int64_t w,
                     int groups, fuse_dtype dt, void* stream);
