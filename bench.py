@@ -439,6 +439,28 @@ def _rms_linear_item(dev, with_unfused, M=16384):
     return it
 
 
+def noalloc_row(dev, peak, peak_kind):
+    """rope_qkv_split_noalloc at the most tokens its fixed array takes at
+    head_dim 128 (8192 x 32 heads, bf16), beside rope_qkv_split on the same
+    tensors: its two launches (the cos/sin rows, then the rotation) against
+    the generated kernel with the library's cached table."""
+    import torch
+
+    import elementwise_chain_jit_gb300 as F
+    import workloads as W
+    T, H, D = 8192, 32, 128
+    qkv = W.device_normal((T, 3 * H * D), 0, 1, 81, W.BF16, dev)
+    q, k, v = (torch.empty(H * T * D, dtype=torch.bfloat16, device=dev) for _ in range(3))
+    nb = 2 * T * 3 * H * D * 2
+    ms = time_fn(lambda: F.rope_qkv_split_noalloc(qkv, q, k, v, H, D, 0, 10000.0, W.BF16),
+                 reps=20, warm=3)
+    ref = time_fn(lambda: F.rope_qkv_split(qkv, q, k, v, H, D, 0, 10000.0, W.BF16), reps=20, warm=3)
+    return {f"rope_qkv_split_noalloc_{T}x{H}x{D}_bf16": {
+        "bytes": nb, "us_fused": ms * 1e3, "gbs": nb / (ms / 1e3) / 1e9,
+        "frac_of_" + peak_kind + "_peak": nb / (ms / 1e3) / 1e9 / peak, "launches": 2,
+        "us_rope_qkv_split_same_shape": ref * 1e3}}
+
+
 def _rope_item(dev, with_unfused):
     import torch
 
@@ -1039,6 +1061,8 @@ def run_gpu(args):
             d.update({"us_cublas_gemm_only": gms * 1e3, "fused_vs_cublas_gemm": gms / rms})
         next_rows[rl.name] = d
         del rl
+    if args.only is None or re.search(args.only, "rope_qkv_split_noalloc"):
+        next_rows.update(noalloc_row(dev, peak, peak_kind))
     if (args.only is None or re.search(args.only, "decode_glue")) and not args.no_unfused:
         next_rows["decode_glue_32_layers_8_tokens"] = decode_glue(dev)
     # the chain sweep's smaller sizes (beside the step, not in it): 2^24 + 7

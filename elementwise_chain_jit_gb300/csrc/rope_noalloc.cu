@@ -11,7 +11,7 @@
 // loops that forbid allocations after start-up.  This entry point serves them:
 // its cos/sin rows live in a fixed array that is part of the library's own
 // module (static device memory, reserved when the module is loaded on a
-// device and held until the process exits), and both kernels are compiled
+// device and held until the process exits), and its kernels are compiled
 // ahead of time.
 //
 // Limits and sharing:
@@ -26,7 +26,7 @@
 //  * Set-up, once per CUDA context: the array's device address is looked up
 //    in the calling thread's current context (host code cannot use the
 //    symbol itself: on the host it names a stand-in, not device memory), and
-//    the file's four kernels are loaded there.  CUDA loads modules and
+//    the file's seven kernels are loaded there.  CUDA loads modules and
 //    kernels lazily by default (on first use), which allocates device memory
 //    for their code and data, so the FIRST call in a context does that work,
 //    whatever its dtype; make it before any stream capture begins and before
@@ -50,19 +50,81 @@ static __device__ __align__(256) float g_rope_rows[kScratchFloats];
 
 namespace {
 
+// sin and cos of a binary64 angle 0 <= theta < 2^22 (positions are below 2^22
+// and the frequencies at most 1), to about binary64 accuracy.  Cody and
+// Waite's reduction by pi/2, with pi/2 in three parts whose first two carry 30
+// bits, so that k times each is exact for k < 2^22: r = theta - k pi/2 in
+// [-pi/4, pi/4].  Then the Taylor series of sin to r^17 and of cos to r^18
+// (remainders below 1e-19 there), and the quadrant k mod 4.
+__device__ __forceinline__ void sincos_pos(double th, double* s, double* c) {
+  const double k = rint(th * 0x1.45f306dc9c883p-1);  // theta * 2/pi
+  double r = th - k * 0x1.921fb54000000p+0;
+  r = r - k * 0x1.10b4611800000p-30;
+  r = r - k * 0x1.313198a2e0370p-61;
+  const double r2 = r * r;
+  // 1/(2j+1)! and 1/(2j)!, alternating signs, j = 8 .. 0
+  double ps = 0x1.952c77030ad4ap-49;
+  ps = ps * r2 - 0x1.ae7f3e733b81fp-41;
+  ps = ps * r2 + 0x1.6124613a86d09p-33;
+  ps = ps * r2 - 0x1.ae64567f544e4p-26;
+  ps = ps * r2 + 0x1.71de3a556c734p-19;
+  ps = ps * r2 - 0x1.a01a01a01a01ap-13;
+  ps = ps * r2 + 0x1.1111111111111p-7;
+  ps = ps * r2 - 0x1.5555555555555p-3;
+  const double sr = r + r * r2 * ps;
+  double pc = -0x1.6827863b97d97p-53;
+  pc = pc * r2 + 0x1.ae7f3e733b81fp-45;
+  pc = pc * r2 - 0x1.93974a8c07c9dp-37;
+  pc = pc * r2 + 0x1.1eed8eff8d898p-29;
+  pc = pc * r2 - 0x1.27e4fb7789f5cp-22;
+  pc = pc * r2 + 0x1.a01a01a01a01ap-16;
+  pc = pc * r2 - 0x1.6c16c16c16c17p-10;
+  pc = pc * r2 + 0x1.5555555555555p-5;
+  pc = pc * r2 - 0.5;
+  const double cr = 1.0 + r2 * pc;
+  switch (static_cast<long long>(k) & 3) {
+    case 0: *s = sr; *c = cr; break;
+    case 1: *s = cr; *c = -sr; break;
+    case 2: *s = -sr; *c = -cr; break;
+    default: *s = -cr; *c = sr; break;
+  }
+}
+
+// Row t of the shared array: cos(theta_i) for i < half, then sin(theta_i), with
+// theta_i = (pos0 + t) * w_i and w_i = base^(-2i/hd).  Each CTA first takes
+// w_i, cos w_i and sin w_i for every i of the head, in binary64; a thread then
+// takes one i over a run of kRun consecutive tokens: sin and cos of the first
+// angle directly (sincos_pos), and each next one by the angle-addition
+// rotation by w_i, also in binary64.  The rotations add at most a few 1e-16 to
+// the values over a run, far below an fp32 rounding, while the direct
+// evaluations, the expensive part in binary64, drop to one in kRun.
+constexpr int kRun = 16;
+
 __global__ void rope_rows_build(float* rows, long long pos0, long long tokens, int hd,
                                 double base) {
+  __shared__ double w[512], cw[512], sw[512];
   const int half = hd / 2;
-  const long long total = tokens * half;
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    w[i] = pow(base, -2.0 * i / hd);
+    sincos_pos(w[i], &sw[i], &cw[i]);
+  }
+  __syncthreads();
+  const long long runs = (tokens + kRun - 1) / kRun;
+  const long long total = runs * half;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
-    const long long t = idx / half;
+    const long long t0 = (idx / half) * kRun;
     const int i = static_cast<int>(idx % half);
-    const double theta = static_cast<double>(pos0 + t) * pow(base, -2.0 * i / hd);
-    double s, c;
-    sincos(theta, &s, &c);
-    rows[t * hd + i] = static_cast<float>(c);
-    rows[t * hd + half + i] = static_cast<float>(s);
+    double sn, cs;
+    sincos_pos(static_cast<double>(pos0 + t0) * w[i], &sn, &cs);
+    const long long tn = tokens - t0 < kRun ? tokens - t0 : kRun;
+    for (long long m = 0; m < tn; ++m) {
+      rows[(t0 + m) * hd + i] = static_cast<float>(cs);
+      rows[(t0 + m) * hd + half + i] = static_cast<float>(sn);
+      const double c2 = cs * cw[i] - sn * sw[i];
+      sn = sn * cw[i] + cs * sw[i];
+      cs = c2;
+    }
   }
 }
 
@@ -128,6 +190,96 @@ __global__ void rope_noalloc_kernel(const void* qkv, void* q, void* k, void* v, 
   }
 }
 
+// 16-byte vectors of NV elements (NV = 8 for f16/bf16, 4 for f32), unpacked to
+// and packed from fp32 registers
+template <int DT>
+struct Vec16 {
+  static constexpr int NV = DT == FUSE_F32 ? 4 : 8;
+  static __device__ void unpack(const uint4& w, float (&x)[NV]) {
+    const unsigned u[4] = {w.x, w.y, w.z, w.w};
+    if constexpr (DT == FUSE_F32) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) x[j] = __uint_as_float(u[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const unsigned short lo = static_cast<unsigned short>(u[j] & 0xffffu);
+        const unsigned short hi = static_cast<unsigned short>(u[j] >> 16);
+        if constexpr (DT == FUSE_BF16) {
+          x[2 * j] = __uint_as_float(static_cast<unsigned>(lo) << 16);
+          x[2 * j + 1] = __uint_as_float(static_cast<unsigned>(hi) << 16);
+        } else {
+          asm("cvt.f32.f16 %0, %1;" : "=f"(x[2 * j]) : "h"(lo));
+          asm("cvt.f32.f16 %0, %1;" : "=f"(x[2 * j + 1]) : "h"(hi));
+        }
+      }
+    }
+  }
+  static __device__ uint4 pack(const float (&y)[NV]) {
+    unsigned u[4];
+    if constexpr (DT == FUSE_F32) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) u[j] = __float_as_uint(y[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if constexpr (DT == FUSE_BF16)
+          asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(u[j]) : "f"(y[2 * j + 1]), "f"(y[2 * j]));
+        else
+          asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(u[j]) : "f"(y[2 * j + 1]), "f"(y[2 * j]));
+      }
+    }
+    return make_uint4(u[0], u[1], u[2], u[3]);
+  }
+};
+
+// The same kernel with 16-byte accesses: a q/k item rotates NV pairs (NV
+// elements of each half row, with their NV cosines and sines), a v item copies
+// NV elements.  The host takes it when head_dim / 2 is a multiple of NV and
+// every tensor is 16-byte aligned (so every access is).
+template <int DT>
+__global__ void rope_noalloc_vec(const void* qkv, void* q, void* k, void* v, const float* rows,
+                                 long long tokens, int heads, int hd) {
+  typedef Vec16<DT> V;
+  constexpr int NV = V::NV;
+  typedef typename Elem<DT>::S S;
+  const long long t = blockIdx.x;
+  const int half = hd / 2, per_half = half / NV;
+  const S* src = static_cast<const S*>(qkv) + t * 3LL * heads * hd;
+  const float* row = rows + t * hd;
+  for (int it = threadIdx.x; it < 2 * heads * per_half; it += blockDim.x) {
+    const int r = it / per_half, i0 = (it % per_half) * NV;
+    const int which = r / heads, h = r % heads;
+    const uint4 wa = *reinterpret_cast<const uint4*>(src + static_cast<long long>(r) * hd + i0);
+    const uint4 wb =
+        *reinterpret_cast<const uint4*>(src + static_cast<long long>(r) * hd + half + i0);
+    float x1[NV], x2[NV], c[NV], s[NV], o1[NV], o2[NV];
+#pragma unroll
+    for (int j = 0; j < NV; j += 4) {
+      const float4 cj = *reinterpret_cast<const float4*>(row + i0 + j);
+      const float4 sj = *reinterpret_cast<const float4*>(row + half + i0 + j);
+      c[j] = cj.x; c[j + 1] = cj.y; c[j + 2] = cj.z; c[j + 3] = cj.w;
+      s[j] = sj.x; s[j + 1] = sj.y; s[j + 2] = sj.z; s[j + 3] = sj.w;
+    }
+    V::unpack(wa, x1);
+    V::unpack(wb, x2);
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      o1[j] = x1[j] * c[j] - x2[j] * s[j];
+      o2[j] = x2[j] * c[j] + x1[j] * s[j];
+    }
+    S* dst = static_cast<S*>(which == 0 ? q : k) + (h * tokens + t) * hd;
+    *reinterpret_cast<uint4*>(dst + i0) = V::pack(o1);
+    *reinterpret_cast<uint4*>(dst + half + i0) = V::pack(o2);
+  }
+  const int per_row = hd / NV;
+  for (int it = threadIdx.x; it < heads * per_row; it += blockDim.x) {
+    const int h = it / per_row, d0 = (it % per_row) * NV;
+    *reinterpret_cast<uint4*>(static_cast<S*>(v) + (h * tokens + t) * hd + d0) =
+        *reinterpret_cast<const uint4*>(src + (2LL * heads + h) * hd + d0);
+  }
+}
+
 // The kernels of this file: loaded in the current context before the first
 // launch, so that no launch (in particular none inside a stream capture)
 // loads one lazily.
@@ -136,6 +288,9 @@ const void* const kKernels[] = {
     reinterpret_cast<const void*>(&rope_noalloc_kernel<FUSE_F32>),
     reinterpret_cast<const void*>(&rope_noalloc_kernel<FUSE_F16>),
     reinterpret_cast<const void*>(&rope_noalloc_kernel<FUSE_BF16>),
+    reinterpret_cast<const void*>(&rope_noalloc_vec<FUSE_F32>),
+    reinterpret_cast<const void*>(&rope_noalloc_vec<FUSE_F16>),
+    reinterpret_cast<const void*>(&rope_noalloc_vec<FUSE_BF16>),
 };
 
 int ensure_loaded(const void* kernel) {
@@ -229,23 +384,33 @@ extern "C" int rope_qkv_split_noalloc(const void* qkv, void* q, void* k, void* v
   // earlier call left there, so that only this call's launches are checked
   (void)cudaGetLastError();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const long long total = tokens * (head_dim / 2);
-  const unsigned grid = static_cast<unsigned>(std::min<long long>(d.sms * 8LL, (total + 255) / 256));
+  // one thread per (run of 16 tokens, pair index), at most two CTAs per SM
+  // (each takes the head's frequencies once)
+  const long long total = (tokens + 15) / 16 * (head_dim / 2);
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(d.sms * 2LL, (total + 255) / 256));
   rope_rows_build<<<grid, 256, 0, s>>>(rows, pos0, tokens, head_dim, static_cast<double>(base));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess)
     return fail(FUSE_E_CUDA, fmt("rope_qkv_split_noalloc rows launch: %s", cudaGetErrorString(e)));
   stat_launch();
-  const unsigned block = 256;
-  if (dt == FUSE_F32)
-    rope_noalloc_kernel<FUSE_F32><<<static_cast<unsigned>(tokens), block, 0, s>>>(
-        qkv, q, k, v, rows, tokens, heads, head_dim);
-  else if (dt == FUSE_F16)
-    rope_noalloc_kernel<FUSE_F16><<<static_cast<unsigned>(tokens), block, 0, s>>>(
-        qkv, q, k, v, rows, tokens, heads, head_dim);
-  else
-    rope_noalloc_kernel<FUSE_BF16><<<static_cast<unsigned>(tokens), block, 0, s>>>(
-        qkv, q, k, v, rows, tokens, heads, head_dim);
+  const unsigned block = 256, ntok = static_cast<unsigned>(tokens);
+  // 16-byte accesses when half a row is a whole number of vectors and every
+  // tensor is 16-byte aligned; element-wise otherwise
+  const int nv = dt == FUSE_F32 ? 4 : 8;
+  bool vec = (head_dim / 2) % nv == 0;
+  for (const void* p : {qkv, static_cast<const void*>(q), static_cast<const void*>(k),
+                        static_cast<const void*>(v)})
+    vec = vec && aligned16(p);
+  if (dt == FUSE_F32) {
+    if (vec) rope_noalloc_vec<FUSE_F32><<<ntok, block, 0, s>>>(qkv, q, k, v, rows, tokens, heads, head_dim);
+    else rope_noalloc_kernel<FUSE_F32><<<ntok, block, 0, s>>>(qkv, q, k, v, rows, tokens, heads, head_dim);
+  } else if (dt == FUSE_F16) {
+    if (vec) rope_noalloc_vec<FUSE_F16><<<ntok, block, 0, s>>>(qkv, q, k, v, rows, tokens, heads, head_dim);
+    else rope_noalloc_kernel<FUSE_F16><<<ntok, block, 0, s>>>(qkv, q, k, v, rows, tokens, heads, head_dim);
+  } else {
+    if (vec) rope_noalloc_vec<FUSE_BF16><<<ntok, block, 0, s>>>(qkv, q, k, v, rows, tokens, heads, head_dim);
+    else rope_noalloc_kernel<FUSE_BF16><<<ntok, block, 0, s>>>(qkv, q, k, v, rows, tokens, heads, head_dim);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess)
     return fail(FUSE_E_CUDA, fmt("rope_qkv_split_noalloc launch: %s", cudaGetErrorString(e)));

@@ -240,6 +240,43 @@ def test_rope_full_config_sampled_tokens():
                 tokens_idx=sel)
 
 
+def _table_check(fn, tokens, pos0, hd=128):
+    """The cos/sin values a RoPE entry point uses, read back exactly: fp32 q
+    rows of ones then zeros rotate to (cos theta_i, sin theta_i) and k rows of
+    zeros then ones to (-sin theta_i, cos theta_i), with no rounding in the
+    rotation (products by 1 and 0).  Each must be within one ulp of the fp32
+    value nearest the oracle's cos or sin, or within the error of the angle
+    itself: both sides form theta = pos * base^(-2i/D) in binary64, which is
+    good to about pos * 2^-52 radians, and near a zero of cos or sin that
+    absolute error is many fp32 ulps (bound used: pos * 2^-50).  Where that
+    error is near an fp32 rounding step the two sides round apart, about one
+    value in 10^3 at positions near 2^22; at most 1 % may."""
+    half = hd // 2
+    qkv = np.zeros((tokens, 3, 1, hd), np.float32)
+    qkv[:, 0, 0, :half] = 1.0
+    qkv[:, 1, 0, half:] = 1.0
+    outs = [torch.empty(tokens * hd, dtype=torch.float32, device="cuda") for _ in range(3)]
+    fn(to_dev(qkv.reshape(-1), F.F32), *outs, 1, hd, pos0, 10000.0, F.F32, tokens=tokens)
+    torch.cuda.synchronize()
+    q, k, _, _, _ = oracle.rope_qkv_split(qkv.reshape(tokens, -1), F.F32, 1, hd,
+                                         pos0 + np.arange(tokens))
+    def order(a):  # monotone integer image of fp32 values (both zeros map to 0)
+        b = a.view(np.int32).astype(np.int64)
+        return np.where(b < 0, -(b & 0x7FFFFFFF), b)
+    theta_err = np.repeat((pos0 + np.arange(tokens)) * 2.0 ** -50, hd)
+    for got, want in ((outs[0], q), (outs[1], k)):
+        g = to_host(got, F.F32)
+        w = want.reshape(-1)
+        d = np.abs(order(g) - order(oracle.store(w, F.F32)))
+        ok = (d <= 1) | (np.abs(g.astype(np.float64) - w) <= theta_err)
+        assert ok.all() and (d > 0).mean() <= 1e-2, (int((~ok).sum()), int((d > 0).sum()))
+
+
+@pytest.mark.parametrize("pos0", [0, 1000, (1 << 22) - 2048])
+def test_rope_table_is_correctly_rounded(pos0):
+    _table_check(F.rope_qkv_split, 2048, pos0)
+
+
 # ------------------------------------------------------------ detection decode
 
 def _detect_case(hw, dt, seed, offset=0, na=3, no=85):

@@ -17,19 +17,19 @@ for fp16, 1e-6 for fp32).
     allocated memory nor the device's free memory.
   * Two calls in a row for each dtype, on different inputs, positions and
     token counts, so the second call runs over rows the first one left
-    behind.
+    behind (16-byte vector kernel), and the element-wise kernel on an odd
+    half row and on tensors off the 16-byte boundary.
   * A call larger than the fixed array is refused with FUSE_E_SHAPE.
 The file is named to be collected last; it needs nothing from earlier tests
 and passes alone in a fresh process.
 """
-import numpy as np
 import pytest
 import torch
 
 import elementwise_chain_jit_gb300 as F
 import workloads
-from gpu_util import to_dev, to_host
-from test_gpu_fixed import _rope_check
+from gpu_util import Guarded, misaligned_copy, to_dev, to_host
+from test_gpu_fixed import _rope_check, _table_check
 
 pytestmark = pytest.mark.gpu
 
@@ -93,6 +93,29 @@ def test_noalloc_matches_the_oracle_on_two_calls_in_a_row(dt):
         F.rope_qkv_split_noalloc(qd, *outs, heads, hd, pos0, 10000.0, dt, tokens=tokens)
         torch.cuda.synchronize()
         _rope_check(qkv, heads, hd, pos0, dt, *(to_host(t, dt) for t in outs))
+
+
+@pytest.mark.parametrize("dt", DTS)
+@pytest.mark.parametrize("tokens,heads,hd,offset", [(33, 3, 6, 0), (17, 2, 128, 1)])
+def test_noalloc_element_wise_path(dt, tokens, heads, hd, offset):
+    """Half a row that is not a whole number of 16-byte vectors, or tensors
+    off the 16-byte boundary: the element-wise kernel, against the oracle."""
+    qkv, qd, _ = _case(tokens, heads, hd, dt, 950 + hd + offset)
+    if offset:
+        qd = misaligned_copy(qd, offset)
+    outs = [Guarded(heads * tokens * hd, dt, offset_elems=offset) for _ in range(3)]
+    F.rope_qkv_split_noalloc(qd, *(o.t for o in outs), heads, hd, 77, 10000.0, dt, tokens=tokens)
+    torch.cuda.synchronize()
+    assert all(o.canary_ok() for o in outs)
+    _rope_check(qkv, heads, hd, 77, dt, *(to_host(o.t, dt) for o in outs))
+
+
+@pytest.mark.parametrize("pos0", [0, 1000, (1 << 22) - 2048])
+def test_noalloc_rows_are_correctly_rounded(pos0):
+    """The cos/sin rows it builds per call (reduced argument, Taylor series in
+    binary64) are the fp32 values nearest the exact ones, up to the largest
+    positions."""
+    _table_check(F.rope_qkv_split_noalloc, 2048, pos0)
 
 
 def test_noalloc_refuses_calls_beyond_its_fixed_array():
