@@ -625,9 +625,13 @@ def graph_per_launch(fn, k=20):
 
 
 def cold_time(item, reps=10):
-    """Median time of one launch with its inputs cold in HBM and no dirty
-    lines left in L2: before each launch a read-only pass over 512 MB (four
-    times L2) evicts L2 with clean lines."""
+    """Mean time of one launch with its inputs cold in HBM and no dirty lines
+    left in L2: before each launch a read-only pass over 512 MB (four times
+    L2) evicts L2 with clean lines.  The mean, not the median: on these boxes
+    an event pair around one launch reads in steps of about 2.05 us, and the
+    launch starts at a random point of that step (after a flush pass of
+    varying length), so the mean of many launches is unbiased where the
+    median is not."""
     import torch
     flush = getattr(cold_time, "buf", None)
     if flush is None:
@@ -642,7 +646,7 @@ def cold_time(item, reps=10):
         b.record(s)
         b.synchronize()
         ts.append(a.elapsed_time(b))
-    return statistics.median(ts[2:]) * 1e3
+    return statistics.mean(ts[2:]) * 1e3
 
 
 def graph_times(item, k=50):
@@ -1014,9 +1018,19 @@ def run_gpu(args):
             d.update(graph_times(it))
         # the same launch alone, inputs cold and no predecessor's dirty lines
         # left in L2 to write back (in the step each item pays for those)
-        cold_us = cold_time(it, reps=10 if it.bytes < 64e6 else 5)
+        cold_us = cold_time(it, reps=40 if it.bytes < 1e9 else 5)
         d.update({"us_fused_cold_clean_l2": cold_us,
                   "frac_cold_clean_l2": it.bytes / (cold_us * 1e-6) / 1e9 / peak})
+        if it.name.startswith("channel_shuffle"):
+            # the same bytes through PyTorch's device-to-device copy, timed the
+            # same way: what a plain copy of this size reaches on this machine
+            src, dst = it.inputs[0], it.outputs[0]
+
+            class _Copy:
+                fused = staticmethod(lambda: dst.copy_(src))
+            copy_us = cold_time(_Copy, reps=40)
+            d.update({"us_device_copy_cold_clean_l2": copy_us,
+                      "frac_of_device_copy_cold": copy_us / cold_us})
         if it.mufu_ops:
             # two rooflines: HBM bytes and special-function unit operations
             # at the clock sampled during the timed region
@@ -1034,7 +1048,7 @@ def run_gpu(args):
     if args.only is None or re.search(args.only, f"layernorm_residual_{LN_ROWS[0]}x4096_bf16"):
         ln = _ln_item(dev, with_unfused=not args.no_unfused)
         lms = time_fn(ln.fused, reps=20, warm=3)
-        cold_us = cold_time(ln, reps=5)
+        cold_us = cold_time(ln, reps=20)
         d = {"bytes": ln.bytes, "us_fused": lms * 1e3, "gbs": ln.bytes / (lms / 1e3) / 1e9,
              "frac_of_" + peak_kind + "_peak": ln.bytes / (lms / 1e3) / 1e9 / peak,
              "us_fused_cold_clean_l2": cold_us,
