@@ -1023,6 +1023,8 @@ def run_gpu(args):
                 for i in range(nitem)]
     per_item = [statistics.mean(t) for t in per_step]
     ms_per_step_item_events = sum(per_item)
+    # and each workload's cost in the undisturbed pipeline, from kernel end times
+    pipe, pipe_step_us = pipeline_times(items, min(args.steps, 20)) if world == 1 else (None, None)
 
     peak, peak_kind = peaks()
     # unfused per-op sequences (outside the timed region)
@@ -1032,6 +1034,9 @@ def run_gpu(args):
              "frac_of_" + peak_kind + "_peak": it.bytes / (ms / 1e3) / 1e9 / peak}
         q = np.percentile(ts, [10, 50, 90])
         d.update({"us_p10": q[0] * 1e3, "us_median": q[1] * 1e3, "us_p90": q[2] * 1e3})
+        if pipe:
+            d.update({"us_in_pipeline": pipe[it.name],
+                      "frac_in_pipeline": it.bytes / (pipe[it.name] * 1e-6) / 1e9 / peak})
         if it.unfused is not None and not args.no_unfused:
             ums = time_fn(it.unfused, reps=3, warm=1)
             L, T = launch_overhead(ums, ms, it.n_unfused)
@@ -1064,6 +1069,8 @@ def run_gpu(args):
             d.update({"mufu_ops": it.mufu_ops, "mufu_bound_us": mufu_us, "hbm_bound_us": hbm_us,
                       "bound": "mufu" if mufu_us > hbm_us else "hbm",
                       "frac_of_bound": max(mufu_us, hbm_us) / (ms * 1e3)})
+            if pipe:
+                d["frac_of_bound_in_pipeline"] = max(mufu_us, hbm_us) / pipe[it.name]
         per_chain[it.name] = d
     # next rows, measured beside the step (not part of its workload)
     next_rows = {}
@@ -1261,9 +1268,12 @@ def run_gpu(args):
                        "storage_dtypes": "f32/f16/bf16 per workload, arithmetic in f32"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clk, "per_chain": per_chain,
-            "per_chain_timing": "a second pass of the same steps with an event between every two "
-                                "launches (each time includes the launch gap the event causes; "
-                                f"that pass: {ms_per_step_item_events:.4f} ms a step)",
+            "per_chain_timing": "us_fused: a second pass of the same steps with an event between "
+                                "every two launches (each time includes the launch gap the event "
+                                f"causes; that pass: {ms_per_step_item_events:.4f} ms a step); "
+                                "us_in_pipeline: end of the workload's kernel minus end of the one "
+                                "before, from the CUPTI trace of up to 20 undisturbed steps"
+                                + (f" ({pipe_step_us / 1e3:.4f} ms a step)" if pipe else ""),
             "next_rows": next_rows, "size_sweep": size_sweep,
             "compile_cache": latency,
             "partial": ({"only": args.only, "flat_elems": args.flat_elems, "spec": args.spec}
@@ -1336,6 +1346,35 @@ def device_ops(fn):
             t0 = e.start_ns() / 1e3
             ops.append((t0, t0 + e.duration_ns() / 1e3, e.name()))
     return sorted(ops)
+
+
+def pipeline_times(items, steps):
+    """Each workload's cost inside the back-to-back step, from the kernels'
+    own end times: `steps` steps run under the CUPTI activity trace
+    (torch.profiler), which timestamps every kernel without serialising the
+    launches, and a workload's time is the end of its kernel minus the end of
+    the kernel before it.  With programmatic dependent launch a kernel's CTAs
+    may start before the previous kernel ends, so end-to-end differences, not
+    start-to-end durations, are what each kernel adds.  Returns
+    ({name: mean us}, mean step us), or (None, None) if the trace does not hold
+    one kernel per workload per step."""
+    import torch
+    from torch.profiler import ProfilerActivity, profile
+    device_ops(lambda: None)  # the process's first session can miss records
+    n = len(items)
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        for _ in range(steps):
+            for it in items:
+                it.fused()
+        torch.cuda.synchronize()
+    ends = sorted((e.start_ns() + e.duration_ns()) / 1e3 for e in prof.profiler.kineto_results.events()
+                  if e.device_type() == torch.autograd.DeviceType.CUDA)
+    if len(ends) != steps * n or steps < 2:
+        return None, None
+    per = {it.name: statistics.mean(ends[k * n + i] - ends[k * n + i - 1] for k in range(1, steps))
+           for i, it in enumerate(items)}
+    return per, (ends[-1] - ends[n - 1]) / (steps - 1)
 
 
 def launch_trace(items):
