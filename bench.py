@@ -439,6 +439,36 @@ def _rms_linear_item(dev, with_unfused, M=16384):
     return it
 
 
+def fast_math_row(dev, peak, peak_kind, mhz):
+    """The shuffle-prefixed 16-op chain (4 exp, 4 sigmoid) with its exp and
+    sigmoid in the opt-in fast form (exp:fast, sigmoid:fast: ex2.approx on
+    x * log2 e, validated against the oracle's bound for it) beside the
+    accurate form, launch after launch on the same tensors."""
+    import torch
+
+    import elementwise_chain_jit_gb300 as F
+    import workloads as W
+    cfg = W.SHUFFLE_CHAIN
+    body, dt = W.random_chain(16, 9, start_dtype=W.F16)
+    fast = ";".join("exp:fast" if o == "exp" else "sigmoid:fast" if o == "sigmoid" else o
+                    for o in body.split(";"))
+    n = int(np.prod(cfg["shape"]))
+    out = {}
+    for tag, spec in (("accurate", body), ("fast", fast)):
+        c = F.fuse_compile(f"shuffle:{cfg['groups']};{spec}", cfg["shape"], dt)
+        ins = [W.device_uniform(n, -2.0, 2.0, 200 + 16 + j, d, dev) for j, d in enumerate(c.in_dtypes)]
+        o = torch.empty(n, dtype=_tdt(c.out_dtype), device=dev)
+        out["us_" + tag] = time_fn(lambda: F.fuse_launch(c, ins, o), reps=20, warm=3) * 1e3
+        nb = sum(n * _esz(d) for d in c.in_dtypes) + n * _esz(c.out_dtype)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mufu_us = mufu_per_element(body) * n / (MUFU_PER_SM_CLK * sms * mhz * 1e6) * 1e6
+    out.update({"bytes": nb, "spec_fast": fast, "mufu_bound_us": mufu_us,
+                "hbm_bound_us": nb / (peak * 1e9) * 1e6,
+                "frac_of_mufu_bound_fast": mufu_us / out["us_fast"],
+                "frac_of_mufu_bound_accurate": mufu_us / out["us_accurate"]})
+    return {"shuffle_chain_L16_fast_math": out}
+
+
 def noalloc_row(dev, peak, peak_kind):
     """rope_qkv_split_noalloc at the most tokens its fixed array takes at
     head_dim 128 (8192 x 32 heads, bf16), beside rope_qkv_split on the same
@@ -1107,6 +1137,9 @@ def run_gpu(args):
         del rl
     if args.only is None or re.search(args.only, "rope_qkv_split_noalloc"):
         next_rows.update(noalloc_row(dev, peak, peak_kind))
+    if args.only is None or re.search(args.only, "fast_math"):
+        next_rows.update(fast_math_row(dev, peak, peak_kind,
+                                       clocks.summary().get("sm_mhz") or 2070.0))
     if (args.only is None or re.search(args.only, "decode_glue")) and not args.no_unfused:
         next_rows["decode_glue_32_layers_8_tokens"] = decode_glue(dev)
     # the chain sweep's smaller sizes (beside the step, not in it): 2^24 + 7

@@ -25,7 +25,10 @@
 
 namespace fuse {
 
-enum ChainOpCode { OP_ADD, OP_MUL, OP_SCALE, OP_RELU, OP_SIGMOID, OP_EXP, OP_CAST };
+enum ChainOpCode {
+  OP_ADD, OP_MUL, OP_SCALE, OP_RELU, OP_SIGMOID, OP_EXP, OP_CAST,
+  OP_SIGMOID_FAST, OP_EXP_FAST  // "sigmoid:fast", "exp:fast": opt-in approximations
+};
 
 struct ChainOp {
   ChainOpCode op;
@@ -101,8 +104,16 @@ int parse_chain(const char* spec, fuse_dtype in_dt, Chain* out) {
       op.op = OP_SCALE;
       op.c = c;
     } else if (name == "relu" || name == "sigmoid" || name == "exp") {
-      if (has_arg) return fail(FUSE_E_SPEC, fmt("'%s' takes no argument", name.c_str()));
-      op.op = name == "relu" ? OP_RELU : name == "sigmoid" ? OP_SIGMOID : OP_EXP;
+      // exp and sigmoid take the optional argument "fast": the hardware
+      // approximation of 2^x on x * log2(e), per expression ("DeepJIT"
+      // section 6.3: no global fast-math, intrinsics only where validated)
+      const bool fast = has_arg && arg == "fast" && name != "relu";
+      if (has_arg && !fast)
+        return fail(FUSE_E_SPEC, fmt("'%s' takes no argument but 'fast' (exp, sigmoid)",
+                                     name.c_str()));
+      op.op = name == "relu" ? OP_RELU
+              : name == "sigmoid" ? (fast ? OP_SIGMOID_FAST : OP_SIGMOID)
+                                  : (fast ? OP_EXP_FAST : OP_EXP);
     } else if (name == "cast") {
       if (!has_arg || parse_dtype(arg, &op.to))
         return fail(FUSE_E_SPEC, fmt("bad cast target '%s' (f16, bf16 or f32)", arg.c_str()));
@@ -182,7 +193,9 @@ int plan_chain(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_d
     bytes_per_elem += dtype_bytes(d);
   }
   bool transcendental = false;
-  for (auto& op : ch.ops) transcendental = transcendental || op.op == OP_EXP || op.op == OP_SIGMOID;
+  for (auto& op : ch.ops)
+    transcendental = transcendental || op.op == OP_EXP || op.op == OP_SIGMOID ||
+                     op.op == OP_EXP_FAST || op.op == OP_SIGMOID_FAST;
   // Measured on GB300 (sweep over the chain workloads): chains touching 12 or
   // more tensors run fastest with a small per-thread footprint (more warps,
   // the 13-input chain 1.64 ms vs 1.86 ms), others with the widest vectors
@@ -238,6 +251,8 @@ static void emit_op(std::ostringstream& s, const ChainOp& op, const std::string&
     // IEEE division
     case OP_SIGMOID: s << "      x = sigmoid(x);\n"; break;
     case OP_EXP: s << "      x = expf(x);\n"; break;
+    case OP_SIGMOID_FAST: s << "      x = sigmoid_fast(x);\n"; break;
+    case OP_EXP_FAST: s << "      x = exp_fast(x);\n"; break;
     case OP_CAST:
       if (op.to == FUSE_F16) s << "      x = round_f16(x);\n";
       else if (op.to == FUSE_BF16) s << "      x = round_bf16(x);\n";

@@ -66,6 +66,12 @@ typedef struct fuse_chain* fuse_handle;
  *   relu               x = x > 0 ? x : 0   (NaN and -0 give +0)
  *   sigmoid            x = 1 / (1 + exp(-x))
  *   exp                x = exp(x)
+ *   exp:fast, sigmoid:fast   the same, opt-in per expression, with exp taken
+ *                      as the hardware's 2^t (ex2.approx, flush to zero) on
+ *                      t = x * log2(e) in fp32: a relative error of up to
+ *                      (1.25 |x| + 3) * 2^-24, results below 2^-126 flushed
+ *                      ("DeepJIT" section 6.3: intrinsics per expression,
+ *                      once validated); the accurate forms use CUDA's expf
  *   cast:f16|bf16|f32  round x to that dtype; later tensors and the output
  *                      take it
  *   shuffle:G          (first item only) ChannelShuffle of input 0 with G

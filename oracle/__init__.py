@@ -9,7 +9,11 @@ What each function follows is cited in ``oracle.c``.  The spec language read
 here is the one the library's ``fuse_compile`` accepts::
 
     [shuffle:G;]op;op;...     op = add | mul | scale:<c> | relu | sigmoid
-                                   | exp | cast:f16 | cast:f32 | cast:bf16
+                                   | exp | sigmoid:fast | exp:fast
+                                   | cast:f16 | cast:f32 | cast:bf16
+
+``exp:fast`` and ``sigmoid:fast`` have the same exact value as exp and
+sigmoid; only the error bound the check allows the device differs.
 
 Reading of the multi-input chain of "DeepJIT" section 4.1 ((a + b) -> relu ->
 scale -> + c): ``add`` and ``mul`` each consume the next input tensor, which
@@ -36,7 +40,9 @@ DTYPE_NAMES = {v: k for k, v in DTYPE_CODES.items()}
 STORAGE = {F32: np.float32, F16: np.uint16, BF16: np.uint16}
 
 OP_ADD, OP_MUL, OP_SCALE, OP_RELU, OP_SIGMOID, OP_EXP, OP_CAST = 1, 2, 3, 4, 5, 6, 7
+OP_EXP_FAST, OP_SIGMOID_FAST = 8, 9
 _UNARY = {"relu": OP_RELU, "sigmoid": OP_SIGMOID, "exp": OP_EXP}
+_FAST = {"sigmoid": OP_SIGMOID_FAST, "exp": OP_EXP_FAST}
 
 
 def build(force: bool = False) -> str:
@@ -174,8 +180,9 @@ def parse_spec(spec: str, in_dtype: int) -> Chain:
             if not 0 < groups <= 1 << 20:
                 raise ValueError("shuffle groups outside 1..2^20")
             continue
-        if colon and name not in ("scale", "cast"):
-            raise ValueError(f"{name!r} takes no argument")
+        fast = colon and name in _FAST and arg == "fast"
+        if colon and name not in ("scale", "cast") and not fast:
+            raise ValueError(f"{name!r} takes no argument (exp and sigmoid take 'fast')")
         if name in ("add", "mul"):
             ops.append(OP_ADD if name == "add" else OP_MUL)
             args.append(0.0)
@@ -189,7 +196,7 @@ def parse_spec(spec: str, in_dtype: int) -> Chain:
             args.append(c)
             in_idx.append(0)
         elif name in _UNARY:
-            ops.append(_UNARY[name])
+            ops.append(_FAST[name] if fast else _UNARY[name])
             args.append(0.0)
             in_idx.append(0)
         elif name == "cast":

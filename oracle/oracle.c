@@ -47,7 +47,9 @@ enum {
   OP_RELU = 4,    /* x > 0 ? x : 0 */
   OP_SIGMOID = 5, /* 1 / (1 + exp(-x)) */
   OP_EXP = 6,     /* exp(x) */
-  OP_CAST = 7     /* round to dtype (arg), continue in the working type */
+  OP_CAST = 7,    /* round to dtype (arg), continue in the working type */
+  OP_EXP_FAST = 8,    /* exp(x), approximated on the device ("exp:fast") */
+  OP_SIGMOID_FAST = 9 /* 1 / (1 + exp(-x)), approximated likewise ("sigmoid:fast") */
 };
 
 /* ------------------------------------------------------------------ */
@@ -180,8 +182,10 @@ static double apply_op(int op, double x, double b, double c) {
     case OP_MUL: return x * b;
     case OP_SCALE: return x * c;
     case OP_RELU: return x > 0.0 ? x : 0.0; /* NaN and -0 give +0 */
-    case OP_SIGMOID: return 1.0 / (1.0 + exp(-x));
-    case OP_EXP: return exp(x);
+    case OP_SIGMOID:
+    case OP_SIGMOID_FAST: return 1.0 / (1.0 + exp(-x));
+    case OP_EXP:
+    case OP_EXP_FAST: return exp(x);
     case OP_CAST: return round_to((int)c, x);
     default: return NAN;
   }
@@ -248,6 +252,17 @@ void oracle_chain_eval(int n_ops, const int* ops, const double* args, const int*
  *                        1/4; expf 2 ulp, the add 1/2 ulp, the reciprocal
  *                        within 1 ulp, with margin), widened to
  *                        [0, sigma(v + E)] where 1 + exp(-x) can reach 2^126
+ *        exp:fast:       E' = e^v (e^E - 1) + (1.25 (|v| + E) + 3) u e^(v+E)
+ *                        + 2^-126 + eta
+ *                        (the device forms x * L with L the fp32 nearest log2 e:
+ *                        the product's rounding and L's are 1.25 u |x| in the
+ *                        exponent, a relative 1.25 u |x| in the result; the
+ *                        hardware 2^t is within 3 u relative; results below
+ *                        2^-126 flush to zero)
+ *        sigmoid:fast:   as sigmoid, with (1.25 (|v| + E) + 9) u in place of
+ *                        10 u (the fast exp's relative error reaches the
+ *                        sigmoid at most in full, plus the add and the
+ *                        reciprocal, with margin)
  *      with u = 2^-24 and eta = 2^-147 covering fp32 underflow.  Where the
  *      interval [v - E, v + E] straddles a rounding boundary of a cast or the
  *      fp32 overflow threshold, each outcome is followed as its own branch;
@@ -265,6 +280,7 @@ typedef struct {
 
 static const double U32 = 5.9604644775390625e-08; /* 2^-24 */
 static const double ETA = 5.605193857299268e-45;  /* 2^-147 */
+static const double FTZ32 = 1.1754943508222875e-38; /* 2^-126: flush-to-zero */
 
 static int f16_order(uint16_t h) { /* monotone integer image of an fp16 */
   return (h & 0x8000) ? -(int)(h & 0x7fff) : (int)h;
@@ -302,20 +318,27 @@ static int step_branch(int op, branch_t s, double b, double c, int out_dt_unused
       vn = exp(v);
       En = vn * expm1(E) + 4 * U32 * exp(v + E) + ETA;
       break;
-    case OP_SIGMOID: {
+    case OP_EXP_FAST:
+      vn = exp(v);
+      En = vn * expm1(E) + (1.25 * (fabs(v) + E) + 3) * U32 * exp(v + E) + FTZ32 + ETA;
+      break;
+    case OP_SIGMOID:
+    case OP_SIGMOID_FAST: {
+      /* the relative error of the device's exp, add and reciprocal */
+      const double c = op == OP_SIGMOID ? 10.0 : 1.25 * (fabs(v) + E) + 9.0;
       vn = 1.0 / (1.0 + exp(-v));
       /* |sigma'(x)| = sigma(x)(1 - sigma(x)) is largest at x = 0: take its
          maximum over [v - E, v + E] (mean value theorem) */
       double xm = (v - E <= 0.0 && v + E >= 0.0) ? 0.0 : (v > 0.0 ? v - E : v + E);
       double sm = 1.0 / (1.0 + exp(-xm));
       double dmax = sm * (1.0 - sm);
-      En = dmax * E + 10 * U32 * (vn + dmax * E) + ETA;
+      En = dmax * E + c * U32 * (vn + dmax * E) + ETA;
       /* from -x >= 87 on, 1 + exp(-x) may reach 2^126 (or overflow to inf) in
          fp32 and the device's reciprocal returns 0 for a true value below
          2^-126: accept any value in [0, sigma(v + E)] there */
       if (-(v - E) >= 87.0) {
         double hi = 1.0 / (1.0 + exp(-(v + E)));
-        if (hi * (1 + 10 * U32) > En) En = hi * (1 + 10 * U32) + ETA;
+        if (hi * (1 + c * U32) > En) En = hi * (1 + c * U32) + ETA;
       }
       break;
     }

@@ -61,7 +61,8 @@ def test_add_relu_scale_golden_on_device():
 
 # ------------------------------------------------------------ every fp16 input, one op
 
-@pytest.mark.parametrize("op", ["relu", "sigmoid", "exp", "scale:0.7529296875", "cast:bf16"])
+@pytest.mark.parametrize("op", ["relu", "sigmoid", "exp", "scale:0.7529296875", "cast:bf16",
+                                "exp:fast", "sigmoid:fast"])
 @pytest.mark.parametrize("out", ["f16", "f32"])
 def test_unary_op_on_every_fp16_value(op, out):
     """All 65,536 fp16 bit patterns (incl. subnormals, inf, NaN) through one
@@ -76,7 +77,8 @@ def test_unary_op_on_every_fp16_value(op, out):
     assert counts[3] == 0, (spec, counts)
 
 
-@pytest.mark.parametrize("op", ["sigmoid", "exp", "sigmoid;sigmoid"])
+@pytest.mark.parametrize("op", ["sigmoid", "exp", "sigmoid;sigmoid", "exp:fast", "sigmoid:fast",
+                                "sigmoid:fast;sigmoid:fast", "exp:fast;scale:0.5;exp:fast"])
 def test_transcendentals_over_the_fp32_range(op):
     """4M fp32 values spread over [-104, 104] plus the special values: where
     exp(-x) overflows, where 1 + exp(-x) passes 2^126 and the reciprocal
@@ -109,6 +111,20 @@ def _check(spec, dt, inputs, shape, got, idx=None):
 @pytest.mark.parametrize("n", [1, 33, 4099, (1 << 16) + 7])
 def test_random_chain_small(length, seed, n):
     spec, dt = workloads.random_chain(length, seed)
+    inputs, _ = workloads.chain_inputs(spec, dt, n, seed)
+    got, _ = _run_chain(spec, dt, inputs, (n,))
+    _check(spec, dt, inputs, (n,), got)
+
+
+@pytest.mark.parametrize("length", workloads.CHAIN_LENGTHS)
+@pytest.mark.parametrize("seed", [0, 1])
+def test_random_chain_with_fast_transcendentals(length, seed):
+    """Random chains with every exp and sigmoid in its opt-in fast form, at
+    2^16 + 7 elements, against the oracle's bound for the fast forms."""
+    spec, dt = workloads.random_chain(length, seed)
+    spec = ";".join("exp:fast" if o == "exp" else "sigmoid:fast" if o == "sigmoid" else o
+                    for o in spec.split(";"))
+    n = (1 << 16) + 7
     inputs, _ = workloads.chain_inputs(spec, dt, n, seed)
     got, _ = _run_chain(spec, dt, inputs, (n,))
     _check(spec, dt, inputs, (n,), got)

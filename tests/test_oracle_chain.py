@@ -157,9 +157,24 @@ def test_shuffle_extra_inputs_are_not_shuffled():
 
 # ------------------------------------------------------------ the acceptance check
 
-def _simulate_fp32_device(spec, in_dtype, inputs, shape, groups=0):
+L32 = np.float32(1.44269502162933349609375)  # the fp32 nearest log2(e)
+
+
+def _fast_exp(x, skew):
+    """The fast exp as the device forms it: t = fp32(x * L), then 2^t with a
+    relative error `skew` (the hardware's approximation), flushed to zero
+    below 2^-126."""
+    t = (x.astype(np.float32) * L32).astype(np.float32).astype(np.float64)
+    with np.errstate(all="ignore"):
+        y = (np.exp2(t) * (1 + skew)).astype(np.float32)
+    return np.where(np.abs(y) < np.float32(2.0 ** -126), np.float32(0), y)
+
+
+def _simulate_fp32_device(spec, in_dtype, inputs, shape, groups=0, fast_skew=2.4 * 2.0 ** -24):
     """A model of an fp32 device: every step rounds to fp32 once (exp and the
-    sigmoid's exp evaluated in binary64 then rounded, i.e. within 1/2 ulp)."""
+    sigmoid's exp evaluated in binary64 then rounded, i.e. within 1/2 ulp);
+    the fast variants through _fast_exp with a relative skew of fast_skew (the
+    largest error the hardware 2^t was measured to make is 2.45 * 2^-24)."""
     ch = oracle.parse_spec(spec, in_dtype)
     vals = [oracle.to_double(a, d).astype(np.float32) for a, d in zip(inputs, ch.in_dtypes)]
     x = vals[0]
@@ -181,6 +196,10 @@ def _simulate_fp32_device(spec, in_dtype, inputs, shape, groups=0):
             elif op == oracle.OP_SIGMOID:
                 e = np.exp(-x.astype(np.float64)).astype(np.float32)
                 x = np.float32(1) / (np.float32(1) + e)
+            elif op == oracle.OP_EXP_FAST:
+                x = _fast_exp(x, fast_skew)
+            elif op == oracle.OP_SIGMOID_FAST:
+                x = np.float32(1) / (np.float32(1) + _fast_exp(-x, fast_skew))
             elif op == oracle.OP_CAST:
                 if int(arg) == oracle.F16:
                     x = x.astype(np.float16).astype(np.float32)
@@ -239,3 +258,44 @@ def test_check_branches_at_an_fp16_midpoint():
         assert (fails == 0) == ok, (dev, counts)
     _, counts, _ = oracle.chain_check(spec, oracle.F32, [a, b], (1,), np.array([1.0], np.float32))
     assert counts[1] == 1  # accepted by the error-bound rule, not the flat one
+
+
+def _fast_chain(length, seed):
+    """A random chain with every exp and sigmoid in its fast form."""
+    spec, dt = workloads.random_chain(length, seed)
+    items = [("exp:fast" if o == "exp" else "sigmoid:fast" if o == "sigmoid" else o)
+             for o in spec.split(";")]
+    return ";".join(items), dt
+
+
+@pytest.mark.parametrize("length", [1, 2, 4, 8, 16, 32])
+@pytest.mark.parametrize("skew", [2.4, -2.4])
+def test_check_accepts_the_fast_variants_within_their_bound(length, skew):
+    spec, dt = _fast_chain(length, 5)
+    inputs, _ = workloads.chain_inputs(spec, dt, 4099, 11)
+    dev = _simulate_fp32_device(spec, dt, inputs, (4099,), fast_skew=skew * 2.0 ** -24)
+    fails, counts, _ = oracle.chain_check(spec, dt, inputs, (4099,), dev)
+    assert fails == 0 and counts[3] == 0, (spec, counts)
+
+
+def test_fast_exp_bound_is_tight_enough_to_catch_errors():
+    # every fp32 value in [-80, 80] on a 2^18 grid through exp:fast: the check
+    # passes the modelled device and fails one whose 2^t is 20 * 2^-24 off, or
+    # one that forgets the product's rounding and errs by 8 |x| 2^-24
+    x = np.linspace(-80, 80, 1 << 18).astype(np.float32)
+    ok = _simulate_fp32_device("exp:fast", oracle.F32, [x], x.shape)
+    assert oracle.chain_check("exp:fast", oracle.F32, [x], x.shape, ok)[0] == 0
+    bad = _simulate_fp32_device("exp:fast", oracle.F32, [x], x.shape, fast_skew=20 * 2.0 ** -24)
+    assert oracle.chain_check("exp:fast", oracle.F32, [x], x.shape, bad)[0] > 1000
+    worse = (ok.astype(np.float64) * (1 + 8 * np.abs(x) * 2.0 ** -24)).astype(np.float32)
+    assert oracle.chain_check("exp:fast", oracle.F32, [x], x.shape, worse)[0] > 1000
+    # the accurate exp's tighter bound refuses the fast device's results
+    assert oracle.chain_check("exp", oracle.F32, [x], x.shape, ok)[0] > 1000
+
+
+def test_fast_spec_parsing():
+    assert oracle.parse_spec("exp:fast;sigmoid:fast", oracle.F32).ops == [
+        oracle.OP_EXP_FAST, oracle.OP_SIGMOID_FAST]
+    for bad in ("relu:fast", "exp:slow", "add:fast"):
+        with pytest.raises(ValueError):
+            oracle.parse_spec(bad, oracle.F32)
