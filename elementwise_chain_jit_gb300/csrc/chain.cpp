@@ -148,6 +148,7 @@ struct ChainPlan {
   int64_t C = 1, HW = 1;
   bool dynamic = false;  // shape bucket: the leading dimension comes with the launch
   bool debug = false;    // FUSE_DEBUG_BOUNDS: every index checked against its tensor
+  bool prefetch = false;  // L2 prefetch of the first chunk before the launch-order wait
   int64_t inner = 1;     // elements per unit of the leading dimension
   std::string source;
 };
@@ -227,6 +228,9 @@ int plan_chain(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_d
   }
   p->vec_ok = !ch.groups || (p->HW % p->vec == 0);
   p->debug = env_int("FUSE_DEBUG_BOUNDS", 0) == 1;
+  // the bulk prefetch needs 16-byte aligned ranges: every tensor's vector a
+  // multiple of 16 bytes (the vector kernel's pointers are 16-byte aligned)
+  p->prefetch = env_int("FUSE_CHAIN_PREFETCH", 1) == 1 && p->vec * minb >= 16;
   return FUSE_OK;
 }
 
@@ -383,10 +387,36 @@ static std::string gen_chain_source(const ChainPlan& p, const char* spec) {
          "    u32 wo[NWO];\n    apply(";
     for (int j = 0; j < nin; ++j) s << "r" << j << "[u], ";
     s << "wo);\n    store_words(static_cast<u32*>(a.out) + v * NWO, wo);\n  }\n}\n";
+    if (p.prefetch) {
+      // Before the wait for the previous kernel on the stream (programmatic
+      // dependent launch lets this grid's first CTAs start while it drains):
+      // one thread per CTA asks L2 for the CTA's first chunk of every input.
+      // L2 is where global memory is coherent, so a line the previous kernel
+      // still writes is updated there, and every load of the chunk is issued
+      // after the wait.
+      s << "\n__device__ __forceinline__ void prefetch_chunk(const Args& a, idx_t c) {\n";
+      for (int j = 0; j < nin; ++j) {
+        if (j == 0 && ch.groups) {
+          // the shuffled input: the chunk's source is one run per plane
+          s << "  for (idx_t v = c * (idx_t)CHUNK, e = v + (idx_t)CHUNK; v < e;) {\n"
+               "    const idx_t pe = (v / VPP + 1) * VPP, se = pe < e ? pe : e;\n"
+               "    prefetch_l2(static_cast<const u32*>(a.in[0]) + (idx_t)src_vec(v) * NW0,\n"
+               "                (unsigned)((se - v) * NW0 * 4));\n"
+               "    v = se;\n  }\n";
+        } else {
+          s << "  prefetch_l2(static_cast<const u32*>(a.in[" << j << "]) + c * (idx_t)CHUNK * NW" << j
+            << ", (unsigned)(CHUNK * NW" << j << " * 4));\n";
+        }
+      }
+      s << "}\n";
+    }
     // sizes: compile-time constants for a fixed shape (the compiler folds
     // every branch below), the launch's element count for a shape bucket
-    s << "\nextern \"C\" __global__ void __launch_bounds__(BLOCK) fuse_chain_vec(const Args a) {\n"
-         "  pdl_enter();\n"
+    s << "\nextern \"C\" __global__ void __launch_bounds__(BLOCK) fuse_chain_vec(const Args a) {\n";
+    if (p.prefetch)
+      s << "  if (threadIdx.x == 0 && (idx_t)blockIdx.x < (idx_t)SIZE_N(a) / VEC / (idx_t)CHUNK)\n"
+           "    prefetch_chunk(a, blockIdx.x);\n";
+    s << "  pdl_enter();\n"
          "  const idx_t n = (idx_t)SIZE_N(a), nvec = n / VEC, nfull = nvec / (idx_t)CHUNK;\n"
          "  const idx_t nrem = nvec - nfull * (idx_t)CHUNK, tail = n - nvec * VEC;\n"
          "  for (idx_t c = blockIdx.x; c < nfull; c += gridDim.x)\n"

@@ -194,6 +194,12 @@ __device__ __forceinline__ void store_words(u32* p, const u32 (&w)[NW]) {
   }
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (one thread issues it; p 16-byte
+// aligned, bytes a multiple of 16).  A hint: it reads nothing into registers.
+__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------- launch order
 // Programmatic dependent launch (sm_90 and later).  A kernel launched with the
 // programmatic-serialization attribute may have its CTAs scheduled before the
