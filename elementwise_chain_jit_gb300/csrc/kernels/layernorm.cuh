@@ -4,6 +4,8 @@
 //   DT, HIDDEN, BLOCK, VEC, R   as for rmsnorm.cuh
 //   HAS_RES, HAS_GAMMA, HAS_BETA  0/1: residual add, scale, shift present
 //   FUSE_LN_VEC  1 when a vector width fits the row
+//   ROW_PREFETCH  1: the vector kernel asks L2 for its first row before the
+//           launch-order wait
 //
 // Per row ("DeepJIT ... 串行小核墙" section 4.3: one block per row, the
 // statistics reduced in the block, then the normalisation in the same pass
@@ -28,6 +30,15 @@ constexpr int NWV = VEC * Dt<DT>::bytes / 4;
 extern "C" __global__ void __maxnreg__(LN_MAX_REGS)
 layernorm_vec(const void* x, const void* res, const void* gamma, const void* beta, void* out,
               void* res_out, long long rows, float eps) {
+  // ask L2 for the CTA's first row before waiting for the previous kernel
+  // (programmatic dependent launch; L2 is coherent, the loads come after)
+  if constexpr (ROW_PREFETCH && (VEC * Dt<DT>::bytes) % 16 == 0) {
+    if (threadIdx.x == 0 && blockIdx.x < rows) {
+      constexpr unsigned RB = HIDDEN * Dt<DT>::bytes;
+      prefetch_l2(static_cast<const char*>(x) + blockIdx.x * (long long)RB, RB);
+      if constexpr (HAS_RES) prefetch_l2(static_cast<const char*>(res) + blockIdx.x * (long long)RB, RB);
+    }
+  }
   pdl_enter();
   // one buffer per statistic: a row's second barrier separates its reads of
   // psum from the next row's writes, and the next row's first barrier its

@@ -9,6 +9,8 @@
 //   R       vectors per thread: ceil(HIDDEN / VEC / BLOCK)
 //   FUSE_RMS_VEC  1 when a vector width fits the row (else only the
 //           scalar kernel exists)
+//   ROW_PREFETCH  1: the vector kernel asks L2 for its first row before the
+//           launch-order wait
 //
 // Per row ("TeleTron", sections 3.3 and 4.2): h = x + residual in fp32,
 // residual_out = dt(h), ms = sum(h^2)/HIDDEN accumulated in fp32,
@@ -27,6 +29,15 @@ constexpr int NWV = VEC * Dt<DT>::bytes / 4;      // words per vector
 extern "C" __global__ void __launch_bounds__(BLOCK)
 rmsnorm_vec(const void* x, const void* res, const void* w, void* out, void* res_out,
             long long rows, float eps) {
+  // ask L2 for the CTA's first row before waiting for the previous kernel
+  // (programmatic dependent launch; L2 is coherent, the loads come after)
+  if constexpr (ROW_PREFETCH && (VEC * Dt<DT>::bytes) % 16 == 0) {
+    if (threadIdx.x == 0 && blockIdx.x < rows) {
+      constexpr unsigned RB = HIDDEN * Dt<DT>::bytes;
+      prefetch_l2(static_cast<const char*>(x) + blockIdx.x * (long long)RB, RB);
+      prefetch_l2(static_cast<const char*>(res) + blockIdx.x * (long long)RB, RB);
+    }
+  }
   pdl_enter();
   __shared__ float part[2][NWARPS];
   for (long long row = blockIdx.x, it = 0; row < rows; row += gridDim.x, ++it) {

@@ -7,6 +7,8 @@
 //   VEC     elements of each half a q/k item covers (HALF % VEC == 0)
 //   VV      elements a v item copies (HD % VV == 0)
 //   FUSE_ROPE_VEC  1 when vector widths fit (else only the scalar kernel)
+//   ROW_PREFETCH  1: the vector kernel asks L2 for its token's row before
+//           the launch-order wait
 //
 // qkv is [tokens, 3, HEADS, HD]; q, k, v are [HEADS, tokens, HD], with the
 // token count a launch argument (one CTA per token), so one compiled kernel
@@ -35,6 +37,13 @@ constexpr int HD_WORDS = HD * BYTES / 4;
 extern "C" __global__ void __launch_bounds__(BLOCK)
 rope_vec(const void* qkv, void* q, void* k, void* v, const float* table, long long pos0,
          long long tokens) {
+  // ask L2 for the token's qkv row before waiting for the previous kernel
+  // (programmatic dependent launch; L2 is coherent, the loads come after)
+  if constexpr (ROW_PREFETCH && (VEC * BYTES) % 16 == 0 && (VV * BYTES) % 16 == 0) {
+    if (threadIdx.x == 0)
+      prefetch_l2(static_cast<const u32*>(qkv) + blockIdx.x * TOKEN_WORDS,
+                  static_cast<unsigned>(TOKEN_WORDS * 4));
+  }
   pdl_enter();
   const long long t = blockIdx.x;
   const u32* src = static_cast<const u32*>(qkv) + t * TOKEN_WORDS;

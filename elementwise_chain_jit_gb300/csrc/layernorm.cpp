@@ -39,6 +39,16 @@ int max_regs(int block, int64_t r) {
   return std::min(limit, std::max(24, want));
 }
 
+// the first-row L2 prefetch before the launch-order wait (FUSE_ROW_PREFETCH=0
+// turns it off; read once)
+int row_prefetch() {
+  static const int on = [] {
+    const char* e = getenv("FUSE_ROW_PREFETCH");
+    return e && *e == '0' ? 0 : 1;
+  }();
+  return on;
+}
+
 int ln_kernel(int64_t hidden, fuse_dtype dt, int flags, LnKernel* out) {
   std::lock_guard<std::mutex> lk(g_mu);
   auto key = std::make_tuple(hidden, static_cast<int>(dt), flags);
@@ -61,10 +71,10 @@ int ln_kernel(int64_t hidden, fuse_dtype dt, int flags, LnKernel* out) {
       "constexpr int DT = %d;\nconstexpr int HIDDEN = %lld;\nconstexpr int BLOCK = %d;\n"
       "constexpr int VEC = %d;\nconstexpr int R = %lld;\n"
       "constexpr bool HAS_RES = %s, HAS_GAMMA = %s, HAS_BETA = %s;\n#define FUSE_LN_VEC %d\n"
-      "#define LN_MAX_REGS %d\n#include \"fuse/layernorm.cuh\"\n",
+      "#define LN_MAX_REGS %d\n#define ROW_PREFETCH %d\n#include \"fuse/layernorm.cuh\"\n",
       (long long)hidden, dtype_name(dt), static_cast<int>(dt), (long long)hidden, k.block, k.vec,
       (long long)r, (flags & 1) ? "true" : "false", (flags & 2) ? "true" : "false",
-      (flags & 4) ? "true" : "false", k.has_vec ? 1 : 0, max_regs(k.block, r));
+      (flags & 4) ? "true" : "false", k.has_vec ? 1 : 0, max_regs(k.block, r), row_prefetch());
   if (int rc = jit_compile(src, "layernorm_residual", &k.mod)) return rc;
   g_kernels.emplace(key, k);
   *out = k;

@@ -8,6 +8,7 @@
 // residual are read once with 32-byte loads, and both outputs are written
 // once.
 #include <algorithm>
+#include <cstdlib>
 #include <map>
 
 #include "internal.h"
@@ -23,6 +24,16 @@ struct RmsKernel {
 
 std::mutex g_mu;
 std::map<std::pair<int64_t, int>, RmsKernel> g_kernels;
+
+// the first-row L2 prefetch before the launch-order wait (FUSE_ROW_PREFETCH=0
+// turns it off; read once)
+int row_prefetch() {
+  static const int on = [] {
+    const char* e = getenv("FUSE_ROW_PREFETCH");
+    return e && *e == '0' ? 0 : 1;
+  }();
+  return on;
+}
 
 int rms_kernel(int64_t hidden, fuse_dtype dt, RmsKernel* out) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -45,9 +56,9 @@ int rms_kernel(int64_t hidden, fuse_dtype dt, RmsKernel* out) {
       "// residual add + RMSNorm + cast, hidden %lld, %s\n"
       "constexpr int DT = %d;\nconstexpr int HIDDEN = %lld;\nconstexpr int BLOCK = %d;\n"
       "constexpr int VEC = %d;\nconstexpr int R = %lld;\n#define FUSE_RMS_VEC %d\n"
-      "#include \"fuse/rmsnorm.cuh\"\n",
+      "#define ROW_PREFETCH %d\n#include \"fuse/rmsnorm.cuh\"\n",
       (long long)hidden, dtype_name(dt), static_cast<int>(dt), (long long)hidden, k.block, k.vec,
-      (long long)r, k.has_vec ? 1 : 0);
+      (long long)r, k.has_vec ? 1 : 0, row_prefetch());
   if (int rc = jit_compile(src, "rmsnorm_residual", &k.mod)) return rc;
   g_kernels.emplace(key, k);
   *out = k;

@@ -8,6 +8,7 @@
 // (fp64-built, fp32-stored) that stays resident in L2 across the 2*H q/k rows
 // of a token.
 #include <algorithm>
+#include <cstdlib>
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -44,6 +45,16 @@ int pick_vec(int n, int bytes) {
   return v * bytes >= 4 ? v : 0;
 }
 
+// the token-row L2 prefetch before the launch-order wait
+// (FUSE_ROW_PREFETCH=0 turns it off; read once)
+int row_prefetch() {
+  static const int on = [] {
+    const char* e = getenv("FUSE_ROW_PREFETCH");
+    return e && *e == '0' ? 0 : 1;
+  }();
+  return on;
+}
+
 // One kernel per (heads, head_dim, dtype): the token count and the start
 // position come with the launch, so a serving loop whose batch changes every
 // step compiles nothing after its first call.
@@ -67,9 +78,9 @@ int rope_kernel(int heads, int hd, fuse_dtype dt, RopeKernel* out) {
       "constexpr int DT = %d;\nconstexpr int HEADS = %d;\nconstexpr int HD = %d;\n"
       "constexpr int HALF = %d;\nconstexpr int BLOCK = %d;\n"
       "constexpr int VEC = %d;\nconstexpr int VV = %d;\n#define FUSE_ROPE_VEC %d\n"
-      "#include \"fuse/rope.cuh\"\n",
+      "#define ROW_PREFETCH %d\n#include \"fuse/rope.cuh\"\n",
       heads, hd, dtype_name(dt), static_cast<int>(dt), heads, hd, hd / 2, k.block, k.vec, k.vv,
-      k.has_vec ? 1 : 0);
+      k.has_vec ? 1 : 0, row_prefetch());
   if (int rc = jit_compile(src, "rope_qkv_split", &k.mod)) return rc;
   g_kernels.emplace(key, k);
   *out = k;
