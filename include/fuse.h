@@ -260,8 +260,9 @@ int rope_qkv_split(const void* qkv, void* q, void* k, void* v, int64_t tokens, i
  * Arguments, layouts and results as rope_qkv_split.  It calls no cudaMalloc,
  * cudaFree or allocating routine: the cos/sin rows of the call are built into
  * a fixed array inside the library's module (2^20 fp32 values, 4 MB, held on
- * every device that has loaded the library until the process exits), and both
- * of its kernels are compiled ahead of time.
+ * every device that has loaded the library until the process exits), and its
+ * kernels (the rows build and, per dtype, a 16-byte-vector and an
+ * element-wise rotation) are compiled ahead of time.
  *   - tokens * head_dim must be <= 2^20, and pos0 + tokens <= 2^22, else
  *     FUSE_E_SHAPE.
  *   - All calls on a device share the array; each call rewrites the rows it
