@@ -138,16 +138,23 @@ class ClockSampler:
 # ---------------------------------------------------------------- workload
 
 # Special-function unit (MUFU) work of a chain: exp is one ex2, sigmoid one
-# ex2 and one rcp (the generated code's exp and sigmoid); the unit retires 16
-# of these per SM and clock (NVIDIA's documented arithmetic throughput).  With
-# the HBM bytes this gives two lower bounds on a chain's time; exp-heavy chains
-# can be bound by instruction issue instead, which is not modelled here.
-MUFU_PER_SM_CLK = 16
+# ex2 and one rcp (the generated code's exp and sigmoid, accurate or fast).
+# Measured on GB300 with independent chains of each instruction on every SM:
+# ex2.approx 9.48 T/s and rcp.approx 4.79 T/s, 30 and 15 per SM and clock at
+# 2.07 GHz over 152 SMs -- the rates of 32 and 16 per SM-clock at a clock 5 %
+# lower; twice Blackwell's documented 16 for ex2, the same for rcp.  An even mix
+# of the two runs at 20 per SM-clock: one unit, where an ex2 takes half the
+# issue slot of an rcp.  With the HBM bytes this gives two lower bounds on a
+# chain's time; chains heavy in the accurate exp and sigmoid can be bound by
+# instruction issue instead, which is not modelled here.
+EX2_PER_SM_CLK, RCP_PER_SM_CLK = 32, 16
 
 
-def mufu_per_element(spec):
+def mufu_clocks_per_element(spec):
+    """SM clocks of special-function unit work per element of a chain."""
     ops = [o.split(":")[0] for o in spec.split(";")]
-    return ops.count("exp") + 2 * ops.count("sigmoid")
+    n_sig = ops.count("sigmoid")
+    return (ops.count("exp") + n_sig) / EX2_PER_SM_CLK + n_sig / RCP_PER_SM_CLK
 
 
 class Item:
@@ -158,7 +165,9 @@ class Item:
         self.unfused, self.n_unfused = unfused, n_unfused
         self.kernel = kernel
         self.inputs, self.outputs = [], []   # device tensors (for the end-to-end copies)
-        self.mufu_ops = 0
+        # the same launch on other tensors of the same shapes (ins, outs)
+        self.launch_on = None
+        self.mufu_clocks = 0.0   # SM clocks of special-function unit work
 
 
 def _tdt(dt):
@@ -195,7 +204,8 @@ def build_items(dev, with_unfused=True, only=None, flat_elems=None, spec=None, s
         nbytes = sum(n * _esz(d) for d in c.in_dtypes) + n * _esz(c.out_dtype)
         it = Item(name, nbytes, lambda: F.fuse_launch(c, ins, out), kernel=("chain", spec, shape, dt))
         it.inputs, it.outputs = ins, [out]
-        it.mufu_ops = n * mufu_per_element(spec)
+        it.launch_on = lambda i_s, o_s: F.fuse_launch(c, i_s, o_s[0])
+        it.mufu_clocks = n * mufu_clocks_per_element(spec)
         if with_unfused:
             it.unfused, it.n_unfused = unfused_chain(spec, dt, shape, ins, out)
         return it
@@ -247,6 +257,7 @@ def _shuffle_item(dev, with_unfused):
               lambda: F.channel_shuffle(x, out, g, W.F16, shape=(n, c, h, w)),
               kernel=("chain", f"shuffle:{g}", cfg["shape"], W.F16))
     it.inputs, it.outputs = [x], [out]
+    it.launch_on = lambda i_s, o_s: F.channel_shuffle(i_s[0], o_s[0], g, W.F16, shape=(n, c, h, w))
     if with_unfused:
         def unfused():
             return x.view(n, g, c // g, h, w).transpose(1, 2).contiguous().view(n, c, h, w)
@@ -270,6 +281,7 @@ def _rms_item(dev, with_unfused):
               lambda: F.rmsnorm_residual(x, r, w, y, ro, rc["eps"], W.BF16),
               kernel=("rmsnorm",))
     it.inputs, it.outputs = [x, r, w], [y, ro]
+    it.launch_on = lambda i_s, o_s: F.rmsnorm_residual(*i_s, *o_s, rc["eps"], W.BF16)
     if with_unfused:
         def rms_unfused():
             h = x + r
@@ -391,6 +403,7 @@ def _ln_item(dev, with_unfused):
     it = Item(f"layernorm_residual_{rows}x{hidden}_bf16", 4 * rows * hidden * 2 + 2 * hidden * 2,
               lambda: F.layernorm_residual(x, r, g, b, y, ro, eps, W.BF16), kernel=("layernorm",))
     it.inputs, it.outputs = [x, r, g, b], [y, ro]
+    it.launch_on = lambda i_s, o_s: F.layernorm_residual(*i_s, *o_s, eps, W.BF16)
     if with_unfused:
         def ln_unfused():
             h = x + r
@@ -443,7 +456,8 @@ def fast_math_row(dev, peak, peak_kind, mhz):
     """The shuffle-prefixed 16-op chain (4 exp, 4 sigmoid) with its exp and
     sigmoid in the opt-in fast form (exp:fast, sigmoid:fast: ex2.approx on
     x * log2 e, validated against the oracle's bound for it) beside the
-    accurate form, launch after launch on the same tensors."""
+    accurate form, each timed as the step's workloads are on their own
+    (steady_times)."""
     import torch
 
     import elementwise_chain_jit_gb300 as F
@@ -458,14 +472,19 @@ def fast_math_row(dev, peak, peak_kind, mhz):
         c = F.fuse_compile(f"shuffle:{cfg['groups']};{spec}", cfg["shape"], dt)
         ins = [W.device_uniform(n, -2.0, 2.0, 200 + 16 + j, d, dev) for j, d in enumerate(c.in_dtypes)]
         o = torch.empty(n, dtype=_tdt(c.out_dtype), device=dev)
-        out["us_" + tag] = time_fn(lambda: F.fuse_launch(c, ins, o), reps=20, warm=3) * 1e3
         nb = sum(n * _esz(d) for d in c.in_dtypes) + n * _esz(c.out_dtype)
+        it = Item(tag, nb, None)
+        it.inputs, it.outputs = ins, [o]
+        it.launch_on = lambda i_s, o_s, c=c: F.fuse_launch(c, i_s, o_s[0])
+        out["us_" + tag] = steady_times(it, 60)[0]
+        del it, ins, o
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    mufu_us = mufu_per_element(body) * n / (MUFU_PER_SM_CLK * sms * mhz * 1e6) * 1e6
-    out.update({"bytes": nb, "spec_fast": fast, "mufu_bound_us": mufu_us,
-                "hbm_bound_us": nb / (peak * 1e9) * 1e6,
-                "frac_of_mufu_bound_fast": mufu_us / out["us_fast"],
-                "frac_of_mufu_bound_accurate": mufu_us / out["us_accurate"]})
+    mufu_us = mufu_clocks_per_element(body) * n / (sms * mhz * 1e6) * 1e6
+    hbm_us = nb / (peak * 1e9) * 1e6
+    out.update({"bytes": nb, "spec_fast": fast, "mufu_bound_us": mufu_us, "hbm_bound_us": hbm_us,
+                "bound": "mufu" if mufu_us > hbm_us else "hbm",
+                "frac_of_bound_fast": max(mufu_us, hbm_us) / out["us_fast"],
+                "frac_of_bound_accurate": max(mufu_us, hbm_us) / out["us_accurate"]})
     return {"shuffle_chain_L16_fast_math": out}
 
 
@@ -504,6 +523,8 @@ def _rope_item(dev, with_unfused):
               lambda: F.rope_qkv_split(qkv, q, k, v, H, D, pc["pos0"], pc["base"], W.BF16),
               kernel=("rope",))
     it.inputs, it.outputs = [qkv], [q, k, v]
+    it.launch_on = lambda i_s, o_s: F.rope_qkv_split(i_s[0], *o_s, H, D, pc["pos0"], pc["base"],
+                                                     W.BF16)
     if with_unfused:
         pos = torch.arange(T, device=dev, dtype=torch.float64)
         inv = pc["base"] ** (-torch.arange(0, D, 2, device=dev, dtype=torch.float64) / D)
@@ -540,6 +561,7 @@ def _detect_item(dev, with_unfused):
               lambda: dec(feats, dout),
               kernel=("detect",))
     it.inputs, it.outputs = feats, [dout]
+    it.launch_on = lambda i_s, o_s: dec(i_s, o_s[0])
     if with_unfused:
         an = torch.tensor(anchors, dtype=torch.float32, device=dev)
         grids = []
@@ -652,6 +674,60 @@ def graph_per_launch(fn, k=20):
         b.synchronize()
     g.release()
     return a.elapsed_time(b) / k
+
+
+def steady_times(item, launches):
+    """One workload launched back to back on its own, `launches` times, on
+    rotating buffer sets: its own tensors and copies of them, enough sets that
+    together they exceed twice the L2, so every launch reads its inputs from
+    HBM and the dirty lines one launch leaves drain during the next ones, as
+    in any pipeline.  The launches are captured into one library graph (from
+    the host a few-microsecond kernel would wait on its own launch) and
+    replayed with launch-order overlap intact and no event between them.
+    Returns (mean us a launch from events around one replay, per-launch us
+    from the CUPTI trace of another -- end of a kernel minus the end of the
+    one before, the first launch left out -- or None where the trace does not
+    hold one kernel per launch)."""
+    import torch
+    from torch.profiler import ProfilerActivity, profile
+
+    import elementwise_chain_jit_gb300 as F
+    nsets = 1 if item.bytes >= 2 * L2_BYTES else int(2 * L2_BYTES // item.bytes) + 2
+    sets = [(item.inputs, item.outputs)]
+    sets += [([t.clone() for t in item.inputs], [torch.empty_like(t) for t in item.outputs])
+             for _ in range(nsets - 1)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i_s, o_s in sets:
+            item.launch_on(i_s, o_s)
+    s.synchronize()
+    F.fuse_graph_begin(s)
+    with torch.cuda.stream(s):
+        for k in range(launches):
+            item.launch_on(*sets[k % nsets])
+    g = F.fuse_graph_end(s)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g.launch(s)
+    s.synchronize()
+    a.record(s)
+    g.launch(s)
+    b.record(s)
+    b.synchronize()
+    mean_us = a.elapsed_time(b) / launches * 1e3
+    # a third replay under the trace (which adds its own cost to the replay)
+    device_ops(lambda: None)  # the process's first session can miss records
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        g.launch(s)
+        s.synchronize()
+    g.release()
+    ends = sorted((e.start_ns() + e.duration_ns()) / 1e3 for e in prof.profiler.kineto_results.events()
+                  if e.device_type() == torch.autograd.DeviceType.CUDA)
+    per = None
+    if len(ends) == launches:
+        per = [ends[i] - ends[i - 1] for i in range(1, launches)]
+    del sets
+    return mean_us, per
 
 
 def cold_time(item, reps=10):
@@ -1064,11 +1140,20 @@ def run_gpu(args):
     peak, peak_kind = peaks()
     # unfused per-op sequences (outside the timed region)
     per_chain = {}
-    for it, ms, ts in zip(items, per_item, per_step):
-        d = {"bytes": it.bytes, "us_fused": ms * 1e3, "gbs": it.bytes / (ms / 1e3) / 1e9,
+    for it, ems, ts in zip(items, per_item, per_step):
+        # the workload's own figure: back to back on rotating buffer sets
+        st_us, st_per = steady_times(it, 60 if it.bytes < 1e9 else 10)
+        ms = st_us / 1e3
+        d = {"bytes": it.bytes, "us_fused": st_us, "gbs": it.bytes / (ms / 1e3) / 1e9,
              "frac_of_" + peak_kind + "_peak": it.bytes / (ms / 1e3) / 1e9 / peak}
+        if st_per:
+            q = np.percentile(st_per, [10, 50, 90])
+            d.update({"us_p10": q[0], "us_median": q[1], "us_p90": q[2]})
+        # inside the step, an event between every two launches
         q = np.percentile(ts, [10, 50, 90])
-        d.update({"us_p10": q[0] * 1e3, "us_median": q[1] * 1e3, "us_p90": q[2] * 1e3})
+        d.update({"us_in_step_events": ems * 1e3,
+                  "frac_in_step_events": it.bytes / (ems / 1e3) / 1e9 / peak,
+                  "us_in_step_events_p10_p50_p90": [q[0] * 1e3, q[1] * 1e3, q[2] * 1e3]})
         if pipe:
             d.update({"us_in_pipeline": pipe[it.name],
                       "frac_in_pipeline": it.bytes / (pipe[it.name] * 1e-6) / 1e9 / peak})
@@ -1094,14 +1179,14 @@ def run_gpu(args):
             copy_us = cold_time(_Copy, reps=40)
             d.update({"us_device_copy_cold_clean_l2": copy_us,
                       "frac_of_device_copy_cold": copy_us / cold_us})
-        if it.mufu_ops:
+        if it.mufu_clocks:
             # two rooflines: HBM bytes and special-function unit operations
             # at the clock sampled during the timed region
             mhz = clocks.summary().get("sm_mhz") or 2070.0
             sms = torch.cuda.get_device_properties(dev).multi_processor_count
-            mufu_us = it.mufu_ops / (MUFU_PER_SM_CLK * sms * mhz * 1e6) * 1e6
+            mufu_us = it.mufu_clocks / (sms * mhz * 1e6) * 1e6
             hbm_us = it.bytes / (peak * 1e9) * 1e6
-            d.update({"mufu_ops": it.mufu_ops, "mufu_bound_us": mufu_us, "hbm_bound_us": hbm_us,
+            d.update({"mufu_bound_us": mufu_us, "hbm_bound_us": hbm_us,
                       "bound": "mufu" if mufu_us > hbm_us else "hbm",
                       "frac_of_bound": max(mufu_us, hbm_us) / (ms * 1e3)})
             if pipe:
@@ -1112,12 +1197,19 @@ def run_gpu(args):
     import re
     if args.only is None or re.search(args.only, f"layernorm_residual_{LN_ROWS[0]}x4096_bf16"):
         ln = _ln_item(dev, with_unfused=not args.no_unfused)
-        lms = time_fn(ln.fused, reps=20, warm=3)
+        st_us, st_per = steady_times(ln, 60)
+        lms = st_us / 1e3
+        ems = time_fn(ln.fused, reps=20, warm=3)
         cold_us = cold_time(ln, reps=20)
-        d = {"bytes": ln.bytes, "us_fused": lms * 1e3, "gbs": ln.bytes / (lms / 1e3) / 1e9,
+        d = {"bytes": ln.bytes, "us_fused": st_us, "gbs": ln.bytes / (lms / 1e3) / 1e9,
              "frac_of_" + peak_kind + "_peak": ln.bytes / (lms / 1e3) / 1e9 / peak,
+             "us_events_one_launch": ems * 1e3,
+             "frac_events_one_launch": ln.bytes / (ems / 1e3) / 1e9 / peak,
              "us_fused_cold_clean_l2": cold_us,
              "frac_cold_clean_l2": ln.bytes / (cold_us * 1e-6) / 1e9 / peak}
+        if st_per:
+            q = np.percentile(st_per, [10, 50, 90])
+            d.update({"us_p10": q[0], "us_median": q[1], "us_p90": q[2]})
         if ln.unfused is not None:
             ums = time_fn(ln.unfused, reps=3, warm=1)
             d.update({"us_unfused": ums * 1e3, "unfused_kernels": ln.n_unfused,
@@ -1317,12 +1409,19 @@ def run_gpu(args):
                        "storage_dtypes": "f32/f16/bf16 per workload, arithmetic in f32"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clk, "per_chain": per_chain,
-            "per_chain_timing": "us_fused: a second pass of the same steps with an event between "
-                                "every two launches (each time includes the launch gap the event "
-                                f"causes; that pass: {ms_per_step_item_events:.4f} ms a step); "
-                                "us_in_pipeline: end of the workload's kernel minus end of the one "
-                                "before, from the CUPTI trace of up to 20 undisturbed steps"
-                                + (f" ({pipe_step_us / 1e3:.4f} ms a step)" if pipe else ""),
+            "per_chain_timing": "us_fused (gbs, frac_of_*_peak): the workload on its own, 60 "
+                                "launches (10 above 1 GB) back to back on rotating buffer sets "
+                                "that together exceed twice the L2, replayed from one graph, mean "
+                                "from events around the replay; us_p10/us_median/us_p90: the same "
+                                "launches, end of each kernel minus the end of the one before "
+                                "(CUPTI); us_in_step_events: the step's launches again with an "
+                                "event between every two (each time includes the launch gap the "
+                                f"event causes; that pass: {ms_per_step_item_events:.4f} ms a "
+                                "step); us_in_pipeline: end of the workload's kernel minus end of "
+                                "the one before, from the CUPTI trace of up to 20 undisturbed "
+                                "steps" + (f" ({pipe_step_us / 1e3:.4f} ms a step)" if pipe else "")
+                                + "; us_fused_cold_clean_l2: one launch after L2 is evicted with "
+                                "clean lines, events around it, mean of 40 (5 above 1 GB)",
             "next_rows": next_rows, "size_sweep": size_sweep,
             "compile_cache": latency,
             "partial": ({"only": args.only, "flat_elems": args.flat_elems, "spec": args.spec}

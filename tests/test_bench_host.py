@@ -35,13 +35,14 @@ def test_reference_arm_prints_one_json_line(capsys):
     assert line["e2e"]["h2d_bytes_per_step"] == 0
 
 
-def test_mufu_count_of_a_chain():
-    # exp: one ex2; sigmoid: one ex2 and one rcp; the prologue, scale
-    # constants and the other ops use no special-function unit
-    assert bench.mufu_per_element("shuffle:4;exp") == 1
-    assert bench.mufu_per_element("relu;sigmoid") == 2
-    assert bench.mufu_per_element("exp;sigmoid;relu;mul") == 3
-    assert bench.mufu_per_element("cast:f32;scale:0.5;add;mul") == 0
+def test_mufu_clocks_of_a_chain():
+    # exp: one ex2 (1/32 SM-clock); sigmoid: one ex2 and one rcp (1/16); the
+    # prologue, scale constants, fast forms' names and the other ops add
+    # nothing of their own
+    assert bench.mufu_clocks_per_element("shuffle:4;exp") == 1 / 32
+    assert bench.mufu_clocks_per_element("relu;sigmoid") == 1 / 32 + 1 / 16
+    assert bench.mufu_clocks_per_element("exp:fast;sigmoid:fast;relu;mul") == 2 / 32 + 1 / 16
+    assert bench.mufu_clocks_per_element("cast:f32;scale:0.5;add;mul") == 0
 
 
 def test_cpu_all_cores_sample_uses_every_core():
