@@ -326,6 +326,20 @@ def test_detect_shapes(hw, dt):
     _detect_case(hw, dt, 11)
 
 
+@pytest.mark.parametrize("hw,dt,na,no", [
+    ([(16, 16), (8, 8), (4, 4)], F.F16, 3, 85),  # 32-byte vectors: 16 cells a warp
+    ([(8, 8), (4, 2)], F.F16, 3, 85),            # a plane of 8 cells: 16-byte vectors
+    ([(16, 16), (8, 8)], F.F32, 3, 85),
+    ([(24, 8)], F.BF16, 2, 6),
+    ([(16, 16)], F.F16, 1, 128),                 # four channels a lane
+    ([(4, 4), (2, 2)], F.F32, 4, 37),
+])
+def test_detect_other_heads_and_vector_planes(hw, dt, na, no):
+    """Planes of whole 16- and 32-byte input vectors, fp32 and bf16 inputs, and
+    heads of 6 to 128 outputs with one to four anchors."""
+    _detect_case(hw, dt, 21, na=na, no=no)
+
+
 def test_detect_unaligned_and_other_heads():
     _detect_case([(16, 16), (8, 8)], F.F16, 12, offset=1)
     _detect_case([(10, 12)], F.F16, 13, na=2, no=6)
