@@ -32,39 +32,40 @@ constexpr int NW = VEC * BYTES / 4;                  // words per half-vector
 constexpr int NWV = VV * BYTES / 4;                  // words per v-vector
 constexpr long long TOKEN_WORDS = 3LL * HEADS * HD * BYTES / 4;
 constexpr int HD_WORDS = HD * BYTES / 4;
-
 #if FUSE_ROPE_VEC
-extern "C" __global__ void __launch_bounds__(BLOCK)
-rope_vec(const void* qkv, void* q, void* k, void* v, const float* table, long long pos0,
-         long long tokens) {
-  // ask L2 for the token's qkv row before waiting for the previous kernel
-  // (programmatic dependent launch; L2 is coherent, the loads come after)
-  if constexpr (ROW_PREFETCH && (VEC * BYTES) % 16 == 0 && (VV * BYTES) % 16 == 0) {
-    if (threadIdx.x == 0)
-      prefetch_l2(static_cast<const u32*>(qkv) + blockIdx.x * TOKEN_WORDS,
-                  static_cast<unsigned>(TOKEN_WORDS * 4));
-  }
-  pdl_enter();
-  const long long t = blockIdx.x;
-  const u32* src = static_cast<const u32*>(qkv) + t * TOKEN_WORDS;
-  const float* tab = table + (pos0 + t) * (2 * HALF);
+__host__ __device__ constexpr int cmin(int x, int y) { return x < y ? x : y; }
+__host__ __device__ constexpr int cmax(int x, int y) { return x > y ? x : y; }
+// Items a thread holds in registers at once: up to about 48 words of q/k
+// operands (two half-vectors, their cosines and sines an item) and 16 words
+// of v.  Rows wider than one round's items per thread take several rounds
+// (a run-time loop), so neither registers nor the unrolled code grow with
+// the head count.
+constexpr int QB = cmin(NQK, cmax(1, 48 / (2 * NW + 2 * VEC)));
+constexpr int VB = cmin(NV, cmax(1, 16 / NWV));
+constexpr int ROUNDS = cmax((NQK + QB - 1) / QB, (NV + VB - 1) / VB);
 
-  // v: issue the loads first, store after the rotation
-  u32 vw[NV][NWV];
+// Round rd of a thread's work on token t: its v loads first, then the q/k
+// loads, the rotation and the q/k stores, then the v stores.  In the common
+// one-round case rd is the constant 0 and every bound check below whose
+// items divide evenly over the block folds away.
+__device__ __forceinline__ void rope_round(int rd, const u32* src, const float* tab, void* q, void* k,
+                                           void* v, long long t, long long tokens) {
+  constexpr bool V_EVEN = ROUNDS == 1 && V_ITEMS % BLOCK == 0;
+  constexpr bool QK_EVEN = ROUNDS == 1 && QK_ITEMS % BLOCK == 0;
+  u32 vw[VB][NWV];
 #pragma unroll
-  for (int n = 0; n < NV; ++n) {
-    const int it = threadIdx.x + n * BLOCK;
-    if (V_ITEMS % BLOCK == 0 || it < V_ITEMS) {
+  for (int n = 0; n < VB; ++n) {
+    const int it = threadIdx.x + (rd * VB + n) * BLOCK;
+    if (V_EVEN || it < V_ITEMS) {
       const int h = it / V_PER_ROW, j = it % V_PER_ROW;
       load_words(src + (2 * HEADS + h) * HD_WORDS + j * (NWV), vw[n]);
     }
   }
-  // q and k
-  u32 a[NQK][NW], b[NQK][NW], cw[NQK][VEC], sw[NQK][VEC];
+  u32 a[QB][NW], b[QB][NW], cw[QB][VEC], sw[QB][VEC];
 #pragma unroll
-  for (int n = 0; n < NQK; ++n) {
-    const int it = threadIdx.x + n * BLOCK;
-    if (QK_ITEMS % BLOCK == 0 || it < QK_ITEMS) {
+  for (int n = 0; n < QB; ++n) {
+    const int it = threadIdx.x + (rd * QB + n) * BLOCK;
+    if (QK_EVEN || it < QK_ITEMS) {
       const int row = it / QK_PER_ROW;  // which * HEADS + h
       const int i0 = (it % QK_PER_ROW) * VEC;
       const u32* r = src + row * HD_WORDS;
@@ -75,9 +76,9 @@ rope_vec(const void* qkv, void* q, void* k, void* v, const float* table, long lo
     }
   }
 #pragma unroll
-  for (int n = 0; n < NQK; ++n) {
-    const int it = threadIdx.x + n * BLOCK;
-    if (QK_ITEMS % BLOCK == 0 || it < QK_ITEMS) {
+  for (int n = 0; n < QB; ++n) {
+    const int it = threadIdx.x + (rd * QB + n) * BLOCK;
+    if (QK_EVEN || it < QK_ITEMS) {
       const int row = it / QK_PER_ROW;
       const int which = row / HEADS, h = row % HEADS;
       const int i0 = (it % QK_PER_ROW) * VEC;
@@ -98,12 +99,35 @@ rope_vec(const void* qkv, void* q, void* k, void* v, const float* table, long lo
     }
   }
 #pragma unroll
-  for (int n = 0; n < NV; ++n) {
-    const int it = threadIdx.x + n * BLOCK;
-    if (V_ITEMS % BLOCK == 0 || it < V_ITEMS) {
+  for (int n = 0; n < VB; ++n) {
+    const int it = threadIdx.x + (rd * VB + n) * BLOCK;
+    if (V_EVEN || it < V_ITEMS) {
       const int h = it / V_PER_ROW, j = it % V_PER_ROW;
       store_words(static_cast<u32*>(v) + (h * tokens + t) * HD_WORDS + j * NWV, vw[n]);
     }
+  }
+}
+
+extern "C" __global__ void __launch_bounds__(BLOCK)
+rope_vec(const void* qkv, void* q, void* k, void* v, const float* table, long long pos0,
+         long long tokens) {
+  // ask L2 for (the first 64 KB of) the token's qkv row before waiting for the
+  // previous kernel (programmatic dependent launch; L2 is coherent, the loads
+  // come after)
+  if constexpr (ROW_PREFETCH && (VEC * BYTES) % 16 == 0 && (VV * BYTES) % 16 == 0) {
+    if (threadIdx.x == 0)
+      prefetch_l2(static_cast<const u32*>(qkv) + blockIdx.x * TOKEN_WORDS,
+                  static_cast<unsigned>(TOKEN_WORDS * 4 < 65536 ? TOKEN_WORDS * 4 : 65536));
+  }
+  pdl_enter();
+  const long long t = blockIdx.x;
+  const u32* src = static_cast<const u32*>(qkv) + t * TOKEN_WORDS;
+  const float* tab = table + (pos0 + t) * (2 * HALF);
+  if constexpr (ROUNDS == 1) {
+    rope_round(0, src, tab, q, k, v, t, tokens);
+  } else {
+#pragma unroll 1
+    for (int rd = 0; rd < ROUNDS; ++rd) rope_round(rd, src, tab, q, k, v, t, tokens);
   }
 }
 

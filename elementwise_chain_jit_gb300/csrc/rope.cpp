@@ -146,6 +146,7 @@ extern "C" int rope_qkv_split(const void* qkv, void* q, void* k, void* v, int64_
   if (!valid_dtype(dt)) return fail(FUSE_E_DTYPE, fmt("invalid dtype %d", dt));
   if (tokens < 0 || heads < 1 || head_dim < 2 || head_dim > 1024 || head_dim % 2)
     return fail(FUSE_E_SHAPE, "need tokens >= 0, heads >= 1, head_dim even in 2..1024");
+  if (heads > (1 << 20) / head_dim) return fail(FUSE_E_SHAPE, "heads * head_dim above 2^20");
   if (tokens > 0x7fffffff) return fail(FUSE_E_SHAPE, "tokens above 2^31 - 1");
   if (pos0 < 0 || pos0 > kMaxPositions || tokens > kMaxPositions - pos0)
     return fail(FUSE_E_SHAPE, "positions must lie in [0, 2^22)");

@@ -365,6 +365,7 @@ extern "C" int rope_qkv_split_noalloc(const void* qkv, void* q, void* k, void* v
   if (!valid_dtype(dt)) return fail(FUSE_E_DTYPE, fmt("invalid dtype %d", dt));
   if (tokens < 0 || heads < 1 || head_dim < 2 || head_dim > 1024 || head_dim % 2)
     return fail(FUSE_E_SHAPE, "need tokens >= 0, heads >= 1, head_dim even in 2..1024");
+  if (heads > (1 << 20) / head_dim) return fail(FUSE_E_SHAPE, "heads * head_dim above 2^20");
   // (no product is formed before the operands are known to be small)
   if (tokens > kScratchFloats / head_dim)
     return fail(FUSE_E_SHAPE,

@@ -239,7 +239,8 @@ int layernorm_residual(const void* x, const void* residual, const void* gamma, c
  * library builds on the device in fp64 and keeps (fp32, 2 * positions *
  * head_dim/2 * 4 bytes) per device, base and head_dim; it grows as larger
  * positions are asked for.  dt: f16, bf16 or f32.  head_dim even,
- * 2 <= head_dim <= 1024; heads >= 1; 0 <= tokens <= 2^31 - 1; 0 <= pos0 and
+ * 2 <= head_dim <= 1024; heads >= 1 and heads * head_dim <= 2^20 (index
+ * arithmetic within a token's row is 32-bit); 0 <= tokens <= 2^31 - 1; 0 <= pos0 and
  * pos0 + tokens <= 2^22 (every position below 2^22); FUSE_E_SHAPE otherwise,
  * FUSE_E_ARG unless base is finite and > 1.  One kernel is compiled per
  * (heads, head_dim, dt) on first use; the token count and pos0 are launch

@@ -112,6 +112,8 @@ def test_rope_shapes_and_positions(noalloc):
     outside(call(hd=1026), E_SHAPE)
     outside(call(hd=63), E_SHAPE)
     outside(call(heads=0), E_SHAPE)
+    outside(call(heads=1025, hd=1024), E_SHAPE)  # heads * head_dim <= 2^20
+    outside(call(heads=(1 << 30), hd=1024), E_SHAPE)
     outside(call(tokens=-1), E_SHAPE)
     # every position below 2^22: pos0 + tokens <= 2^22
     outside(call(tokens=4, pos0=(1 << 22) - 3), E_SHAPE)
@@ -124,6 +126,7 @@ def test_rope_shapes_and_positions(noalloc):
     outside(call(tokens=1, pos0=(1 << 63) - 1), E_SHAPE)
     inside(call(tokens=4, pos0=(1 << 22) - 4))
     inside(call(hd=1024, tokens=2))
+    inside(call(heads=1024, hd=1024, tokens=2))
     inside(call(hd=2))
     if noalloc:
         # its fixed array: tokens * head_dim <= 2^20

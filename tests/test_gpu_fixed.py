@@ -207,6 +207,24 @@ def test_rope_shapes(tokens, heads, hd, pos0, dt):
     _rope_check(qkv, heads, hd, pos0, dt, *(to_host(o.t, dt) for o in outs))
 
 
+@pytest.mark.parametrize("tokens,heads,hd,pos0,dt", [
+    (4, 96, 128, 0, F.F16),        # 3 q/k items a thread: 3 rounds
+    (3, 160, 256, 5, F.F32),       # 20 rounds
+    (2, 1024, 1024, 11, F.BF16),   # the widest row the entry point takes: heads * head_dim = 2^20
+])
+def test_rope_wide_rows(tokens, heads, hd, pos0, dt):
+    """Rows with more q/k items than one round of a thread's registers holds
+    run in several rounds of the same kernel."""
+    qkv = workloads.normal((tokens, 3 * heads * hd), 0, 1, 3 * tokens + heads, dt)
+    qd = to_dev(qkv.reshape(-1), dt)
+    outs = [Guarded(heads * tokens * hd, dt) for _ in range(3)]
+    F.rope_qkv_split(qd, outs[0].t, outs[1].t, outs[2].t, heads, hd, pos0, 10000.0, dt,
+                     tokens=tokens)
+    torch.cuda.synchronize()
+    assert all(o.canary_ok() for o in outs)
+    _rope_check(qkv, heads, hd, pos0, dt, *(to_host(o.t, dt) for o in outs))
+
+
 def test_rope_unaligned_and_position_zero_identity():
     tokens, heads, hd, dt = 9, 4, 128, F.BF16
     qkv = workloads.normal((tokens, 3 * heads * hd), 0, 1, 77, dt)
