@@ -139,22 +139,63 @@ class ClockSampler:
 
 # Special-function unit (MUFU) work of a chain: exp is one ex2, sigmoid one
 # ex2 and one rcp (the generated code's exp and sigmoid, accurate or fast).
-# Measured on GB300 with independent chains of each instruction on every SM:
-# ex2.approx 9.48 T/s and rcp.approx 4.79 T/s, 30 and 15 per SM and clock at
-# 2.07 GHz over 152 SMs -- the rates of 32 and 16 per SM-clock at a clock 5 %
-# lower; twice Blackwell's documented 16 for ex2, the same for rcp.  An even mix
-# of the two runs at 20 per SM-clock: one unit, where an ex2 takes half the
-# issue slot of an rcp.  With the HBM bytes this gives two lower bounds on a
-# chain's time; chains heavy in the accurate exp and sigmoid can be bound by
-# instruction issue instead, which is not modelled here.
+# Rates per SM and clock: a probe of independent chains of each instruction
+# on every SM of a GB300 measured ex2.approx at 9.5-9.9 T/s and rcp.approx at
+# 4.8-5.0 T/s, 30-32 and 15-16 per SM-clock at 2.07 GHz: twice Blackwell's
+# documented 16 for ex2, the same for rcp; an even mix of the two ran at 20,
+# so they share one unit.  The floors take these at the sampled clock, or the
+# rates every bench run measures with the library's own chains (mufu_rates)
+# where those are higher, so that each floor stays a lower bound.
+# With the HBM bytes this gives two lower bounds on a chain's time; chains
+# heavy in the accurate exp and sigmoid can be bound by instruction issue
+# instead, which is not modelled here.
 EX2_PER_SM_CLK, RCP_PER_SM_CLK = 32, 16
 
 
-def mufu_clocks_per_element(spec):
-    """SM clocks of special-function unit work per element of a chain."""
+def mufu_ops_per_element(spec):
+    """(ex2, rcp) operations per element of a chain."""
     ops = [o.split(":")[0] for o in spec.split(";")]
     n_sig = ops.count("sigmoid")
-    return (ops.count("exp") + n_sig) / EX2_PER_SM_CLK + n_sig / RCP_PER_SM_CLK
+    return ops.count("exp") + n_sig, n_sig
+
+
+def mufu_floor_us(ops, rates):
+    """Time the unit needs for (ex2, rcp) operations at rates (per second)."""
+    return (ops[0] / rates["ex2_per_s"] + ops[1] / rates["rcp_per_s"]) * 1e6
+
+
+def nominal_mufu_rates(sms, mhz):
+    return {"ex2_per_s": EX2_PER_SM_CLK * sms * mhz * 1e6,
+            "rcp_per_s": RCP_PER_SM_CLK * sms * mhz * 1e6,
+            "source": f"{EX2_PER_SM_CLK} ex2 and {RCP_PER_SM_CLK} rcp per SM-clock at {mhz:.0f} MHz"}
+
+
+def mufu_rates(dev, sms, mhz):
+    """The special-function unit's ex2 and rcp rates, measured with the
+    library's own kernels: a chain of 256 exp:fast (a multiply and an ex2
+    each) and one of 128 sigmoid:fast (a multiply, an ex2, an add and an rcp)
+    over 2^22 fp32 elements that stay in L2, 10 launches of each replayed
+    from a graph.  The unit, not memory or issue, sets both times; the rcp
+    rate is what the second leaves after its ex2s."""
+    import torch
+
+    import elementwise_chain_jit_gb300 as F
+    import workloads as W
+    n = 1 << 22
+    x = W.device_uniform(n, -2.0, 2.0, 7, W.F32, dev)
+    y = torch.empty_like(x)
+    t = {}
+    for name, op, k in (("exp", "exp:fast", 256), ("sigmoid", "sigmoid:fast", 128)):
+        c = F.fuse_compile(";".join([op] * k), (n,), W.F32)
+        t[name] = graph_per_launch(lambda c=c: F.fuse_launch(c, [x], y), k=10) / 1e3  # seconds
+    ex2 = n * 256 / t["exp"]
+    left = t["sigmoid"] / (n * 128) - 1.0 / ex2
+    if left <= 0:
+        raise RuntimeError("sigmoid chain no slower than its ex2s alone")
+    rcp = 1.0 / left
+    return {"ex2_per_s": ex2, "rcp_per_s": rcp, "ex2_per_sm_clk": ex2 / (sms * mhz * 1e6),
+            "rcp_per_sm_clk": rcp / (sms * mhz * 1e6), "at_sm_mhz": mhz,
+            "source": "measured: 256 exp:fast and 128 sigmoid:fast over 2^22 fp32 in L2"}
 
 
 class Item:
@@ -167,7 +208,7 @@ class Item:
         self.inputs, self.outputs = [], []   # device tensors (for the end-to-end copies)
         # the same launch on other tensors of the same shapes (ins, outs)
         self.launch_on = None
-        self.mufu_clocks = 0.0   # SM clocks of special-function unit work
+        self.mufu_ops = None     # (ex2, rcp) special-function unit operations
 
 
 def _tdt(dt):
@@ -205,7 +246,8 @@ def build_items(dev, with_unfused=True, only=None, flat_elems=None, spec=None, s
         it = Item(name, nbytes, lambda: F.fuse_launch(c, ins, out), kernel=("chain", spec, shape, dt))
         it.inputs, it.outputs = ins, [out]
         it.launch_on = lambda i_s, o_s: F.fuse_launch(c, i_s, o_s[0])
-        it.mufu_clocks = n * mufu_clocks_per_element(spec)
+        e, r = mufu_ops_per_element(spec)
+        it.mufu_ops = (n * e, n * r) if e or r else None
         if with_unfused:
             it.unfused, it.n_unfused = unfused_chain(spec, dt, shape, ins, out)
         return it
@@ -452,7 +494,7 @@ def _rms_linear_item(dev, with_unfused, M=16384):
     return it
 
 
-def fast_math_row(dev, peak, peak_kind, mhz):
+def fast_math_row(dev, peak, peak_kind, rates):
     """The shuffle-prefixed 16-op chain (4 exp, 4 sigmoid) with its exp and
     sigmoid in the opt-in fast form (exp:fast, sigmoid:fast: ex2.approx on
     x * log2 e, validated against the oracle's bound for it) beside the
@@ -478,8 +520,8 @@ def fast_math_row(dev, peak, peak_kind, mhz):
         it.launch_on = lambda i_s, o_s, c=c: F.fuse_launch(c, i_s, o_s[0])
         out["us_" + tag] = steady_times(it, 60)[0]
         del it, ins, o
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    mufu_us = mufu_clocks_per_element(body) * n / (sms * mhz * 1e6) * 1e6
+    e, r = mufu_ops_per_element(body)
+    mufu_us = mufu_floor_us((n * e, n * r), rates)
     hbm_us = nb / (peak * 1e9) * 1e6
     out.update({"bytes": nb, "spec_fast": fast, "mufu_bound_us": mufu_us, "hbm_bound_us": hbm_us,
                 "bound": "mufu" if mufu_us > hbm_us else "hbm",
@@ -1138,6 +1180,22 @@ def run_gpu(args):
             print(f"pipeline attribution skipped: {e}", file=sys.stderr)
 
     peak, peak_kind = peaks()
+    # the special-function unit's rates, for the chains' second floor
+    mhz = clocks.summary().get("sm_mhz") or 2070.0
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    rates = nominal_mufu_rates(sms, mhz)
+    mufu_report = {"floor": rates}
+    if any(it.mufu_ops for it in items) or args.only is None or re.search(args.only, "fast_math"):
+        try:
+            measured = mufu_rates(dev, sms, mhz)
+            mufu_report["measured"] = measured
+            if measured["ex2_per_s"] > rates["ex2_per_s"] or measured["rcp_per_s"] > rates["rcp_per_s"]:
+                rates = {"ex2_per_s": max(rates["ex2_per_s"], measured["ex2_per_s"]),
+                         "rcp_per_s": max(rates["rcp_per_s"], measured["rcp_per_s"]),
+                         "source": "the larger of the per-clock rates and the measured ones"}
+                mufu_report["floor"] = rates
+        except Exception as e:  # the floors keep the per-clock rates
+            mufu_report["measured"] = {"error": str(e)[:200]}
     # unfused per-op sequences (outside the timed region)
     per_chain = {}
     for it, ems, ts in zip(items, per_item, per_step):
@@ -1179,12 +1237,10 @@ def run_gpu(args):
             copy_us = cold_time(_Copy, reps=40)
             d.update({"us_device_copy_cold_clean_l2": copy_us,
                       "frac_of_device_copy_cold": copy_us / cold_us})
-        if it.mufu_clocks:
+        if it.mufu_ops:
             # two rooflines: HBM bytes and special-function unit operations
-            # at the clock sampled during the timed region
-            mhz = clocks.summary().get("sm_mhz") or 2070.0
-            sms = torch.cuda.get_device_properties(dev).multi_processor_count
-            mufu_us = it.mufu_clocks / (sms * mhz * 1e6) * 1e6
+            # at the unit's rates measured in this run
+            mufu_us = mufu_floor_us(it.mufu_ops, rates)
             hbm_us = it.bytes / (peak * 1e9) * 1e6
             d.update({"mufu_bound_us": mufu_us, "hbm_bound_us": hbm_us,
                       "bound": "mufu" if mufu_us > hbm_us else "hbm",
@@ -1194,7 +1250,6 @@ def run_gpu(args):
         per_chain[it.name] = d
     # next rows, measured beside the step (not part of its workload)
     next_rows = {}
-    import re
     if args.only is None or re.search(args.only, f"layernorm_residual_{LN_ROWS[0]}x4096_bf16"):
         ln = _ln_item(dev, with_unfused=not args.no_unfused)
         st_us, st_per = steady_times(ln, 60)
@@ -1239,7 +1294,7 @@ def run_gpu(args):
         extras.append(("rope_qkv_split_noalloc", lambda: noalloc_row(dev, peak, peak_kind)))
     if args.only is None or re.search(args.only, "fast_math"):
         extras.append(("shuffle_chain_L16_fast_math", lambda: fast_math_row(
-            dev, peak, peak_kind, clocks.summary().get("sm_mhz") or 2070.0)))
+            dev, peak, peak_kind, rates)))
     for name, fn in extras:
         try:
             next_rows.update(fn())
@@ -1408,7 +1463,7 @@ def run_gpu(args):
                              f"{step_bytes / 1e9:.1f} GB, evicting the small workloads' buffers",
                        "storage_dtypes": "f32/f16/bf16 per workload, arithmetic in f32"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clk, "per_chain": per_chain,
+            "clocks": clk, "per_chain": per_chain, "mufu_rates": mufu_report,
             "per_chain_timing": "us_fused (gbs, frac_of_*_peak): the workload on its own, 60 "
                                 "launches (10 above 1 GB) back to back on rotating buffer sets "
                                 "that together exceed twice the L2, replayed from one graph, mean "

@@ -35,14 +35,22 @@ def test_reference_arm_prints_one_json_line(capsys):
     assert line["e2e"]["h2d_bytes_per_step"] == 0
 
 
-def test_mufu_clocks_of_a_chain():
-    # exp: one ex2 (1/32 SM-clock); sigmoid: one ex2 and one rcp (1/16); the
-    # prologue, scale constants, fast forms' names and the other ops add
-    # nothing of their own
-    assert bench.mufu_clocks_per_element("shuffle:4;exp") == 1 / 32
-    assert bench.mufu_clocks_per_element("relu;sigmoid") == 1 / 32 + 1 / 16
-    assert bench.mufu_clocks_per_element("exp:fast;sigmoid:fast;relu;mul") == 2 / 32 + 1 / 16
-    assert bench.mufu_clocks_per_element("cast:f32;scale:0.5;add;mul") == 0
+def test_mufu_operations_of_a_chain():
+    # exp: one ex2; sigmoid: one ex2 and one rcp; the prologue, scale
+    # constants, the fast forms' names and the other ops add nothing
+    assert bench.mufu_ops_per_element("shuffle:4;exp") == (1, 0)
+    assert bench.mufu_ops_per_element("relu;sigmoid") == (1, 1)
+    assert bench.mufu_ops_per_element("exp:fast;sigmoid:fast;relu;mul") == (2, 1)
+    assert bench.mufu_ops_per_element("cast:f32;scale:0.5;add;mul") == (0, 0)
+
+
+def test_mufu_floor_adds_the_two_instructions_at_their_rates():
+    rates = bench.nominal_mufu_rates(sms=152, mhz=2000.0)
+    assert rates["ex2_per_s"] == 32 * 152 * 2e9 and rates["rcp_per_s"] == 16 * 152 * 2e9
+    # 8 ex2 and 4 rcp per element, 2^20 elements: one SM-clock of unit time
+    # per 2 elements on each SM
+    us = bench.mufu_floor_us((8 << 20, 4 << 20), rates)
+    assert us == pytest.approx((1 << 20) * 0.5 / (152 * 2e9) * 1e6)
 
 
 def test_cpu_all_cores_sample_uses_every_core():
