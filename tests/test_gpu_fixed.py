@@ -376,3 +376,23 @@ def test_detect_sigmoid_zero_closed_form():
     assert np.all(o[:, 4:] == 0.5)
     assert o[0, 0] == 4.0 and o[0, 1] == 4.0 and o[0, 2] == anchors[0, 0, 0]
     assert o[3 * 64, 0] == 8.0  # first row of scale 1: (0.5 + 0) * 16
+
+
+# ------------------------------------------------------------ zero-size calls
+
+def test_zero_size_calls_launch_nothing_and_write_nothing():
+    """rows = 0, tokens = 0 and a batch of 0 are valid calls: they return
+    without a launch and leave every output byte as it was."""
+    dt = F.BF16
+    buf = [torch.full((4096,), 3.0, dtype=torch.bfloat16, device="cuda") for _ in range(6)]
+    before = [b.clone() for b in buf]
+    stats = F.fuse_stats()
+    F.rmsnorm_residual(buf[0], buf[1], buf[2], buf[3], buf[4], 1e-6, dt, rows=0, hidden=4096)
+    F.layernorm_residual(buf[0], buf[1], buf[2], buf[5], buf[3], buf[4], 1e-5, dt, rows=0,
+                         hidden=4096)
+    F.rope_qkv_split(buf[0], buf[3], buf[4], buf[5], 4, 128, 0, 10000.0, dt, tokens=0)
+    F.rope_qkv_split_noalloc(buf[0], buf[3], buf[4], buf[5], 4, 128, 0, 10000.0, dt, tokens=0)
+    F.channel_shuffle(buf[0], buf[3], 4, dt, shape=(0, 16, 8, 8))
+    torch.cuda.synchronize()
+    assert F.fuse_stats()["launches"] == stats["launches"]
+    assert all(torch.equal(a, b) for a, b in zip(buf, before))
