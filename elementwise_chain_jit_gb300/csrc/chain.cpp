@@ -15,6 +15,7 @@
 // and the scalar tail after its share of the main loop.
 #include <algorithm>
 #include <atomic>
+#include <cctype>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -149,6 +150,7 @@ struct ChainPlan {
   bool dynamic = false;  // shape bucket: the leading dimension comes with the launch
   bool debug = false;    // FUSE_DEBUG_BOUNDS: every index checked against its tensor
   bool prefetch = false;  // L2 prefetch of the first chunk before the launch-order wait
+  bool pack2 = false;     // add, mul and scale as packed fp32 pairs (f32x2)
   int64_t inner = 1;     // elements per unit of the leading dimension
   std::string source;
 };
@@ -231,6 +233,11 @@ int plan_chain(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_d
   // the bulk prefetch needs 16-byte aligned ranges: every tensor's vector a
   // multiple of 16 bytes (the vector kernel's pointers are 16-byte aligned)
   p->prefetch = env_int("FUSE_CHAIN_PREFETCH", 1) == 1 && p->vec * minb >= 16;
+  // two elements a step, add / mul / scale as one packed instruction each
+  // (FUSE_CHAIN_F32X2=0 turns it off)
+  bool arith = false;
+  for (auto& op : p->ch.ops) arith = arith || op.op == OP_ADD || op.op == OP_MUL || op.op == OP_SCALE;
+  p->pack2 = env_int("FUSE_CHAIN_F32X2", 1) == 1 && p->vec % 2 == 0 && arith;
   return FUSE_OK;
 }
 
@@ -262,6 +269,39 @@ static void emit_op(std::ostringstream& s, const ChainOp& op, const std::string&
       else if (op.to == FUSE_BF16) s << "      x = round_bf16(x);\n";
       else s << "      /* cast:f32 keeps the fp32 value */\n";
       break;
+  }
+}
+
+// the same op on a pair of elements x0, x1 (operands elem0 / elem1)
+static void emit_op2(std::ostringstream& s, const ChainOp& op, const std::string& elem0,
+                     const std::string& elem1) {
+  switch (op.op) {
+    case OP_ADD:
+      s << "      add2(x0, x1, " << operand(elem0, op.input) << ", " << operand(elem1, op.input)
+        << ");\n";
+      break;
+    case OP_MUL:
+      s << "      mul2(x0, x1, " << operand(elem0, op.input) << ", " << operand(elem1, op.input)
+        << ");\n";
+      break;
+    case OP_SCALE:
+      s << "      mul2(x0, x1, " << hex_float(op.c) << ", " << hex_float(op.c) << ");\n";
+      break;
+    default: {
+      std::ostringstream one;
+      emit_op(one, op, elem0);
+      std::string t = one.str(), a, b;
+      for (size_t i = 0; i < t.size(); ++i) {
+        // the scalar statement on x, once for each element of the pair
+        const bool var = t[i] == 'x' && (i == 0 || !isalnum(static_cast<unsigned char>(t[i - 1])) &&
+                                                      t[i - 1] != '_') &&
+                         (i + 1 == t.size() || !isalnum(static_cast<unsigned char>(t[i + 1])) &&
+                                                   t[i + 1] != '_');
+        a += var ? std::string("x0") : std::string(1, t[i]);
+        b += var ? std::string("x1") : std::string(1, t[i]);
+      }
+      s << a << b;
+    }
   }
 }
 
@@ -344,6 +384,11 @@ static std::string gen_chain_source(const ChainPlan& p, const char* spec) {
   if (p.copy) {
     s << "  static_assert(NWO == NW0, \"copy\");\n"
          "#pragma unroll\n  for (int i = 0; i < NWO; ++i) wo[i] = w0[i];\n}\n";
+  } else if (p.pack2) {
+    s << "  float y[VEC];\n#pragma unroll\n  for (int e = 0; e < VEC; e += 2) {\n";
+    s << "      float x0 = get_elem<DT0>(w0, e), x1 = get_elem<DT0>(w0, e + 1);\n";
+    for (auto& op : ch.ops) emit_op2(s, op, "get_elem<DT@>(w@, e)", "get_elem<DT@>(w@, e + 1)");
+    s << "      y[e] = x0;\n      y[e + 1] = x1;\n  }\n  pack_vec<DTO>(y, wo);\n}\n";
   } else {
     s << "  float y[VEC];\n#pragma unroll\n  for (int e = 0; e < VEC; ++e) {\n";
     s << "      float x = get_elem<DT0>(w0, e);\n";

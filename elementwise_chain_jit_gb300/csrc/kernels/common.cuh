@@ -67,6 +67,25 @@ __device__ __forceinline__ float exp_fast(float x) {
 }
 __device__ __forceinline__ float sigmoid_fast(float x) { return rcp_ge1(1.0f + exp_fast(-x)); }
 
+// Packed fp32 pairs (sm_100 and later): one instruction adds or multiplies two
+// lanes, each rounded to nearest even without flushing, the same bits as two
+// scalar operations.  Inline asm, so the compiler does not contract them into
+// fused multiply-adds.
+__device__ __forceinline__ void add2(float& a, float& b, float c, float d) {
+  unsigned long long x, y;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(c), "f"(d));
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(y));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+}
+__device__ __forceinline__ void mul2(float& a, float& b, float c, float d) {
+  unsigned long long x, y;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(c), "f"(d));
+  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(y));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+}
+
 __device__ __forceinline__ float round_f16(float x) { return f16_to_f32(f32_to_f16(x)); }
 __device__ __forceinline__ float round_bf16(float x) { return bf16_to_f32(f32_to_bf16(x)); }
 
