@@ -150,7 +150,7 @@ struct ChainPlan {
   bool dynamic = false;  // shape bucket: the leading dimension comes with the launch
   bool debug = false;    // FUSE_DEBUG_BOUNDS: every index checked against its tensor
   bool prefetch = false;  // L2 prefetch of the first chunk before the launch-order wait
-  bool pack2 = false;     // add, mul and scale as packed fp32 pairs (f32x2)
+  bool pack2 = false;     // adds and multiplies as packed fp32 pairs (f32x2)
   int64_t inner = 1;     // elements per unit of the leading dimension
   std::string source;
 };
@@ -233,10 +233,14 @@ int plan_chain(const char* spec, const int64_t* shape, int ndim, fuse_dtype in_d
   // the bulk prefetch needs 16-byte aligned ranges: every tensor's vector a
   // multiple of 16 bytes (the vector kernel's pointers are 16-byte aligned)
   p->prefetch = env_int("FUSE_CHAIN_PREFETCH", 1) == 1 && p->vec * minb >= 16;
-  // two elements a step, add / mul / scale as one packed instruction each
-  // (FUSE_CHAIN_F32X2=0 turns it off)
+  // two elements a step, the adds and multiplies of add / mul / scale and of
+  // the fast forms as one packed instruction each (FUSE_CHAIN_F32X2=0 turns
+  // it off).  The accurate sigmoid stays per element: pairing its add made
+  // the 16-op shuffle chain slower (64.0 against 61.6 us on GB300).
   bool arith = false;
-  for (auto& op : p->ch.ops) arith = arith || op.op == OP_ADD || op.op == OP_MUL || op.op == OP_SCALE;
+  for (auto& op : p->ch.ops)
+    arith = arith || op.op == OP_ADD || op.op == OP_MUL || op.op == OP_SCALE ||
+            op.op == OP_EXP_FAST || op.op == OP_SIGMOID_FAST;
   p->pack2 = env_int("FUSE_CHAIN_F32X2", 1) == 1 && p->vec % 2 == 0 && arith;
   return FUSE_OK;
 }
@@ -287,6 +291,8 @@ static void emit_op2(std::ostringstream& s, const ChainOp& op, const std::string
     case OP_SCALE:
       s << "      mul2(x0, x1, " << hex_float(op.c) << ", " << hex_float(op.c) << ");\n";
       break;
+    case OP_EXP_FAST: s << "      exp_fast2(x0, x1);\n"; break;
+    case OP_SIGMOID_FAST: s << "      sigmoid_fast2(x0, x1);\n"; break;
     default: {
       std::ostringstream one;
       emit_op(one, op, elem0);

@@ -86,6 +86,26 @@ __device__ __forceinline__ void mul2(float& a, float& b, float c, float d) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
 }
 
+// exp_fast and sigmoid_fast on a pair, their adds and multiplies packed:
+// each lane gets the bits of the scalar function
+__device__ __forceinline__ float ex2_ftz(float t) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+  return r;
+}
+__device__ __forceinline__ void exp_fast2(float& a, float& b) {
+  mul2(a, b, 1.44269502162933349609375f, 1.44269502162933349609375f);
+  a = ex2_ftz(a);
+  b = ex2_ftz(b);
+}
+__device__ __forceinline__ void sigmoid_fast2(float& a, float& b) {
+  mul2(a, b, -1.44269502162933349609375f, -1.44269502162933349609375f);
+  float ea = ex2_ftz(a), eb = ex2_ftz(b);
+  add2(ea, eb, 1.0f, 1.0f);
+  a = rcp_ge1(ea);
+  b = rcp_ge1(eb);
+}
+
 __device__ __forceinline__ float round_f16(float x) { return f16_to_f32(f32_to_f16(x)); }
 __device__ __forceinline__ float round_bf16(float x) { return bf16_to_f32(f32_to_bf16(x)); }
 
