@@ -72,3 +72,17 @@ def test_link_bound_takes_the_slower_direction():
     # two ranks move twice the bytes in the same time
     assert bench.link_bound(step, 2, h2d, d2h, {"h2d": 210.0, "d2h": 193.0}) == \
         pytest.approx(2 * fast)
+
+
+def test_traffic_record_matches_the_dominant_kernel_as_it_is():
+    """profiles/traffic.txt holds the ncu DRAM traffic of the step's dominant
+    kernel under that kernel's source hash; the bench reports it only while
+    the hash matches.  A changed chain generator or common header shows here,
+    before a GPU run, as a record to capture again."""
+    import workloads as W
+    spec, dt = W.random_chain(32, 5)
+
+    class Item:
+        kernel = ("chain", spec, (W.FLAT_SIZES[-1],), dt)
+    name = f"flat_chain_L32_n{W.FLAT_SIZES[-1]}"
+    assert bench.traffic_record(name, bench.kernel_source_hash(Item)) is not None
