@@ -1410,10 +1410,10 @@ def run_gpu(args):
         e2e_step()
         torch.cuda.synchronize()
         # the host side of the copies varies from second to second on a shared
-        # node (118-182 ms for the same step, back to back): three timed runs
+        # node (115-182 ms for the same step, back to back): five timed runs
         # of e2e_steps steps each, the median reported, every run listed
         runs = []
-        for _ in range(3):
+        for _ in range(5):
             barrier()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
