@@ -358,7 +358,14 @@ const char* fuse_last_error(void);
  * its tensor before the access and record code 3 in the device error word,
  * skipping the access, instead of touching memory outside the tensors),
  * FUSE_PDL=0 (launch in plain stream order instead of with programmatic
- * dependent launch; read once per process). */
+ * dependent launch; read once per process).  Switches of the generated code,
+ * read when a kernel is generated (FUSE_ROW_PREFETCH once per process) and so
+ * part of its source and cache key: FUSE_CHAIN_PREFETCH=0 (no L2 prefetch of a chain CTA's first chunk
+ * before the launch-order wait), FUSE_ROW_PREFETCH=0 (the same for the first
+ * row of RMSNorm, LayerNorm and RoPE), FUSE_CHAIN_F32X2=0 (chains do their
+ * adds and multiplies one element at a time instead of on packed fp32
+ * pairs), FUSE_DETECT_TC and FUSE_DETECT_BLOCK (the detect decode's cells per
+ * tile and threads per CTA), FUSE_LN_MAX_REGS (LayerNorm's register cap). */
 int fuse_stats(int64_t* compiles, int64_t* cache_hits, int64_t* launches, double* compile_ms);
 
 /* Number of SMs the library sizes persistent grids for on the current
