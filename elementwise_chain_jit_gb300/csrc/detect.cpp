@@ -100,7 +100,7 @@ int detect_kernel(const int* hw, const float* strides, const float* anchors, int
   s << "}\n\n";
   for (const char* v : {"vec", "scalar"})
     s << "extern \"C\" __global__ void __launch_bounds__(BLOCK) detect_" << v
-      << "(const Feats f, float* out) {\n  pdl_enter();\n  __shared__ float tile[TC * NO];\n  dispatch<"
+      << "(const Feats f, float* out) {\n  pdl_enter();\n  __shared__ __align__(16) float tile[TC * NO];\n  dispatch<"
       << (v[0] == 'v' ? "true" : "false") << ">(f, out, tile);\n}\n";
   if (cta > 0x7fffffff) return fail(FUSE_E_SHAPE, "too many tiles");
   k.grid = static_cast<unsigned>(cta);

@@ -81,11 +81,22 @@ __device__ __forceinline__ void tile_work(const void* feat, float* out, int a, i
                          : total;
     const int body = (total - head) / 4;
     if (threadIdx.x < head) dst[threadIdx.x] = tile[threadIdx.x];
-    for (int i = threadIdx.x; i < body; i += BLOCK) {
-      u32 w[4];
+    if (head == 0) {
+      // the tile is 16-byte aligned: one 16-byte shared load a store
+      const float4* t4 = reinterpret_cast<const float4*>(tile);
+      for (int i = threadIdx.x; i < body; i += BLOCK) {
+        const float4 v = t4[i];
+        const u32 w[4] = {__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
+                          __float_as_uint(v.w)};
+        st_words16(reinterpret_cast<u32*>(dst) + 4 * i, w);
+      }
+    } else {
+      for (int i = threadIdx.x; i < body; i += BLOCK) {
+        u32 w[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) w[e] = __float_as_uint(tile[head + 4 * i + e]);
-      st_words16(reinterpret_cast<u32*>(dst + head) + 4 * i, w);
+        for (int e = 0; e < 4; ++e) w[e] = __float_as_uint(tile[head + 4 * i + e]);
+        st_words16(reinterpret_cast<u32*>(dst + head) + 4 * i, w);
+      }
     }
     for (int i = head + 4 * body + threadIdx.x; i < total; i += BLOCK) dst[i] = tile[i];
   } else {
