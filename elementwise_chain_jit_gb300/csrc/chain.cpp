@@ -544,7 +544,7 @@ static void chain_grids(const ChainPlan& p, const fuse_chain::PerDevice& pd, int
   const int64_t want = (n + 255) / 256;
   *scalar_grid = static_cast<unsigned>(std::max<int64_t>(
       1, std::min<int64_t>(want, int64_t(pd.sms) * std::max(pd.occ_scalar, 1))));
-  const int per_sm = env_int("FUSE_CHAIN_CTAS_PER_SM", 0);
+  static const int per_sm = env_int("FUSE_CHAIN_CTAS_PER_SM", 0);  // read once
   const int64_t nfull = (n / p.vec) / (int64_t(p.block) * p.unroll);
   int64_t cap = int64_t(1) << 30;
   if (per_sm > 0) cap = int64_t(pd.sms) * std::min(per_sm, std::max(pd.occ_vec, 1));
@@ -609,7 +609,7 @@ int chain_launch(fuse_chain* h, const void* const* inputs, int n_in, void* outpu
   if (int rc = chain_device_state(h, d, &pd)) return rc;
   // kernel parameter: the Args struct {in[NIN], out[, n][, err]} as 8-byte
   // words (the debug build always has n, then the device error word)
-  std::vector<uint64_t> args(static_cast<size_t>(nin) + 3);
+  uint64_t args[kMaxInputs + 3];  // on the stack: no allocation per launch
   for (int j = 0; j < nin; ++j) args[j] = reinterpret_cast<uintptr_t>(inputs[j]);
   args[nin] = reinterpret_cast<uintptr_t>(output);
   args[nin + 1] = static_cast<uint64_t>(n);
@@ -618,7 +618,7 @@ int chain_launch(fuse_chain* h, const void* const* inputs, int n_in, void* outpu
     if (int rc = device_error_word(d.ordinal, &err)) return rc;
     args[nin + 2] = static_cast<uint64_t>(err);
   }
-  void* kargs[] = {args.data()};
+  void* kargs[] = {args};
   unsigned vec_grid, scalar_grid;
   chain_grids(p, *pd, n, &vec_grid, &scalar_grid);
   // 32-byte accesses need 32-byte alignment when a vector spans 32 bytes
