@@ -159,6 +159,10 @@ class Chain:
         fuse_launch(self, inputs, output, stream)
         return output
 
+    def bind(self, inputs, output) -> "BoundLaunch":
+        """This chain on these tensors, for launching again and again."""
+        return BoundLaunch(self, inputs, output)
+
     def release(self):
         if self.handle:
             fuse_release(self)
@@ -175,6 +179,28 @@ def fuse_compile(spec: str, shape, in_dtype) -> Chain:
 def fuse_launch(chain: Chain, inputs, output, stream=None) -> None:
     ptrs = (_P * max(1, len(inputs)))(*[_ptr(t) for t in inputs])
     _check(_lib.fuse_launch(chain.handle, ptrs, len(inputs), _ptr(output), _stream(stream)))
+
+
+class BoundLaunch:
+    """A chain bound to fixed input and output tensors: the pointer array is
+    built once, so each call only hands it to fuse_launch (for serving loops
+    that launch the same chain on the same buffers step after step).  It holds
+    references to the tensors, so they stay allocated while it lives."""
+
+    __slots__ = ("_fn", "_h", "_ptrs", "_n", "_out", "_keep")
+
+    def __init__(self, chain: Chain, inputs, output):
+        self._fn = _lib.fuse_launch
+        self._h = chain.handle
+        self._n = len(inputs)
+        self._ptrs = (_P * max(1, self._n))(*[_ptr(t) for t in inputs])
+        self._out = _ptr(output)
+        self._keep = (chain, list(inputs), output)
+
+    def __call__(self, stream=None) -> None:
+        rc = self._fn(self._h, self._ptrs, self._n, self._out, _stream(stream))
+        if rc:
+            _check(rc)
 
 
 def fuse_release(chain: Chain) -> None:

@@ -46,6 +46,28 @@ def test_add_relu_scale_bit_exact(n, offset):
     assert np.array_equal(got, oracle.store(want, F.F32))
 
 
+def test_bound_launch_runs_the_chain_on_its_tensors():
+    """Chain.bind: the same chain on the same tensors step after step, with
+    new input values each step, bit-exact against the oracle's closed form."""
+    cfg = workloads.ADD_RELU_SCALE
+    n = (1 << 20) + 7
+    c = F.fuse_compile(cfg["spec"], (n,), F.F32)
+    a_t = torch.empty(n, dtype=torch.float32, device="cuda")
+    b_t = torch.empty_like(a_t)
+    out = Guarded(n, F.F32)
+    step = c.bind([a_t, b_t], out.t)
+    for k in range(3):
+        a = workloads.uniform(n, cfg["lo"], cfg["hi"], 50 + k, F.F32)
+        b = workloads.uniform(n, cfg["lo"], cfg["hi"], 60 + k, F.F32)
+        a_t.copy_(torch.from_numpy(a))
+        b_t.copy_(torch.from_numpy(b))
+        step()
+        torch.cuda.synchronize()
+        assert out.canary_ok()
+        want, _ = oracle.chain_eval(cfg["spec"], F.F32, [a, b], (n,))
+        assert np.array_equal(to_host(out.t, F.F32), oracle.store(want, F.F32))
+
+
 def test_add_relu_scale_golden_on_device():
     import os
     path = os.path.join(os.path.dirname(__file__), "golden", "add_relu_scale.txt")

@@ -225,3 +225,15 @@ def test_detect_decoder_checks_the_feature_count():
     dec = F.DetectDecoder([(8, 8), (4, 4)], [8, 16], [[[1, 2]] * 3] * 2, 3, 85, F.F16)
     with pytest.raises(ValueError):
         dec([256], 256, stream=0)
+
+
+@pytest.mark.skipif(not NO_GPU, reason="checks the no-device error path")
+def test_bound_launch_reaches_the_device_step():
+    c = F.fuse_compile("add;relu;scale:0.5", (1024,), F.F32)
+    step = c.bind([256, 512], 768)
+    with pytest.raises(F.FuseError) as e:
+        step()
+    assert e.value.code == -7  # validated, then no driver
+    with pytest.raises(F.FuseError) as e:
+        c.bind([256], 768)()   # one input where the chain takes two
+    assert e.value.code == -8  # FUSE_E_ARG, before any device step
