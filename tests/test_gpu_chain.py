@@ -68,6 +68,22 @@ def test_bound_launch_runs_the_chain_on_its_tensors():
         assert np.array_equal(to_host(out.t, F.F32), oracle.store(want, F.F32))
 
 
+def test_longest_and_widest_chain():
+    """The engine's limits at once: 1024 ops and 128 input tensors (127 adds),
+    over the vector body, the remainder and the scalar tail, against the
+    oracle.  Every exp follows a sigmoid, so the values stay bounded and the
+    running error bound decides every element."""
+    group = ["add", "sigmoid", "relu", "scale:0.75", "exp", "sigmoid", "scale:1.5", "relu"]
+    tail = ["sigmoid", "exp", "relu", "scale:0.5", "sigmoid", "exp", "scale:0.25", "relu"]
+    ops = group * 127 + tail
+    spec = ";".join(ops)
+    n = 4099
+    inputs, _ = workloads.chain_inputs(spec, F.F32, n, 77)
+    got, c = _run_chain(spec, F.F32, inputs, (n,))
+    assert len(ops) == 1024 and c.n_in == 128
+    _check(spec, F.F32, inputs, (n,), got)
+
+
 def test_add_relu_scale_golden_on_device():
     import os
     path = os.path.join(os.path.dirname(__file__), "golden", "add_relu_scale.txt")
