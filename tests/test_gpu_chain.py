@@ -270,7 +270,7 @@ def test_shuffle_chain_full_config(length):
 
 @pytest.mark.parametrize("shape,groups,dt", [
     ((32, 256, 56, 56), 4, F.F16), ((2, 24, 5, 7), 3, F.F16), ((4, 8, 16, 16), 2, F.F32),
-    ((1, 64, 9, 9), 8, F.BF16), ((2, 6, 1, 1), 6, F.F16),
+    ((1, 64, 9, 9), 8, F.BF16), ((2, 6, 1, 1), 6, F.F16), ((3, 16, 4, 4), 1, F.F16),
 ])
 def test_channel_shuffle_bit_exact(shape, groups, dt):
     x = workloads.uniform(shape, -2, 2, 17, dt)
