@@ -193,7 +193,7 @@ def _rope_check(qkv_host, heads, hd, pos0, dt, got_q, got_k, got_v, tokens_idx=N
 
 @pytest.mark.parametrize("tokens,heads,hd,pos0", [
     (5, 4, 128, 0), (37, 3, 64, 32000), (8, 2, 80, 7), (3, 1, 6, 100), (16, 32, 128, 32752),
-    (2, 2, 256, 1_000_000),
+    (2, 2, 256, 1_000_000), (4, 3, 2, 5),  # head_dim 2: one rotation pair
 ])
 @pytest.mark.parametrize("dt", [F.BF16, F.F16, F.F32])
 def test_rope_shapes(tokens, heads, hd, pos0, dt):
