@@ -254,6 +254,39 @@ def test_detect_logit_recovers_source_index():
                         assert code[key] == (s, a * 85 + k, y, x)
 
 
+def test_detect_box_outputs_follow_the_class_outputs():
+    # every channel of a cell carries the same logit, so the cell's box
+    # outputs and its class outputs share one p, which the class outputs give
+    # (pinned on their own above); then x / stride - grid_x + 0.5 = 2p,
+    # likewise for y, and w / anchor_w = h / anchor_h = (2p)^2 -- away from
+    # p = 1/2, where the zero-logit closed form cannot tell (2p)^2 from 2p
+    hw = [(2, 3), (1, 2), (1, 1)]
+    strides = [8.0, 16.0, 32.0]
+    logits = [-3.0, -1.0, 0.5, 2.0, 1.25, -0.75]
+    feats = []
+    for s, (h, w) in enumerate(hw):
+        vals = np.zeros((1, 255, h, w))
+        for y in range(h):
+            for x in range(w):
+                vals[0, :, y, x] = logits[(s + y * w + x) % len(logits)]
+        feats.append(oracle.store(vals, oracle.F16))
+    anc = _anchors()
+    out, _ = oracle.detect_decode(feats, oracle.F16, strides, anc, 3, 85)
+    row = 0
+    for s, (h, w) in enumerate(hw):
+        for a in range(3):
+            for y in range(h):
+                for x in range(w):
+                    p = out[row, 4]
+                    assert np.all(out[row, 4:] == p) and 0.0 < p < 1.0 and p != 0.5
+                    two_p = 2.0 * p
+                    assert out[row, 0] / strides[s] - x + 0.5 == pytest.approx(two_p, rel=1e-12)
+                    assert out[row, 1] / strides[s] - y + 0.5 == pytest.approx(two_p, rel=1e-12)
+                    assert out[row, 2] / anc[s, a, 0] == pytest.approx(two_p ** 2, rel=1e-12)
+                    assert out[row, 3] / anc[s, a, 1] == pytest.approx(two_p ** 2, rel=1e-12)
+                    row += 1
+
+
 def test_detect_concat_offsets_full_shapes():
     hw = [(80, 80), (40, 40), (20, 20)]
     rows = [3 * h * w for h, w in hw]
