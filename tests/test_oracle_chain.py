@@ -171,9 +171,10 @@ def _fast_exp(x, skew):
     return np.where(np.abs(y) < np.float32(2.0 ** -126), np.float32(0), y)
 
 
-def _simulate_fp32_device(spec, in_dtype, inputs, shape, groups=0, fast_skew=2.4 * 2.0 ** -24):
+def _simulate_fp32_device(spec, in_dtype, inputs, shape, groups=0, fast_skew=2.4 * 2.0 ** -24,
+                          exp_skew=0.0):
     """A model of an fp32 device: every step rounds to fp32 once (exp and the
-    sigmoid's exp evaluated in binary64 then rounded, i.e. within 1/2 ulp);
+    sigmoid's exp evaluated in binary64, times (1 + exp_skew), then rounded);
     the fast variants through _fast_exp with a relative skew of fast_skew (the
     largest error the hardware 2^t was measured to make is 2.45 * 2^-24)."""
     ch = oracle.parse_spec(spec, in_dtype)
@@ -193,7 +194,7 @@ def _simulate_fp32_device(spec, in_dtype, inputs, shape, groups=0, fast_skew=2.4
             elif op == oracle.OP_RELU:
                 x = np.where(x > 0, x, np.float32(0))
             elif op == oracle.OP_EXP:
-                x = np.exp(x.astype(np.float64)).astype(np.float32)
+                x = (np.exp(x.astype(np.float64)) * (1 + exp_skew)).astype(np.float32)
             elif op == oracle.OP_SIGMOID:
                 e = np.exp(-x.astype(np.float64)).astype(np.float32)
                 x = np.float32(1) / (np.float32(1) + e)
@@ -221,6 +222,23 @@ def test_check_accepts_an_fp32_device(length, seed):
     fails, counts, _ = oracle.chain_check(spec, dt, inputs, (4099,), dev)
     assert fails == 0, (spec, counts)
     assert counts[3] == 0, (spec, counts)  # none unpinned
+
+
+@pytest.mark.parametrize("skew", [3.9 * 2.0 ** -24, -3.9 * 2.0 ** -24])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_check_accepts_an_exp_at_its_documented_error(skew, seed):
+    """CUDA documents expf to 2 ulp (4u relative): a device whose exp is off
+    by nearly that much everywhere must pass, including where it moves a
+    later fp16 cast across a rounding midpoint (the bound's exp term, not the
+    flat tolerance, decides those)."""
+    spec = "exp;cast:f16;add;exp;scale:0.375;cast:f16;mul;exp;cast:f16"
+    dt = oracle.F16
+    n = 1 << 16
+    inputs, _ = workloads.chain_inputs(spec, dt, n, 90 + seed)
+    dev = _simulate_fp32_device(spec, dt, inputs, (n,), exp_skew=skew)
+    fails, counts, _ = oracle.chain_check(spec, dt, inputs, (n,), dev)
+    assert fails == 0, counts
+    assert counts[3] == 0, counts
 
 
 def test_check_rejects_perturbed_results():

@@ -1,7 +1,8 @@
 """The oracle's pins catch plausible mistakes in it.
 
 Each case plants one mistake (a dropped term, a wrong sign, index or
-divisor, a swapped operand) in a copy of oracle.c, compiles the copy to a
+divisor, a swapped operand, a bound too tight for the device's documented
+error) in a copy of oracle.c, compiles the copy to a
 library of its own in a temporary directory, and runs the CPU pins with the
 oracle loading that library (ORACLE_LIB).  At least one pin must fail; the
 committed oracle.c is never touched.
@@ -48,6 +49,24 @@ MUTATIONS = [
     ("chain scale ignored", "case OP_SCALE: return x * c;", "case OP_SCALE: return x;"),
     ("shuffle direction", "int64_t co = j * groups + i, ci = i * cpg + j;",
      "int64_t co = i * cpg + j, ci = j * groups + i;"),
+    ("rmsnorm residual out is x", "      res_out[r * hidden + k] = hk;\n",
+     "      res_out[r * hidden + k] = load_elem(x, dt, r * hidden + k);\n"),
+    ("layernorm beta dropped", "      double b = beta ? load_elem(beta, dt, k) : 0.0;",
+     "      double b = 0.0;"),
+    ("rope v from the k block", "        int64_t src = ((t * 3 + which) * heads + h) * (int64_t)D;",
+     "        int64_t src = ((t * 3 + (which == 2 ? 1 : which)) * heads + h) * (int64_t)D;"),
+    ("detect anchor w and h swapped",
+     "              o = (2.0 * p) * (2.0 * p) * anchors[(s * na + a) * 2 + 0];",
+     "              o = (2.0 * p) * (2.0 * p) * anchors[(s * na + a) * 2 + 1];"),
+    ("detect channels anchor-minor", "            int64_t src = ((int64_t)(a * no + k) * H + y) * W + x;",
+     "            int64_t src = ((int64_t)(k * na + a) * H + y) * W + x;"),
+    ("rmsnorm-linear bias dropped", "      out[i * N + n] = (double)scale * (acc + b);",
+     "      out[i * N + n] = (double)scale * acc;"),
+    ("chain check without the exp's own error",
+     "      En = vn * expm1(E) + 4 * U32 * exp(v + E) + ETA;", "      En = vn * expm1(E) + ETA;"),
+    ("chain check with 1u for the exp",
+     "      En = vn * expm1(E) + 4 * U32 * exp(v + E) + ETA;",
+     "      En = vn * expm1(E) + 1 * U32 * exp(v + E) + ETA;"),
 ]
 
 
