@@ -172,9 +172,10 @@ def _fast_exp(x, skew):
 
 
 def _simulate_fp32_device(spec, in_dtype, inputs, shape, groups=0, fast_skew=2.4 * 2.0 ** -24,
-                          exp_skew=0.0):
+                          exp_skew=0.0, rcp_skew=0.0):
     """A model of an fp32 device: every step rounds to fp32 once (exp and the
-    sigmoid's exp evaluated in binary64, times (1 + exp_skew), then rounded);
+    sigmoid's exp evaluated in binary64, times (1 + exp_skew), then rounded;
+    the sigmoid's reciprocal likewise times (1 + rcp_skew));
     the fast variants through _fast_exp with a relative skew of fast_skew (the
     largest error the hardware 2^t was measured to make is 2.45 * 2^-24)."""
     ch = oracle.parse_spec(spec, in_dtype)
@@ -196,8 +197,9 @@ def _simulate_fp32_device(spec, in_dtype, inputs, shape, groups=0, fast_skew=2.4
             elif op == oracle.OP_EXP:
                 x = (np.exp(x.astype(np.float64)) * (1 + exp_skew)).astype(np.float32)
             elif op == oracle.OP_SIGMOID:
-                e = np.exp(-x.astype(np.float64)).astype(np.float32)
-                x = np.float32(1) / (np.float32(1) + e)
+                e = (np.exp(-x.astype(np.float64)) * (1 + exp_skew)).astype(np.float32)
+                d = (np.float32(1) + e).astype(np.float64)
+                x = (1.0 / d * (1 + rcp_skew)).astype(np.float32)
             elif op == oracle.OP_EXP_FAST:
                 x = _fast_exp(x, fast_skew)
             elif op == oracle.OP_SIGMOID_FAST:
@@ -236,6 +238,24 @@ def test_check_accepts_an_exp_at_its_documented_error(skew, seed):
     n = 1 << 16
     inputs, _ = workloads.chain_inputs(spec, dt, n, 90 + seed)
     dev = _simulate_fp32_device(spec, dt, inputs, (n,), exp_skew=skew)
+    fails, counts, _ = oracle.chain_check(spec, dt, inputs, (n,), dev)
+    assert fails == 0, counts
+    assert counts[3] == 0, counts
+
+
+@pytest.mark.parametrize("skew", [1.0, -1.0])
+def test_check_accepts_a_sigmoid_at_its_documented_error(skew):
+    """The accurate sigmoid is expf (2 ulp), an add and rcp.approx (1 ulp, 1.65u
+    measured): a device off by 3.9u in the exp and 1.6u in the reciprocal,
+    both the same way, must pass.  The fp16 cast after the sigmoid, amplified
+    by exp(16 x), turns every midpoint the device's error can cross into an
+    element the flat tolerance cannot decide and the bound must."""
+    spec = "sigmoid;cast:f16;cast:f32;scale:16;exp"
+    dt = oracle.F32
+    n = 1 << 16
+    inputs, _ = workloads.chain_inputs(spec, dt, n, 95)
+    dev = _simulate_fp32_device(spec, dt, inputs, (n,), exp_skew=-skew * 3.9 * 2.0 ** -24,
+                                rcp_skew=skew * 1.6 * 2.0 ** -24)
     fails, counts, _ = oracle.chain_check(spec, dt, inputs, (n,), dev)
     assert fails == 0, counts
     assert counts[3] == 0, counts

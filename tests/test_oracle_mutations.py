@@ -64,6 +64,8 @@ MUTATIONS = [
      "      out[i * N + n] = (double)scale * acc;"),
     ("chain check without the exp's own error",
      "      En = vn * expm1(E) + 4 * U32 * exp(v + E) + ETA;", "      En = vn * expm1(E) + ETA;"),
+    ("chain check with 3u for the sigmoid",
+     "const double c = op == OP_SIGMOID ? 10.0 :", "const double c = op == OP_SIGMOID ? 3.0 :"),
     ("chain check with 1u for the exp",
      "      En = vn * expm1(E) + 4 * U32 * exp(v + E) + ETA;",
      "      En = vn * expm1(E) + 1 * U32 * exp(v + E) + ETA;"),
